@@ -1,0 +1,468 @@
+"""Benchmark of tile-elementwise streaming on GB300.
+
+One step = one ``tsx_ewise`` call: the whole path (tile loads through the
+S-stage mbarrier ring, the shared-memory elementwise stage, the TMA stores)
+over the workload's tensors.  Default workload: fp32 fma over three
+[128, 1048576] tensors (box 8x128 = four 8x32 TMA loads per operand, 4
+stages), the largest stated configuration (2 GiB moved per step).
+
+Prints one JSON line (rank 0).  Metric: HBM GB/s = (n_in + 1) * rows * cols *
+element size / device time, i.e. algorithmic bytes read plus written.
+
+    python bench.py [--steps K] [--warmup W] [--workload NAME] [--stages S]
+                    [--variant tma|tma_rank3|ldgsts|sync] [--impl reference]
+
+``--impl reference`` times the CPU oracle (the only reference there is) on
+bounded samples of the same workload, one sample per step.  Under torchrun
+with N > 1 every rank runs an independent replica (the path has no exchange
+step); only timing is reduced across ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import tsx_inputs as ti  # noqa: E402
+
+METRIC = "pipelined tile-ewise HBM GB/s (read+write) and % of GB300 peak/memcpy ceiling"
+DEFAULT_WORKLOAD = "fma_128x1048576_f32"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DTYPE_NAME = {"f32": "f32", "f16": "f16", "bf16": "bf16"}
+KERNEL_SOURCES = ["pipelined_elementwise_streaming_gb300/csrc/k_tma.cu",
+                  "pipelined_elementwise_streaming_gb300/csrc/tsx_device.cuh",
+                  "pipelined_elementwise_streaming_gb300/csrc/tsx_internal.h"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ti.WORKLOADS))
+    p.add_argument("--stages", type=int, default=None, help="default: the workload's last stated stage count")
+    p.add_argument("--variant", default=None, help="default: the workload's variant")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as td
+
+    if world > 1 and not td.is_initialized():
+        td.init_process_group(backend=backend)
+    return td if world > 1 else None
+
+
+def aggregate(td, seconds: float, units: float):
+    """(max seconds over ranks, sum of units over ranks)."""
+    if td is None:
+        return seconds, units
+    import torch
+
+    dev = "cuda" if td.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    td.all_reduce(u, op=td.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(td):
+    if td is not None:
+        td.barrier()
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, variant: str, stages: int):
+    """DRAM bytes per launch from the committed ncu summary of this kernel
+    and workload, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"tma_ewise_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_sources_sha256_16") != source_digest():
+        return None
+    if fields.get("variant") != variant or fields.get("stages") != str(stages):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        time.sleep(0.6)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self):
+        return time.monotonic()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons, n = [], None, set(), 0
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            n += 1
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# --------------------------------------------------------------- our path
+
+def to_host_tensors(w, torch):
+    """The workload's inputs as pinned host tensors of the element type."""
+    out = []
+    for bits in w.inputs():
+        if w.dtype == "f32":
+            t = torch.from_numpy(bits.view(np.float32))
+        else:
+            t = torch.from_numpy(bits.view(np.int16)).view(torch.float16 if w.dtype == "f16" else torch.bfloat16)
+        out.append(t.pin_memory())
+    return out
+
+
+def memcpy_ceiling(torch, nbytes=1 << 30, reps=20):
+    """Device-to-device copy GB/s (read + write counted), median of reps."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    for _ in range(3):
+        dst.copy_(src)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src)
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    del src, dst
+    return 2 * nbytes / statistics.median(times) / 1e9
+
+
+def run_ours(args, w, stages, variant):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    td = init_dist(world, "nccl")
+    import pipelined_elementwise_streaming_gb300 as tsx
+
+    host = to_host_tensors(w, torch)
+    dev_in = [h.to("cuda", non_blocking=False) for h in host]
+    out = torch.empty_like(dev_in[0])
+    plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant)
+    info = plan.info(w.op)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))
+    po = out.data_ptr()
+    small = w.algorithmic_bytes < 4 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
+
+    ceiling = memcpy_ceiling(torch)
+
+    def step():
+        plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], po, sh)
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if plan.status() != tsx.TSX_OK:
+        raise RuntimeError("device-side wait gave up during warm-up")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(td)
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    region0.record(stream)
+    for k in range(K):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize()
+    barrier(td)
+    t_wall1 = time.monotonic()
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    if plan.status() != tsx.TSX_OK:
+        raise RuntimeError("device-side wait gave up in the timed region")
+
+    launch_s = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    kernel_total = sum(launch_s)
+    region_s = region0.elapsed_time(region1) / 1e3
+    step_s = kernel_total if small else region_s   # with flushes, only the kernels are counted
+    max_s, total_bytes = aggregate(td, step_s, float(w.algorithmic_bytes) * K)
+    value = total_bytes / max_s / 1e9
+    avg_launch = kernel_total / K
+    achieved = w.algorithmic_bytes / avg_launch / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end: pinned host inputs in, host result out, every step
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    E = max(1, args.e2e_steps)
+    for _ in range(2):
+        for h, d in zip(host, dev_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(td)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        for h, d in zip(host, dev_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s, e2e_bytes = aggregate(td, e0.elapsed_time(e1) / 1e3, float(w.algorithmic_bytes) * E)
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = host_out.numel() * host_out.element_size()
+    plan.close()
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_s / K * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": DTYPE_NAME[w.dtype],
+        "data": "synthetic (seeded SplitMix64 inputs, the workload's stated distribution)",
+        "config": {
+            "workload": w.name, "op": w.op, "rows": w.rows, "cols": w.cols, "box": [w.box_rows, w.box_cols],
+            "stages": stages, "variant": variant, "threads": info["threads"], "grid": info["grid"],
+            "ctas_per_sm": info["ctas_per_sm"], "loads_per_operand": info["loads_per_operand"],
+            "algorithmic_bytes_per_step": w.algorithmic_bytes,
+            "l2": "L2 flushed between timed steps (kernel time only)" if small
+                  else f"inputs larger than L2 ({w.algorithmic_bytes >> 20} MiB moved per step vs 129 MiB L2), "
+                       "steps back to back",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "memcpy_ceiling_gbs": round(ceiling, 1),
+        "frac_of_memcpy_ceiling": round(value / world / ceiling, 4),
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "steps": E,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K,
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+            "traffic": recorded_traffic(w.name, variant, stages),
+            "kernel": f"tma_ewise<{w.dtype},{w.op}>" if variant.startswith("tma") else f"{variant}_ewise",
+            "median_launch_ms": round(statistics.median(launch_s) * 1e3, 5),
+        },
+    }
+    return result, td, rank
+
+
+# ------------------------------------------------------------ the oracle
+
+def cpu_time_oracle(w, seconds_budget, start_row=0, max_rows=None):
+    """Run the oracle over row bands of the workload until the budget is
+    spent or the rows run out.  Returns (bytes, seconds, rows, cores)."""
+    import oracle
+
+    oracle.build()
+    rows_done, spent, nbytes = 0, 0.0, 0
+    band = max(1, min(w.rows, (1 << 22) // w.cols or 1))
+    r = start_row
+    limit = w.rows if max_rows is None else min(w.rows, start_row + max_rows)
+    while r < limit and spent < seconds_budget:
+        r1 = min(limit, r + band)
+        idx = np.arange(r * w.cols, r1 * w.cols, dtype=np.uint64)
+        ins = w.inputs_at(idx)
+        t0 = time.perf_counter()
+        oracle.ewise(w.op, w.dtype, *ins)
+        spent += time.perf_counter() - t0
+        nbytes += (w.n_in + 1) * idx.size * ti.ELEM_SIZE[w.dtype]
+        rows_done += r1 - r
+        r = r1
+    return nbytes, spent, rows_done, 1
+
+
+def cpu_baseline(w, seconds):
+    nbytes, spent, rows, cores = cpu_time_oracle(w, seconds)
+    return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of {w.name} ({rows * w.cols} elements), single-threaded C oracle, "
+                      f"{spent:.1f} s of CPU time"}
+
+
+def run_reference(args, w, stages, variant):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    K, W = args.steps, args.warmup
+    # size each step so the whole run stays within about a minute
+    per_step_budget = max(1e-3, 60.0 / max(1, K + W))
+    import oracle
+
+    oracle.build()
+    probe = np.arange(0, min(w.elems, 1 << 16), dtype=np.uint64)
+    ins = w.inputs_at(probe)
+    t0 = time.perf_counter()
+    oracle.ewise(w.op, w.dtype, *ins)
+    per_elem = (time.perf_counter() - t0) / probe.size
+    n = int(max(1024, min(w.elems, per_step_budget / max(per_elem, 1e-10))))
+    rng = np.random.default_rng(0)
+    total_bytes, total_s = 0, 0.0
+    for k in range(W + K):
+        start = int(rng.integers(0, max(1, w.elems - n)))
+        idx = np.arange(start, start + n, dtype=np.uint64)
+        x = w.inputs_at(idx)
+        t0 = time.perf_counter()
+        oracle.ewise(w.op, w.dtype, *x)
+        dt = time.perf_counter() - t0
+        if k >= W:
+            total_s += dt
+            total_bytes += (w.n_in + 1) * n * ti.ELEM_SIZE[w.dtype]
+    value = total_bytes / total_s / 1e9
+    sample = f"{n} contiguous elements of {w.name} per step (random offset), single-threaded C oracle"
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(total_s / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype], "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "rows": w.rows, "cols": w.cols,
+                   "box": [w.box_rows, w.box_cols], "stages": stages, "variant": variant},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    w = ti.WORKLOADS[args.workload]
+    stages = args.stages if args.stages is not None else w.stages[-1]
+    variant = args.variant or w.variant
+    if args.impl == "reference":
+        res = run_reference(args, w, stages, variant)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    res, td, rank = run_ours(args, w, stages, variant)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    barrier(td)
+    if td is not None:
+        td.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

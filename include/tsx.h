@@ -1,0 +1,175 @@
+/*
+ * tsx.h -- tile-elementwise streaming on NVIDIA GB300 (sm_103a).
+ *
+ * One operation: stream a dense row-major 2-D tensor [rows, cols] tile by
+ * tile from global into shared memory through an S-stage circular buffer
+ * whose stages are guarded by mbarriers, apply an elementwise op to each
+ * staged tile in shared memory, and write the result tile back to global.
+ *
+ * Sources for the operation (cited by page title and section):
+ *  - TVM docs "copy_async -> tma": one elected thread issues a
+ *    descriptor-driven bulk tensor copy; the descriptor is encoded once on
+ *    the host; completion is signalled on the caller's mbarrier
+ *    (introduction, "Demonstration program", "Algorithm" steps 2-4).
+ *  - TVM docs "elementwise -> smem": the op is applied to operands that all
+ *    live in shared memory under an [outer, threads, vec] partition
+ *    ("Algorithm", "Generated CUDA").
+ *  - nvFuser PR #2833 "Add TMA support for circular buffering pass": the
+ *    pre-prologue / prologue / main / epilogue / post-epilogue loops, box
+ *    dimensions of at most 256, and expect_tx = bytes per load x loads per
+ *    stage ("Lowering Details", "Loop Structure", "Detailed Pseudo-Code").
+ *  - TVM docs "copy_async -> ldgsts": the cp.async variant kept as an
+ *    ablation ("Algorithm", table under "How inputs change the algorithm").
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are CUDA device (or managed) addresses on the device
+ *    that was current when the plan was created.  The caller owns every
+ *    buffer and keeps it alive until the work queued on the stream is done.
+ *  - Tensors are dense and row-major: element (r, c) sits at byte offset
+ *    (r * cols + c) * element_size from the base pointer.
+ *  - Functions returning int return a tsx_status (0 = TSX_OK, negative =
+ *    error).  On an error nothing was queued on the stream, and
+ *    tsx_last_error() describes it.
+ *  - A plan may be used by one host thread at a time; different plans are
+ *    independent.
+ */
+#ifndef TSX_H
+#define TSX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  Arithmetic on 16-bit types is carried out in fp32 and
+ * rounded once to nearest-even into the element type (fma: one rounding of
+ * the exact a * b + c). */
+typedef enum { TSX_F16 = 0, TSX_BF16 = 1, TSX_F32 = 2 } tsx_dtype;
+
+/* How stages are filled.
+ *  TSX_TMA       one elected thread issues cp.async.bulk.tensor loads (one
+ *                rank-2 box per 128-byte atom of a tile row and per <= 256-row
+ *                chunk) completing on the stage's mbarrier; the result goes
+ *                back with cp.async.bulk.tensor stores.  The primary path.
+ *  TSX_LDGSTS    every thread issues cp.async (LDGSTS) copies of 16, 8 or 4
+ *                bytes; commit_group / wait_group per stage; the result is
+ *                written with vector stores.  Ablation.
+ *  TSX_SYNC      plain synchronous vector loads into shared memory, one
+ *                stage; ablation (stages is ignored beyond validation).
+ *  TSX_TMA_RANK3 as TSX_TMA, but one rank-3 box covers all 128-byte atoms of
+ *                a row chunk ("copy_async -> tma", "Generated TIRx IR");
+ *                needs cols to be a whole number of atoms. */
+typedef enum { TSX_TMA = 0, TSX_LDGSTS = 1, TSX_SYNC = 2, TSX_TMA_RANK3 = 3 } tsx_variant;
+
+/* Elementwise ops ("elementwise -> smem", table under "How inputs change
+ * the algorithm").  copy moves bits unchanged; sqrt and add/mul/fma are
+ * correctly rounded; exp is within 2 ulp (fp32) or 1 ulp (fp16, bf16) of the
+ * exact value. */
+typedef enum { TSX_COPY = 0, TSX_SQRT = 1, TSX_EXP = 2, TSX_ADD = 3, TSX_MUL = 4, TSX_FMA = 5 } tsx_op;
+
+typedef enum {
+    TSX_OK = 0,
+    TSX_ERR_INVALID = -1,     /* bad handle, op, shape, NULL / extra operand */
+    TSX_ERR_UNSUPPORTED = -2, /* no legal plan for this shape / variant ("declines") */
+    TSX_ERR_ALIGN = -3,       /* a base pointer is not aligned as the variant needs */
+    TSX_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
+    TSX_ERR_TIMEOUT = -5,     /* a device-side wait gave up (see tsx_plan_status) */
+    TSX_ERR_NOMEM = -6        /* host or device allocation failed */
+} tsx_status;
+
+/* A CUDA stream: the same type as cudaStream_t (pass 0 for the legacy
+ * default stream). */
+struct CUstream_st;
+typedef struct CUstream_st *tsx_stream_t;
+
+typedef struct tsx_plan *tsx_plan_t;
+
+/* Everything the planner decided, as plain numbers (see tsx_plan_query). */
+typedef struct tsx_plan_info {
+    int32_t dtype, variant, op, n_in, elem_size;
+    int32_t box_rows, box_cols, stages;
+    int64_t rows, cols, tiles, tiles_r, tiles_c;
+    /* TMA box split ("Lowering Details"): loads per operand and stage, and
+     * the expect_tx byte count of one stage = n_in * loads * bytes_per_load */
+    int32_t inner_elems, inner_bytes, atoms, rows_per_load, row_chunks;
+    int32_t loads_per_operand, bytes_per_load, tx_bytes;
+    /* tensor-map encode arguments, innermost dimension first */
+    int32_t rank;
+    uint64_t global_dim[5];
+    uint64_t global_stride_bytes[4];
+    uint32_t box_dim[5];
+    uint32_t element_strides[5];
+    int32_t interleave, swizzle, l2_promotion, oob_fill; /* CUtensorMap* enum values */
+    /* [outer, threads, vec] of the shared-memory elementwise stage, in
+     * elements of the element type (vec = 16 bytes); copy_vec_bytes is the
+     * width of one cp.async / vector copy for TSX_LDGSTS and TSX_SYNC */
+    int32_t threads, vec, outer, copy_vec_bytes;
+    /* shared memory: one operand's slot, one stage, the whole CTA */
+    int32_t slot_bytes, stage_bytes;
+    int32_t smem_bytes;
+    /* launch (0 from tsx_plan_query, which does not look at a GPU) */
+    int32_t ctas_per_sm, grid, sm_count;
+} tsx_plan_info;
+
+/* Create a plan for [rows, cols] tensors of `dtype`, streamed in stage
+ * tiles of box_rows x box_cols through `stages` stages by `variant`.
+ * Binds the plan to the current CUDA device and allocates one 4-byte device
+ * status word.  rows or cols may be 0 (every call is then a no-op).
+ * Limits: rows, cols < 2^31; 1 <= stages <= 16; box dims >= 1; TMA variants
+ * need cols * element_size to be a multiple of 16 bytes and a tile row of a
+ * whole number of 16-byte units (and of 128-byte atoms when wider than one).
+ * Returns NULL on failure (tsx_last_error() says why). */
+tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols,
+                           int stages, tsx_variant variant);
+
+/* out = op(a, b, c) element by element over the plan's [rows, cols].
+ * a is required; b is required by add / mul / fma and must be NULL
+ * otherwise; c is required by fma and must be NULL otherwise (else
+ * TSX_ERR_INVALID).  out may be exactly a, b or c; any other overlap is
+ * undefined.  For an empty tensor (rows or cols 0) the call does nothing
+ * and the pointers are not examined.  Base pointers must be 16-byte aligned
+ * for the TMA variants;
+ * TSX_LDGSTS / TSX_SYNC narrow their copy width to the pointers' alignment
+ * (16, 8 or 4 bytes) and return TSX_ERR_ALIGN below 4.
+ * Asynchronous on `stream`: returns once the kernel is queued.  A device-side
+ * wait that exceeds its time limit (default 1 s, env TSX_TIMEOUT_MS) makes
+ * the kernel record TSX_ERR_TIMEOUT in the plan's status word and return;
+ * read it with tsx_plan_status.  With env TSX_CHECKED=1 the call
+ * synchronizes the stream and returns the device status instead. */
+int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, void *out,
+              tsx_stream_t stream);
+
+/* Release the plan, its tensor-map cache and its device status word.
+ * NULL is ignored.  Work already queued must not need the plan's status
+ * word afterwards (synchronize first). */
+void tsx_plan_destroy(tsx_plan_t plan);
+
+/* The first device-side error recorded by this plan's kernels since the
+ * last call (TSX_OK if none), then clears it.  Call after synchronizing the
+ * streams the plan was used on; this call itself blocks on a small
+ * device-to-host copy. */
+int tsx_plan_status(tsx_plan_t plan);
+
+/* Message for the last error on the calling host thread ("" if none).  The
+ * pointer stays valid until the next tsx_* call on this thread. */
+const char *tsx_last_error(void);
+
+/* The plan tsx_plan_create would build and the launch tsx_ewise would make
+ * for `op`, computed on the host alone: no CUDA call, no GPU needed
+ * (ctas_per_sm, grid and sm_count are left 0).  Base pointers are assumed
+ * 16-byte aligned.  Returns TSX_OK and fills *info, or the error
+ * tsx_plan_create / tsx_ewise would return. */
+int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
+                   tsx_variant variant, tsx_op op, tsx_plan_info *info);
+
+/* tsx_plan_query for an existing plan, including the launch it makes on its
+ * device (occupancy-derived CTAs per SM and grid). */
+int tsx_plan_get_info(tsx_plan_t plan, tsx_op op, tsx_plan_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSX_H */

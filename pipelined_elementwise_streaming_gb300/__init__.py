@@ -1,0 +1,186 @@
+"""Python binding of libtsx: tile-elementwise streaming on GB300.
+
+Argument marshalling only: every step of the path runs in the CUDA library
+``libtsx.so`` (built from ``csrc/`` by ``_build.py``).  There is no Python or
+CPU fallback; importing this module fails loudly when the library is absent.
+
+The C functions are exposed under their own names (``tsx_plan_create``,
+``tsx_ewise``, ``tsx_plan_destroy``, ``tsx_plan_status``, ``tsx_last_error``,
+``tsx_plan_query``, ``tsx_plan_get_info``) with plain-integer arguments;
+``Plan`` wraps them for torch tensors::
+
+    plan = Plan("bf16", rows, cols, box=(128, 128), stages=4, variant="tma")
+    plan.ewise("exp", a, out=out)          # a, out: CUDA tensors, [rows, cols]
+
+PyTorch only supplies device memory and the current stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtsx.so")
+
+DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
+VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3}
+OPS = {"copy": 0, "sqrt": 1, "exp": 2, "add": 3, "mul": 4, "fma": 5}
+ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
+STATUS = {0: "TSX_OK", -1: "TSX_ERR_INVALID", -2: "TSX_ERR_UNSUPPORTED", -3: "TSX_ERR_ALIGN",
+          -4: "TSX_ERR_CUDA", -5: "TSX_ERR_TIMEOUT", -6: "TSX_ERR_NOMEM"}
+TSX_OK, TSX_ERR_INVALID, TSX_ERR_UNSUPPORTED, TSX_ERR_ALIGN, TSX_ERR_CUDA, TSX_ERR_TIMEOUT, TSX_ERR_NOMEM = \
+    0, -1, -2, -3, -4, -5, -6
+
+
+class TsxError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS.get(code, code)}: {message}")
+        self.code = code
+
+
+class tsx_plan_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("dtype", "variant", "op", "n_in", "elem_size",
+                                               "box_rows", "box_cols", "stages")] + \
+               [(n, ctypes.c_int64) for n in ("rows", "cols", "tiles", "tiles_r", "tiles_c")] + \
+               [(n, ctypes.c_int32) for n in ("inner_elems", "inner_bytes", "atoms", "rows_per_load",
+                                               "row_chunks", "loads_per_operand", "bytes_per_load",
+                                               "tx_bytes", "rank")] + \
+               [("global_dim", ctypes.c_uint64 * 5), ("global_stride_bytes", ctypes.c_uint64 * 4),
+                ("box_dim", ctypes.c_uint32 * 5), ("element_strides", ctypes.c_uint32 * 5)] + \
+               [(n, ctypes.c_int32) for n in ("interleave", "swizzle", "l2_promotion", "oob_fill",
+                                               "threads", "vec", "outer", "copy_vec_bytes",
+                                               "slot_bytes", "stage_bytes", "smem_bytes",
+                                               "ctas_per_sm", "grid", "sm_count")]
+
+    def as_dict(self) -> dict:
+        d = {}
+        for name, _ in self._fields_:
+            v = getattr(self, name)
+            d[name] = list(v) if hasattr(v, "__len__") else int(v)
+        return d
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                          "(libtsx is the only implementation; there is no fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    L.tsx_plan_create.restype = ctypes.c_void_p
+    L.tsx_plan_create.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_int]
+    L.tsx_ewise.restype = ctypes.c_int
+    L.tsx_ewise.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5
+    L.tsx_plan_destroy.restype = None
+    L.tsx_plan_destroy.argtypes = [ctypes.c_void_p]
+    L.tsx_plan_status.restype = ctypes.c_int
+    L.tsx_plan_status.argtypes = [ctypes.c_void_p]
+    L.tsx_last_error.restype = ctypes.c_char_p
+    L.tsx_last_error.argtypes = []
+    L.tsx_plan_query.restype = ctypes.c_int
+    L.tsx_plan_query.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
+    L.tsx_plan_get_info.restype = ctypes.c_int
+    L.tsx_plan_get_info.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
+    return L
+
+
+lib = _load()
+
+# The C entry points under their own names (plain integers / addresses).
+tsx_plan_create = lib.tsx_plan_create
+tsx_ewise = lib.tsx_ewise
+tsx_plan_destroy = lib.tsx_plan_destroy
+tsx_plan_status = lib.tsx_plan_status
+tsx_plan_query = lib.tsx_plan_query
+tsx_plan_get_info = lib.tsx_plan_get_info
+
+
+def tsx_last_error() -> str:
+    return lib.tsx_last_error().decode()
+
+
+def _code(table: dict, key) -> int:
+    return table[key] if isinstance(key, str) else int(key)
+
+
+def query(dtype, rows, cols, box, stages, variant="tma", op="copy") -> dict:
+    """The plan and launch shape the library would use (host only, no GPU)."""
+    info = tsx_plan_info()
+    rc = tsx_plan_query(_code(DTYPES, dtype), rows, cols, box[0], box[1], stages, _code(VARIANTS, variant),
+                        _code(OPS, op), ctypes.byref(info))
+    if rc != TSX_OK:
+        raise TsxError(rc, tsx_last_error())
+    return info.as_dict()
+
+
+_TORCH_DTYPE_NAME = {"torch.float16": "f16", "torch.bfloat16": "bf16", "torch.float32": "f32"}
+
+
+class Plan:
+    """A tsx plan bound to the current CUDA device."""
+
+    def __init__(self, dtype: str, rows: int, cols: int, box=(32, 32), stages: int = 2, variant: str = "tma"):
+        self.dtype, self.rows, self.cols = dtype, int(rows), int(cols)
+        self.box, self.stages, self.variant = (int(box[0]), int(box[1])), int(stages), variant
+        h = tsx_plan_create(_code(DTYPES, dtype), self.rows, self.cols, self.box[0], self.box[1], self.stages,
+                            _code(VARIANTS, variant))
+        if not h:
+            raise TsxError(TSX_ERR_UNSUPPORTED, tsx_last_error())
+        self.handle = h
+
+    def _check(self, t, name):
+        if t is None:
+            return None
+        if not t.is_cuda:
+            raise TsxError(TSX_ERR_INVALID, f"{name} must be a CUDA tensor")
+        if _TORCH_DTYPE_NAME.get(str(t.dtype)) != self.dtype:
+            raise TsxError(TSX_ERR_INVALID, f"{name} has dtype {t.dtype}, the plan is {self.dtype}")
+        if t.numel() != self.rows * self.cols or not t.is_contiguous():
+            raise TsxError(TSX_ERR_INVALID, f"{name} must be a contiguous [{self.rows}, {self.cols}] tensor")
+        return t.data_ptr()
+
+    def ewise_ptr(self, op, a: int, b: int | None, c: int | None, out: int, stream: int = 0) -> None:
+        """tsx_ewise on raw device addresses (an int stream handle)."""
+        rc = tsx_ewise(self.handle, _code(OPS, op), a, b, c, out, stream)
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+
+    def ewise(self, op: str, a, b=None, c=None, out=None, stream=None):
+        """out = op(a[, b[, c]]) on the current (or given) torch CUDA stream."""
+        import torch
+
+        if out is None:
+            out = torch.empty_like(a)
+        pa, pb, pc, po = (self._check(a, "a"), self._check(b, "b"), self._check(c, "c"), self._check(out, "out"))
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        self.ewise_ptr(op, pa, pb, pc, po, s.cuda_stream)
+        return out
+
+    def status(self) -> int:
+        """Device-side status since the last call (reads and clears it)."""
+        return tsx_plan_status(self.handle)
+
+    def info(self, op: str = "copy") -> dict:
+        info = tsx_plan_info()
+        rc = tsx_plan_get_info(self.handle, _code(OPS, op), ctypes.byref(info))
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+        return info.as_dict()
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            tsx_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

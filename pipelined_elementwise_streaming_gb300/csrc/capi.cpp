@@ -1,0 +1,410 @@
+// The C ABI of libtsx (include/tsx.h): plans, tensor maps, launches and the
+// device status word.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "plan.h"
+
+namespace tsx {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int set_error(int rc, const std::string& msg)
+{
+    g_last_error = msg;
+    return rc;
+}
+
+int cuda_error(cudaError_t e, const char* what)
+{
+    return set_error(TSX_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+int64_t env_i64(const char* name, int64_t fallback)
+{
+    const char* v = std::getenv(name);
+    if (!v || !*v)
+        return fallback;
+    return std::strtoll(v, nullptr, 10);
+}
+
+// cuTensorMapEncodeTiled, looked up through the runtime so that the library
+// does not link against the driver library (it then loads on machines
+// without a GPU, where only tsx_plan_query is usable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(std::string* why)
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    static std::string err;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            err = std::string("cuTensorMapEncodeTiled is unavailable: ") + cudaGetErrorString(e);
+        else
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn && why)
+        *why = err;
+    return fn;
+}
+
+CUtensorMapDataType map_dtype(int dtype)
+{
+    return dtype == TSX_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+         : dtype == TSX_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+}  // namespace
+
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+}  // namespace tsx
+
+using namespace tsx;
+
+struct tsx_plan {
+    Geometry g;
+    int device = 0;
+    int sm_count = 0;
+    int max_smem = 0;
+    int* d_status = nullptr;
+    uint64_t timeout_ns = 1000000000ull;
+    int64_t fault_tile = -1;
+    bool checked = false;
+    int ctas_per_sm_cap = 0;
+
+    struct OpLaunch {
+        bool ready = false;
+        OpGeometry og;
+        int ctas_per_sm = 0;
+        int grid = 0;
+    } ops[6];
+
+    // tensor maps, keyed by base pointer (the shape is the plan's)
+    struct MapEntry {
+        const void* ptr = nullptr;
+        uint64_t used = 0;
+        alignas(64) CUtensorMap map;
+    } maps[8];
+    uint64_t clock = 0;
+};
+
+namespace {
+
+const void* kernel_of(int variant, int dtype, int op)
+{
+    if (variant == TSX_LDGSTS)
+        return ldgsts_kernel(dtype, op);
+    if (variant == TSX_SYNC)
+        return sync_kernel(dtype, op);
+    return tma_kernel(dtype, op);
+}
+
+// Geometry, kernel attributes, occupancy and grid for one op (cached).
+int prepare_op(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
+{
+    tsx_plan::OpLaunch& L = p->ops[op];
+    if (!L.ready) {
+        std::string why;
+        const int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
+        if (rc != TSX_OK)
+            return set_error(rc, why);
+        const void* fn = kernel_of(p->g.variant, p->g.dtype, op);
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.og.smem_bytes));
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaFuncSetAttribute");
+        int blocks = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, p->g.threads, L.og.smem_bytes);
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (blocks < 1)
+            return set_error(TSX_ERR_UNSUPPORTED, "the kernel cannot be resident with this shared memory / threads");
+        if (p->ctas_per_sm_cap > 0 && blocks > p->ctas_per_sm_cap)
+            blocks = p->ctas_per_sm_cap;
+        L.ctas_per_sm = blocks;
+        // persistent grid: every resident CTA slot once, no more CTAs than tiles
+        const int64_t slots = int64_t(p->sm_count) * blocks;
+        L.grid = int(p->g.tiles < slots ? p->g.tiles : slots);
+        L.ready = true;
+    }
+    *out = &L;
+    return TSX_OK;
+}
+
+int encode_map(tsx_plan* p, const void* ptr, CUtensorMap* map)
+{
+    std::string why;
+    EncodeTiledFn fn = encode_fn(&why);
+    if (!fn)
+        return set_error(TSX_ERR_CUDA, why);
+    TensorMapArgs m;
+    tensor_map_args(p->g, &m);
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5];
+    for (int d = 0; d < m.rank; ++d) {
+        dims[d] = m.dims[d];
+        box[d] = m.box[d];
+        estr[d] = 1;
+    }
+    for (int d = 0; d + 1 < m.rank; ++d)
+        strides[d] = m.strides[d];
+    const CUresult r = fn(map, map_dtype(p->g.dtype), cuuint32_t(m.rank), const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(m.swizzle),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[96];
+        std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+        return set_error(TSX_ERR_CUDA, buf);
+    }
+    return TSX_OK;
+}
+
+// The tensor map of `ptr`, from the plan's cache or freshly encoded.
+int get_map(tsx_plan* p, const void* ptr, CUtensorMap* out)
+{
+    tsx_plan::MapEntry* victim = &p->maps[0];
+    for (auto& e : p->maps) {
+        if (e.ptr == ptr) {
+            e.used = ++p->clock;
+            *out = e.map;
+            return TSX_OK;
+        }
+        if (e.used < victim->used)
+            victim = &e;
+    }
+    const int rc = encode_map(p, ptr, &victim->map);
+    if (rc != TSX_OK) {
+        victim->ptr = nullptr;
+        victim->used = 0;
+        return rc;
+    }
+    victim->ptr = ptr;
+    victim->used = ++p->clock;
+    *out = victim->map;
+    return TSX_OK;
+}
+
+int alignment_of(const void* ptr)
+{
+    const uintptr_t v = reinterpret_cast<uintptr_t>(ptr);
+    for (int a : {16, 8, 4, 2})
+        if (v % a == 0)
+            return a;
+    return 1;
+}
+
+int read_status(tsx_plan* p, bool clear)
+{
+    int h = 0;
+    cudaError_t e = cudaMemcpy(&h, p->d_status, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_error(e, "reading the status word");
+    if (clear && h != TSX_OK) {
+        e = cudaMemset(p->d_status, 0, sizeof(int));
+        if (e != cudaSuccess)
+            return cuda_error(e, "clearing the status word");
+    }
+    return h;
+}
+
+}  // namespace
+
+extern "C" {
+
+tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
+                           tsx_variant variant)
+{
+    std::string why;
+    Geometry g;
+    int rc = make_geometry(dtype, rows, cols, box_rows, box_cols, stages, variant, &g, &why);
+    if (rc != TSX_OK) {
+        set_error(rc, why);
+        return nullptr;
+    }
+    tsx_plan* p = new (std::nothrow) tsx_plan;
+    if (!p) {
+        set_error(TSX_ERR_NOMEM, "out of host memory");
+        return nullptr;
+    }
+    p->g = g;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+    if (e == cudaSuccess) {
+        e = cudaMalloc(&p->d_status, sizeof(int));
+        if (e == cudaSuccess)
+            e = cudaMemset(p->d_status, 0, sizeof(int));
+    }
+    if (e != cudaSuccess) {
+        cuda_error(e, "tsx_plan_create");
+        if (p->d_status)
+            cudaFree(p->d_status);
+        delete p;
+        return nullptr;
+    }
+    const int64_t ms = env_i64("TSX_TIMEOUT_MS", 1000);
+    p->timeout_ns = uint64_t(ms > 0 ? ms : 1000) * 1000000ull;
+    p->fault_tile = env_i64("TSX_FAULT_SKIP_TILE", -1);
+    p->checked = env_i64("TSX_CHECKED", 0) != 0;
+    p->ctas_per_sm_cap = int(env_i64("TSX_CTAS_PER_SM", 0));
+    set_last_error("");
+    return p;
+}
+
+void tsx_plan_destroy(tsx_plan_t p)
+{
+    if (!p)
+        return;
+    if (p->d_status)
+        cudaFree(p->d_status);
+    delete p;
+}
+
+int tsx_plan_status(tsx_plan_t p)
+{
+    if (!p)
+        return set_error(TSX_ERR_INVALID, "NULL plan");
+    return read_status(p, true);
+}
+
+const char* tsx_last_error(void) { return g_last_error.c_str(); }
+
+int tsx_plan_get_info(tsx_plan_t p, tsx_op op, tsx_plan_info* info)
+{
+    if (!p || !info)
+        return set_error(TSX_ERR_INVALID, "NULL plan or info");
+    if (op < TSX_COPY || op > TSX_FMA)
+        return set_error(TSX_ERR_INVALID, "unknown op");
+    tsx_plan::OpLaunch* L = nullptr;
+    const int rc = prepare_op(p, op, &L);
+    if (rc != TSX_OK)
+        return rc;
+    fill_info(p->g, L->og, info);
+    info->ctas_per_sm = L->ctas_per_sm;
+    info->grid = L->grid;
+    info->sm_count = p->sm_count;
+    return TSX_OK;
+}
+
+int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void* c, void* out, tsx_stream_t stream)
+{
+    if (!p)
+        return set_error(TSX_ERR_INVALID, "NULL plan");
+    if (op < TSX_COPY || op > TSX_FMA)
+        return set_error(TSX_ERR_INVALID, "unknown op");
+    const int n_in = op_arity(op);
+    const Geometry& g = p->g;
+    if (g.tiles == 0) {
+        set_last_error("");
+        return TSX_OK;   // empty tensor: nothing to do, pointers are not examined
+    }
+    if (!a || !out)
+        return set_error(TSX_ERR_INVALID, "a and out are required");
+    if ((n_in >= 2) != (b != nullptr))
+        return set_error(TSX_ERR_INVALID, n_in >= 2 ? "this op needs b" : "b must be NULL for this op");
+    if ((n_in >= 3) != (c != nullptr))
+        return set_error(TSX_ERR_INVALID, n_in >= 3 ? "this op needs c" : "c must be NULL for this op");
+    const void* ops[4] = {a, b, c, out};
+    int align = 16;
+    for (int j = 0; j < 4; ++j)
+        if (ops[j] && alignment_of(ops[j]) < align)
+            align = alignment_of(ops[j]);
+
+    tsx_plan::OpLaunch* L = nullptr;
+    int rc = prepare_op(p, op, &L);
+    if (rc != TSX_OK)
+        return rc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (g.variant == TSX_TMA || g.variant == TSX_TMA_RANK3) {
+        if (align < 16)
+            return set_error(TSX_ERR_ALIGN, "TMA needs 16-byte aligned base pointers");
+        CUtensorMap maps[4];
+        std::memset(maps, 0, sizeof maps);
+        for (int j = 0; j < 4; ++j) {
+            if (!ops[j])
+                continue;
+            rc = get_map(p, ops[j], &maps[j]);
+            if (rc != TSX_OK)
+                return rc;
+        }
+        TmaArgs args{};
+        args.tiles = g.tiles;
+        args.tiles_c = g.tiles_c;
+        args.fault_tile = p->fault_tile;
+        args.status = p->d_status;
+        args.timeout_ns = p->timeout_ns;
+        args.rows = int(g.rows);
+        args.cols = int(g.cols);
+        args.box_rows = g.box_rows;
+        args.box_cols = g.box_cols;
+        args.stages = g.stages;
+        args.inner_elems = g.inner_elems;
+        args.atoms = g.atoms;
+        args.rows_per_load = g.rows_per_load;
+        args.row_chunks = g.row_chunks;
+        args.rank3 = g.variant == TSX_TMA_RANK3;
+        args.load_smem_bytes = g.load_smem_bytes;
+        args.slot_bytes = g.slot_bytes;
+        args.stage_bytes = L->og.stage_bytes;
+        args.bytes_per_load = uint32_t(g.bytes_per_load);
+        args.vec16_per_slot = L->og.vec16_per_slot;
+        e = launch_tma(g.dtype, op, L->grid, g.threads, L->og.smem_bytes, st, maps, args);
+    } else {
+        int vb = g.copy_vec_bytes < align ? g.copy_vec_bytes : align;
+        if (vb < 4)
+            return set_error(TSX_ERR_ALIGN, "cp.async / vector copies need 4-byte aligned base pointers");
+        CopyArgs args{};
+        args.rows = g.rows;
+        args.cols = g.cols;
+        args.tiles = g.tiles;
+        args.tiles_c = g.tiles_c;
+        args.box_rows = g.box_rows;
+        args.box_cols = g.box_cols;
+        args.stages = g.variant == TSX_SYNC ? 1 : g.stages;
+        args.vec_bytes = vb;
+        args.tile_bytes = uint32_t(g.box_rows) * uint32_t(g.box_cols) * uint32_t(g.es);
+        args.slot_bytes = g.slot_bytes;
+        args.stage_bytes = L->og.stage_bytes;
+        args.chunks_per_slot = args.tile_bytes / uint32_t(vb);
+        args.vec16_per_slot = L->og.vec16_per_slot;
+        e = g.variant == TSX_LDGSTS
+                ? launch_ldgsts(g.dtype, op, L->grid, g.threads, L->og.smem_bytes, st, a, b, c, out, args)
+                : launch_sync(g.dtype, op, L->grid, g.threads, L->og.smem_bytes, st, a, b, c, out, args);
+    }
+    if (e != cudaSuccess)
+        return cuda_error(e, "kernel launch");
+    if (p->checked) {
+        e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaStreamSynchronize");
+        const int s = read_status(p, true);
+        if (s != TSX_OK)
+            return set_error(s, "a device-side wait gave up");
+    }
+    set_last_error("");
+    return TSX_OK;
+}
+
+}  // extern "C"

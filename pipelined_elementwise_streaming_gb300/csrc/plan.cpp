@@ -1,0 +1,277 @@
+// Host planner of libtsx: argument validation, the TMA box split, the
+// tensor-map encode arguments, the [outer, threads, vec] partition and the
+// shared-memory budget.  Pure integer arithmetic: no CUDA call happens here,
+// so tsx_plan_query works on a machine without a GPU.
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "plan.h"
+
+namespace tsx {
+
+namespace {
+
+bool fail(std::string* why, const char* fmt, long long a = 0, long long b = 0)
+{
+    if (why) {
+        char buf[256];
+        std::snprintf(buf, sizeof buf, fmt, a, b);
+        *why = buf;
+    }
+    return false;
+}
+
+int env_int(const char* name, int fallback)
+{
+    const char* v = std::getenv(name);
+    if (!v || !*v)
+        return fallback;
+    return std::atoi(v);
+}
+
+uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+int default_threads(int variant)
+{
+    // 256 threads for the TMA paths (8 warps share one elected producer
+    // lane); 128 for the cp.async / synchronous ablations, the thread count
+    // of the TVM ldgsts demonstration program.
+    const int fallback = (variant == TSX_TMA || variant == TSX_TMA_RANK3) ? 256 : 128;
+    int t = env_int("TSX_THREADS", fallback);
+    if (t < 32 || t > kMaxThreads || t % 32)
+        t = fallback;
+    return t;
+}
+
+int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
+                  Geometry* g, std::string* why)
+{
+    *g = Geometry{};
+    if (dtype < TSX_F16 || dtype > TSX_F32)
+        return fail(why, "unknown dtype %lld", dtype), TSX_ERR_INVALID;
+    if (variant < TSX_TMA || variant > TSX_TMA_RANK3)
+        return fail(why, "unknown variant %lld", variant), TSX_ERR_INVALID;
+    if (rows < 0 || cols < 0)
+        return fail(why, "negative shape %lld x %lld", rows, cols), TSX_ERR_INVALID;
+    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31))
+        return fail(why, "rows and cols must be < 2^31 (got %lld x %lld)", rows, cols), TSX_ERR_UNSUPPORTED;
+    if (box_rows < 1 || box_cols < 1)
+        return fail(why, "box dims must be >= 1 (got %lld x %lld)", box_rows, box_cols), TSX_ERR_UNSUPPORTED;
+    if (stages < 1 || stages > kMaxStages)
+        return fail(why, "stages must be in [1, %lld] (got %lld)", kMaxStages, stages), TSX_ERR_UNSUPPORTED;
+
+    const int es = elem_size(dtype);
+    g->dtype = dtype;
+    g->es = es;
+    g->variant = variant;
+    g->rows = rows;
+    g->cols = cols;
+    g->box_rows = box_rows;
+    g->box_cols = box_cols;
+    g->stages = stages;
+    g->tiles_r = rows == 0 ? 0 : (rows + box_rows - 1) / box_rows;
+    g->tiles_c = cols == 0 ? 0 : (cols + box_cols - 1) / box_cols;
+    g->tiles = g->tiles_r * g->tiles_c;
+    g->threads = default_threads(variant);
+
+    const int64_t row_bytes = int64_t(box_cols) * es;
+    const int64_t tile_bytes = row_bytes * box_rows;
+    if (tile_bytes > kMaxDynSmem)
+        return fail(why, "a %lld-byte stage tile cannot fit in shared memory", tile_bytes), TSX_ERR_UNSUPPORTED;
+
+    if (variant == TSX_TMA || variant == TSX_TMA_RANK3) {
+        // Global strides of a tensor map are multiples of 16 bytes.
+        if ((cols * es) % 16)
+            return fail(why, "TMA needs a row pitch that is a multiple of 16 bytes (cols * elem = %lld)", cols * es),
+                   TSX_ERR_UNSUPPORTED;
+        // The innermost box spans at most one 128-byte swizzle atom and a
+        // whole number of 16-byte units; a wider tile row is several atoms.
+        if (row_bytes % 16)
+            return fail(why, "a tile row of %lld bytes is not a multiple of 16", row_bytes), TSX_ERR_UNSUPPORTED;
+        const int inner_bytes = row_bytes < kSwizzleAtom ? int(row_bytes) : kSwizzleAtom;
+        if (row_bytes % inner_bytes)
+            return fail(why, "a tile row of %lld bytes is not a whole number of 128-byte atoms", row_bytes),
+                   TSX_ERR_UNSUPPORTED;
+        // Every box dimension is at most 256: taller tiles take several
+        // equal row chunks.
+        const int chunks = (box_rows + kBoxMax - 1) / kBoxMax;
+        if (box_rows % chunks)
+            return fail(why, "%lld tile rows cannot be cut into equal chunks of at most 256", box_rows),
+                   TSX_ERR_UNSUPPORTED;
+        g->inner_bytes = inner_bytes;
+        g->inner_elems = inner_bytes / es;
+        g->atoms = int(row_bytes / inner_bytes);
+        g->row_chunks = chunks;
+        g->rows_per_load = box_rows / chunks;
+        g->swizzle_bytes = (inner_bytes == 32 || inner_bytes == 64 || inner_bytes == 128) ? inner_bytes : 0;
+        const uint32_t atom_bytes = uint32_t(g->rows_per_load) * inner_bytes;
+        if (variant == TSX_TMA) {
+            g->loads_per_operand = g->atoms * g->row_chunks;
+            g->bytes_per_load = int(atom_bytes);
+            // each box lands on its own 1024-byte boundary: the swizzle
+            // pattern repeats every 1024 bytes
+            g->load_smem_bytes = round_up(atom_bytes, g->swizzle_bytes ? kSmemAlign : 128);
+        } else {
+            if (cols % g->inner_elems)
+                return fail(why, "the rank-3 form needs cols to be a whole number of %lld-element atoms",
+                            g->inner_elems),
+                       TSX_ERR_UNSUPPORTED;
+            if (g->atoms > kBoxMax)
+                return fail(why, "%lld atoms per tile row exceed a box dimension", g->atoms), TSX_ERR_UNSUPPORTED;
+            if (g->swizzle_bytes && atom_bytes % kSmemAlign)
+                return fail(why, "the rank-3 form needs rows_per_load * 128 B to be a multiple of 1024 (%lld)",
+                            atom_bytes),
+                       TSX_ERR_UNSUPPORTED;
+            g->loads_per_operand = g->row_chunks;
+            g->bytes_per_load = int(atom_bytes) * g->atoms;
+            g->load_smem_bytes = round_up(uint32_t(g->bytes_per_load), g->swizzle_bytes ? kSmemAlign : 128);
+        }
+        g->slot_bytes = g->load_smem_bytes * uint32_t(g->loads_per_operand);
+        g->copy_vec_bytes = 0;
+    } else {
+        // cp.async copies 16, 8 or 4 bytes; the synchronous variant uses the
+        // same widths.  The widest one dividing the row pitch and the tile
+        // row is taken (base pointers are checked per call).
+        int vb = 0;
+        for (int cand : {16, 8, 4}) {
+            if ((cols * es) % cand == 0 && row_bytes % cand == 0) {
+                vb = cand;
+                break;
+            }
+        }
+        if (!vb)
+            return fail(why, "no copy width of 16, 8 or 4 bytes divides the rows (%lld-byte tile row)", row_bytes),
+                   TSX_ERR_UNSUPPORTED;
+        g->copy_vec_bytes = vb;
+        g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
+    }
+    return TSX_OK;
+}
+
+int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, std::string* why)
+{
+    *og = OpGeometry{};
+    if (op < TSX_COPY || op > TSX_FMA)
+        return fail(why, "unknown op %lld", op), TSX_ERR_INVALID;
+    og->op = op;
+    og->n_in = op_arity(op);
+    og->stage_bytes = g.slot_bytes * uint32_t(og->n_in);
+    const bool tma = g.variant == TSX_TMA || g.variant == TSX_TMA_RANK3;
+    const int stages = g.variant == TSX_SYNC ? 1 : g.stages;
+    if (tma) {
+        // expect_tx of a stage: every load of every operand
+        og->tx_bytes = uint32_t(og->n_in) * uint32_t(g.loads_per_operand) * uint32_t(g.bytes_per_load);
+        og->smem_bytes = size_t(stages) * og->stage_bytes + size_t(stages) * 8 + kSmemAlign;
+    } else {
+        og->tx_bytes = 0;
+        og->smem_bytes = size_t(stages) * og->stage_bytes;
+    }
+    if (og->smem_bytes > size_t(max_smem))
+        return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
+               TSX_ERR_UNSUPPORTED;
+    // [outer, threads, vec] of the elementwise stage: 16-byte vectors
+    og->vec = 16 / g.es;
+    const uint32_t units = g.slot_bytes / 16;
+    og->outer = int((units + g.threads - 1) / g.threads);
+    og->vec16_per_slot = units;
+    return TSX_OK;
+}
+
+void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
+{
+    std::memset(info, 0, sizeof *info);
+    info->dtype = g.dtype;
+    info->variant = g.variant;
+    info->op = og.op;
+    info->n_in = og.n_in;
+    info->elem_size = g.es;
+    info->box_rows = g.box_rows;
+    info->box_cols = g.box_cols;
+    info->stages = g.stages;
+    info->rows = g.rows;
+    info->cols = g.cols;
+    info->tiles = g.tiles;
+    info->tiles_r = g.tiles_r;
+    info->tiles_c = g.tiles_c;
+    info->inner_elems = g.inner_elems;
+    info->inner_bytes = g.inner_bytes;
+    info->atoms = g.atoms;
+    info->rows_per_load = g.rows_per_load;
+    info->row_chunks = g.row_chunks;
+    info->loads_per_operand = g.loads_per_operand;
+    info->bytes_per_load = g.bytes_per_load;
+    info->tx_bytes = int32_t(og.tx_bytes);
+    info->threads = g.threads;
+    info->vec = og.vec;
+    info->outer = og.outer;
+    info->copy_vec_bytes = g.copy_vec_bytes;
+    info->slot_bytes = int32_t(g.slot_bytes);
+    info->stage_bytes = int32_t(og.stage_bytes);
+    info->smem_bytes = int32_t(og.smem_bytes);
+    if (g.variant == TSX_TMA || g.variant == TSX_TMA_RANK3) {
+        TensorMapArgs m;
+        tensor_map_args(g, &m);
+        info->rank = m.rank;
+        for (int d = 0; d < m.rank; ++d) {
+            info->global_dim[d] = m.dims[d];
+            info->box_dim[d] = m.box[d];
+            info->element_strides[d] = 1;
+        }
+        for (int d = 0; d + 1 < m.rank; ++d)
+            info->global_stride_bytes[d] = m.strides[d];
+        info->interleave = 0;                       // CU_TENSOR_MAP_INTERLEAVE_NONE
+        info->swizzle = m.swizzle;
+        info->l2_promotion = 2;                     // CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+        info->oob_fill = 0;                         // CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE: zeros
+    }
+}
+
+void tensor_map_args(const Geometry& g, TensorMapArgs* m)
+{
+    *m = TensorMapArgs{};
+    m->swizzle = g.swizzle_bytes == 128 ? 3 : g.swizzle_bytes == 64 ? 2 : g.swizzle_bytes == 32 ? 1 : 0;
+    // dims[0] is the innermost (contiguous) dimension
+    const uint64_t rows = uint64_t(g.rows), cols = uint64_t(g.cols);
+    if (g.variant == TSX_TMA_RANK3) {
+        // [cols / atom, rows, atom]: the atom axis strides by one atom
+        m->rank = 3;
+        m->dims[0] = uint64_t(g.inner_elems);
+        m->dims[1] = rows;
+        m->dims[2] = cols / uint64_t(g.inner_elems);
+        m->strides[0] = cols * uint64_t(g.es);
+        m->strides[1] = uint64_t(g.inner_bytes);
+        m->box[0] = uint32_t(g.inner_elems);
+        m->box[1] = uint32_t(g.rows_per_load);
+        m->box[2] = uint32_t(g.atoms);
+    } else {
+        m->rank = 2;
+        m->dims[0] = cols;
+        m->dims[1] = rows;
+        m->strides[0] = cols * uint64_t(g.es);
+        m->box[0] = uint32_t(g.inner_elems);
+        m->box[1] = uint32_t(g.rows_per_load);
+    }
+}
+
+}  // namespace tsx
+
+extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
+                              tsx_variant variant, tsx_op op, tsx_plan_info* info)
+{
+    std::string why;
+    tsx::Geometry g;
+    int rc = tsx::make_geometry(dtype, rows, cols, box_rows, box_cols, stages, variant, &g, &why);
+    if (rc == TSX_OK) {
+        tsx::OpGeometry og;
+        rc = tsx::make_op_geometry(g, op, tsx::kMaxDynSmem, &og, &why);
+        if (rc == TSX_OK && info)
+            tsx::fill_info(g, og, info);
+    }
+    tsx::set_last_error(rc == TSX_OK ? "" : why.c_str());
+    return rc;
+}

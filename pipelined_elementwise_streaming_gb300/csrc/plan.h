@@ -1,0 +1,55 @@
+// Host-side plan geometry of libtsx (pure integer logic, see plan.cpp).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "tsx_internal.h"
+
+namespace tsx {
+
+// Everything fixed by (dtype, shape, box, stages, variant).
+struct Geometry {
+    int dtype = 0, es = 0, variant = 0, stages = 0;
+    int64_t rows = 0, cols = 0;
+    int box_rows = 0, box_cols = 0;
+    int64_t tiles_r = 0, tiles_c = 0, tiles = 0;
+    int threads = 0;
+    // TMA split
+    int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
+    int loads_per_operand = 0, bytes_per_load = 0, swizzle_bytes = 0;
+    uint32_t load_smem_bytes = 0;
+    // one operand's tile in shared memory
+    uint32_t slot_bytes = 0;
+    // copy width of the cp.async / synchronous variants (16-byte aligned bases)
+    int copy_vec_bytes = 0;
+};
+
+// What additionally depends on the op (operand count).
+struct OpGeometry {
+    int op = 0, n_in = 0;
+    uint32_t stage_bytes = 0, tx_bytes = 0, vec16_per_slot = 0;
+    size_t smem_bytes = 0;
+    int vec = 0, outer = 0;
+};
+
+struct TensorMapArgs {
+    int rank = 0;
+    uint64_t dims[5] = {};
+    uint64_t strides[4] = {};
+    uint32_t box[5] = {};
+    int swizzle = 0;   // CUtensorMapSwizzle value
+};
+
+int default_threads(int variant);
+int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
+                  Geometry* g, std::string* why);
+int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, std::string* why);
+void tensor_map_args(const Geometry& g, TensorMapArgs* m);
+void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info);
+
+// Thread-local message behind tsx_last_error (capi.cpp).
+void set_last_error(const char* msg);
+
+}  // namespace tsx

@@ -1,0 +1,78 @@
+// Internal declarations shared by the host planner, the C ABI and the
+// kernels of libtsx.  Not part of the public interface (include/tsx.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tsx.h"
+
+#ifdef __CUDACC__
+#define TSX_HD __host__ __device__
+#else
+#define TSX_HD
+#endif
+
+namespace tsx {
+
+constexpr int kMaxStages = 16;
+constexpr int kMaxThreads = 1024;
+constexpr int kSmemAlign = 1024;       // 128-B swizzle pattern period
+constexpr int kBoxMax = 256;           // per TMA box dimension
+constexpr int kSwizzleAtom = 128;      // bytes
+constexpr int kMaxDynSmem = 232448;    // 227 KiB opt-in per CTA on sm_100 / sm_103
+
+TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
+TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }
+
+// Kernel arguments of the TMA circular-buffer kernel.
+struct TmaArgs {
+    int64_t tiles;          // T: tiles in the tensor
+    int64_t tiles_c;        // tiles along a row
+    int64_t fault_tile;     // test hook: the producer skips this tile's loads (-1: none)
+    int* status;            // device status word (TSX_OK until a wait gives up)
+    uint64_t timeout_ns;    // limit of every mbarrier wait
+    int rows, cols;         // tensor extent (< 2^31)
+    int box_rows, box_cols;
+    int stages;
+    int inner_elems;        // innermost box extent
+    int atoms;              // boxes side by side along a tile row (rank 2)
+    int rows_per_load;
+    int row_chunks;         // boxes stacked along the rows
+    int rank3;              // 1: one rank-3 box per row chunk covers all atoms
+    uint32_t load_smem_bytes;  // shared-memory footprint of one load
+    uint32_t slot_bytes;       // one operand's tile
+    uint32_t stage_bytes;      // n_in slots
+    uint32_t bytes_per_load;   // bytes one box delivers (out-of-bounds part zero-filled)
+    uint32_t vec16_per_slot;   // 16-byte units of one slot
+};
+
+// Kernel arguments of the cp.async and synchronous ablation kernels.
+struct CopyArgs {
+    int64_t rows, cols;
+    int64_t tiles, tiles_c;
+    int box_rows, box_cols;
+    int stages;
+    int vec_bytes;            // width of one copy: 16, 8 or 4
+    uint32_t tile_bytes;      // box_rows * box_cols * element size
+    uint32_t slot_bytes;      // tile_bytes rounded up to 16
+    uint32_t stage_bytes;
+    uint32_t chunks_per_slot; // tile_bytes / vec_bytes
+    uint32_t vec16_per_slot;  // slot_bytes / 16
+};
+
+// Kernel lookup and launch, one set per variant (k_tma.cu, k_ldgsts.cu,
+// k_sync.cu).  `maps` holds the tensor maps of a, b, c and out.
+const void* tma_kernel(int dtype, int op);
+cudaError_t launch_tma(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
+                       const CUtensorMap* maps, const TmaArgs& args);
+const void* ldgsts_kernel(int dtype, int op);
+cudaError_t launch_ldgsts(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
+                          const void* a, const void* b, const void* c, void* out, const CopyArgs& args);
+const void* sync_kernel(int dtype, int op);
+cudaError_t launch_sync(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
+                        const void* a, const void* b, const void* c, void* out, const CopyArgs& args);
+
+}  // namespace tsx

@@ -1,0 +1,144 @@
+"""The C ABI on the host: the library loads, exports every declared symbol,
+and its planner agrees with the oracle's structure models (no GPU needed)."""
+
+import ctypes
+import itertools
+import os
+import re
+
+import pytest
+
+from oracle import structure as st
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsx.h")
+
+
+@pytest.fixture(scope="module")
+def tsx():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import pipelined_elementwise_streaming_gb300 as m
+
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsx_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("tsx_plan_create", "tsx_ewise", "tsx_plan_destroy", "tsx_plan_status", "tsx_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tsx):
+    lib = ctypes.CDLL(tsx.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_uses_the_c_names(tsx):
+    for n in _declared_functions():
+        assert hasattr(tsx, n), n
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_query_matches_oracle_split_and_encode(tsx, dtype):
+    es = st.ELEM_SIZE[dtype]
+    for br, bc, variant in itertools.product((1, 7, 8, 32, 64, 128, 256, 300, 512), (8, 16, 32, 64, 128, 192, 256),
+                                             ("tma", "tma_rank3")):
+        rows, cols = 1000, 4096
+        mode = "rank3" if variant == "tma_rank3" else "rank2"
+        sp = st.split(dtype, br, bc, mode, cols=cols)
+        why = ""
+        try:
+            q = tsx.query(dtype, rows, cols, (br, bc), 2, variant, "add")
+        except tsx.TsxError as e:
+            q, why = None, str(e)
+        if sp is None:
+            assert q is None, (br, bc, variant)
+            continue
+        if q is None:
+            # a legal split the library declines for one of its own limits:
+            # the stages do not fit in shared memory, or (rank 3) the atoms of
+            # a swizzled box would not each start on the 1024-byte period
+            assert "shared memory" in why or "1024" in why, (br, bc, variant, why)
+            continue
+        assert q["loads_per_operand"] == sp.loads_per_operand
+        assert q["bytes_per_load"] == sp.bytes_per_load
+        assert q["tx_bytes"] == sp.tx_bytes(2)
+        assert q["inner_elems"] == sp.inner_elems and q["atoms"] == sp.atoms
+        assert q["rows_per_load"] == sp.rows_per_load and q["row_chunks"] == sp.row_chunks
+        enc = st.encode_args(dtype, rows, cols, sp)
+        rank = enc[1]
+        assert q["rank"] == rank
+        assert q["global_dim"][:rank] == list(enc[2:2 + rank])
+        assert q["global_stride_bytes"][:rank - 1] == list(enc[2 + rank:1 + 2 * rank])
+        assert q["box_dim"][:rank] == list(enc[1 + 2 * rank:1 + 3 * rank])
+        assert (q["interleave"], q["swizzle"], q["l2_promotion"], q["oob_fill"]) == enc[-4:]
+
+
+def test_query_rank3_demo_tuple(tsx):
+    """The 8x256 float16 tile with the 128-B swizzle: the encode arguments
+    printed by the TVM page ("copy_async -> tma", Generated TIRx IR)."""
+    q = tsx.query("f16", 8, 256, (8, 256), 1, "tma_rank3", "copy")
+    got = (3, *q["global_dim"][:3], *q["global_stride_bytes"][:2], *q["box_dim"][:3], *q["element_strides"][:3],
+           q["interleave"], q["swizzle"], q["l2_promotion"], q["oob_fill"])
+    assert got == (3, 64, 8, 4, 512, 128, 64, 8, 4, 1, 1, 1, 0, 3, 2, 0)
+
+
+def test_query_workload_plans(tsx):
+    q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma")
+    assert (q["loads_per_operand"], q["tx_bytes"], q["box_dim"][:2]) == (4, 12288, [32, 8])
+    q = tsx.query("bf16", 16384, 16384, (128, 128), 4, "tma", "exp")
+    assert (q["loads_per_operand"], q["tx_bytes"], q["box_dim"][:2]) == (2, 32768, [64, 128])
+    q = tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")
+    assert (q["vec"], q["outer"], q["threads"], q["tiles"]) == (4, 1, 256, 16 * 128)
+
+
+def test_query_partition_matches_oracle(tsx):
+    # TMA elementwise stage: 16-byte vectors over 256 threads
+    for dtype, br, bc in (("f32", 32, 32), ("f16", 64, 64), ("f32", 8, 128), ("bf16", 128, 128)):
+        q = tsx.query(dtype, 1024, 4096, (br, bc), 2, "tma", "copy")
+        want = st.partition(br * bc, q["threads"], st.ELEM_SIZE[dtype], run_bytes=bc * st.ELEM_SIZE[dtype],
+                            align_bytes=16)
+        assert (q["vec"], q["outer"]) == want
+    # cp.async: 128x32 fp16 over 128 threads -> 16-byte copies, vec 8, outer 4
+    q = tsx.query("f16", 500, 4096, (128, 32), 2, "ldgsts", "sqrt")
+    assert q["threads"] == 128 and q["copy_vec_bytes"] == 16
+    assert st.partition(128 * 32, 128, 2, 64, 16, st.LDGSTS_VEC_BITS) == (8, 4)
+    assert (q["copy_vec_bytes"] // 2, (128 * 32 * 2) // (q["copy_vec_bytes"] * q["threads"])) == (8, 4)
+    # copy width narrows with the row pitch (8-byte and 4-byte rows)
+    assert tsx.query("f16", 64, 4100, (8, 4), 2, "ldgsts", "copy")["copy_vec_bytes"] == 8
+    assert tsx.query("f16", 64, 4098, (8, 2), 2, "ldgsts", "copy")["copy_vec_bytes"] == 4
+
+
+@pytest.mark.parametrize("args,code", [
+    (("f32", 100, 102, (8, 32), 2, "tma", "copy"), -2),       # row pitch 408 B: not a 16-B multiple
+    (("f32", 100, 128, (8, 40), 2, "tma", "copy"), -2),       # 160-B tile row
+    (("f32", 100, 128, (257, 32), 2, "tma", "copy"), -2),     # 257 rows: no equal chunks <= 256
+    (("f32", 100, 128, (8, 32), 0, "tma", "copy"), -2),       # stages < 1
+    (("f32", 100, 128, (8, 32), 17, "tma", "copy"), -2),      # stages > 16
+    (("f32", 100, 128, (0, 32), 2, "tma", "copy"), -2),       # empty box
+    (("f16", 8, 100, (8, 256), 1, "tma_rank3", "copy"), -2),  # cols not a whole number of atoms
+    (("f16", 64, 4097, (8, 1), 2, "ldgsts", "copy"), -2),     # 2-byte rows: below the 4-byte cp_size
+    (("f32", 1 << 31, 128, (8, 32), 2, "tma", "copy"), -2),   # rows >= 2^31
+    (("f32", 100, 128, (256, 256), 4, "tma", "fma"), -2),     # stages do not fit in shared memory
+    (("f32", -1, 128, (8, 32), 2, "tma", "copy"), -1),
+    (("f32", 100, 128, (8, 32), 2, "tma", 9), -1),            # unknown op
+])
+def test_query_declines(tsx, args, code):
+    with pytest.raises(tsx.TsxError) as ei:
+        tsx.query(*args)
+    assert ei.value.code == code
+    assert tsx.tsx_last_error()
+
+
+def test_query_empty_tensor_is_legal(tsx):
+    q = tsx.query("f32", 0, 128, (8, 32), 2, "tma", "copy")
+    assert q["tiles"] == 0
