@@ -2,8 +2,10 @@
 
 Each translation unit is compiled in parallel into ``_build/``, then linked
 (cudart static) into the package directory.  A unit is recompiled when it or
-any header is newer than its object.  ``python -m
-pipelined_elementwise_streaming_gb300._build`` runs it from the command line.
+any header is newer than its object.  ``python
+pipelined_elementwise_streaming_gb300/_build.py`` runs it from the command
+line (``__graft_entry__.build()`` loads this file by path, since importing
+the package needs the library this builds).
 """
 
 from __future__ import annotations
