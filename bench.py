@@ -53,7 +53,10 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ti.WORKLOADS))
-    p.add_argument("--stages", type=int, default=None, help="default: the workload's last stated stage count")
+    p.add_argument("--stages", type=int, default=None,
+                   help="default: the workload's benchmark stage count (one of its stated ones)")
+    p.add_argument("--rows", type=int, default=None,
+                   help="run the workload over its first ROWS rows only (a smaller case, e.g. for profiling)")
     p.add_argument("--variant", default=None, help="default: the workload's variant")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -343,7 +346,7 @@ def run_ours(args, w, stages, variant):
         "dtype": DTYPE_NAME[w.dtype],
         "data": "synthetic (seeded SplitMix64 inputs, the workload's stated distribution)",
         "config": {
-            "workload": w.name, "op": w.op, "rows": w.rows, "cols": w.cols, "box": [w.box_rows, w.box_cols],
+            "workload": w.name + ("" if args.rows is None else f" (first {w.rows} rows)"), "op": w.op, "rows": w.rows, "cols": w.cols, "box": [w.box_rows, w.box_cols],
             "stages": stages, "variant": variant, "threads": info["threads"], "grid": info["grid"],
             "ctas_per_sm": info["ctas_per_sm"], "loads_per_operand": info["loads_per_operand"],
             "algorithmic_bytes_per_step": w.algorithmic_bytes,
@@ -446,7 +449,9 @@ def run_reference(args, w, stages, variant):
 def main(argv=None):
     args = parse_args(argv)
     w = ti.WORKLOADS[args.workload]
-    stages = args.stages if args.stages is not None else w.stages[-1]
+    if args.rows is not None:
+        w = w.with_rows(args.rows)
+    stages = args.stages if args.stages is not None else w.default_stages
     variant = args.variant or w.variant
     if args.impl == "reference":
         res = run_reference(args, w, stages, variant)

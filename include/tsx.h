@@ -111,6 +111,9 @@ typedef struct tsx_plan_info {
     int32_t smem_bytes;
     /* launch (0 from tsx_plan_query, which does not look at a GPU) */
     int32_t ctas_per_sm, grid, sm_count;
+    /* threads of one CTA: for the TMA variants the elementwise threads plus
+     * a producer warp and a store warp */
+    int32_t block_threads;
 } tsx_plan_info;
 
 /* Create a plan for [rows, cols] tensors of `dtype`, streamed in stage

@@ -51,7 +51,7 @@ class tsx_plan_info(ctypes.Structure):
                [(n, ctypes.c_int32) for n in ("interleave", "swizzle", "l2_promotion", "oob_fill",
                                                "threads", "vec", "outer", "copy_vec_bytes",
                                                "slot_bytes", "stage_bytes", "smem_bytes",
-                                               "ctas_per_sm", "grid", "sm_count")]
+                                               "ctas_per_sm", "grid", "sm_count", "block_threads")]
 
     def as_dict(self) -> dict:
         d = {}

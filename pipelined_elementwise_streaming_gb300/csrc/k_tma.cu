@@ -1,34 +1,42 @@
 // The TMA circular-buffer elementwise kernel.
 //
 // A persistent CTA c of G takes tiles c, c + G, c + 2G, ... (row-major tile
-// order) and streams them through S stage buffers in shared memory.  Each
-// stage has one mbarrier, initialised with an arrival count of 1: the
-// elected producer lane of warp 0 arrives once with expect_tx = the bytes of
-// all the stage's loads, then issues the loads; the TMA unit completes the
-// phase when the bytes have landed (TVM docs "copy_async -> tma",
-// "Demonstration program"; nvFuser PR #2833 "Add TMA support for circular
-// buffering pass", "Lowering Details").
+// order) and streams them through S stage buffers in shared memory.  The
+// warps of a CTA have three roles:
 //
-// The loop structure is the one of the nvFuser page ("Loop Structure",
-// "Detailed Pseudo-Code"): a pre-prologue that initialises every stage's
-// barrier, a prologue that issues the loads of the first S - 1 tiles, a main
-// loop whose iteration i issues the loads of tile i + S - 1 into stage
-// (i + S - 1) mod S and then waits on tile i in stage i mod S with parity
-// (i / S) mod 2, an epilogue that only waits, and a post-epilogue that
-// invalidates the barriers.
+//   warp 0      the producer: its elected lane arrives once on the stage's
+//               `full` mbarrier with expect_tx = the bytes of the stage's
+//               loads, then issues the cp.async.bulk.tensor loads; the TMA
+//               unit completes the phase when the bytes have landed (TVM docs
+//               "copy_async -> tma", "Demonstration program"; nvFuser PR
+//               #2833 "Add TMA support for circular buffering pass",
+//               "Lowering Details").
+//   warp 1      the store warp: its elected lane waits until the tile is
+//               computed, issues the TMA store from the stage, and hands the
+//               stage back to the producer (`empty`) once the store has
+//               finished reading shared memory.
+//   warps 2..   the compute warps: wait on `full` (parity (i / S) mod 2 for
+//               their i-th tile), apply the op to 16-byte vectors (f *
+//               threads + tid) of each operand's slot, write the result over
+//               operand a's slot and arrive on `computed` (TVM docs
+//               "elementwise -> smem", "Algorithm").
 //
-// The body of an iteration is the shared-memory elementwise stage (TVM docs
-// "elementwise -> smem"): every thread takes 16-byte vectors (f * threads +
-// tid) of each operand's slot, applies the op, and writes the result over
-// operand a's slot.  The tile then goes back to global with a TMA store from
-// that slot.  Stage reuse (write after read) is guarded twice: a CTA barrier
-// after the body, and, before the producer refills a stage, a wait until the
-// bulk store that read it has finished reading shared memory.
+// The producer follows the loop structure of the nvFuser page ("Loop
+// Structure", "Detailed Pseudo-Code"): a pre-prologue that initialises the
+// barriers, a prologue that issues the first S - 1 tiles, a main loop that
+// issues tile i + S - 1 into stage (i + S - 1) mod S while the compute warps
+// wait on tile i in stage i mod S, and a post-epilogue that invalidates the
+// barriers; the consumers' loop over their tiles is the main loop plus the
+// epilogue.  Stage reuse is ordered by the `empty` barrier: the store warp
+// releases tile i's stage once the bulk stores up to tile i have read shared
+// memory, which it checks `lag` tiles later (cp.async.bulk.wait_group.read)
+// so that a draining store never holds up the compute warps.
 //
-// Every mbarrier wait is bounded in time.  If one gives up, the whole CTA
-// leaves the loop together (the decision is a CTA-wide OR), the producer
-// records TSX_ERR_TIMEOUT in the status word, waits (again bounded) for the
-// loads it still has in flight and for its stores, and the CTA exits.
+// Every mbarrier wait is bounded in time and also gives up when another
+// thread has raised the CTA's abort flag.  A wait that runs out records
+// TSX_ERR_TIMEOUT in the status word and raises the flag; every role then
+// leaves its loop, the producer waits (again bounded) for the loads it still
+// has in flight, the store warp for its stores, and the CTA exits.
 
 #include "tsx_device.cuh"
 
@@ -68,7 +76,7 @@ __device__ __forceinline__ TileBoxes tile_boxes(const TmaArgs& p, int64_t t)
 }
 
 // expect_tx (the bytes of every load this tile issues), then the loads of
-// tile t into the stage at shared address `stage` (producer lane only).
+// tile t into the stage at shared address `stage`.
 template <int NIN>
 __device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p, uint32_t stage, uint32_t bar,
                                            int64_t t)
@@ -93,7 +101,7 @@ __device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p
     }
 }
 
-// TMA store of tile t from the slot at shared address `slot` (producer lane).
+// TMA store of tile t from the slot at shared address `slot`.
 __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, uint32_t slot, int64_t t)
 {
     const TileBoxes b = tile_boxes(p, t);
@@ -110,36 +118,23 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
     bulk_commit();
 }
 
-// Wait on tile i (the CTA's i-th), apply the op in shared memory and store
-// the result.  Returns false on every thread if any thread's wait gave up.
-template <int DT, int OP, int NIN>
-__device__ __forceinline__ bool consume_tile(const TmaMaps& maps, const TmaArgs& p, uint8_t* smem, uint32_t base,
-                                             uint32_t bars, int64_t i, int64_t t, bool producer)
+// Bounded wait that also gives up when the CTA's abort flag is raised.  A
+// wait that runs out of time raises the flag and records the timeout.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const TmaArgs& p,
+                                              volatile int* abort_flag)
 {
-    const int S = p.stages;
-    const int s = static_cast<int>(i % S);
-    const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
-    const bool ok = mbar_wait(bars + 8u * s, parity, p.timeout_ns);
-
-    if constexpr (OP != TSX_COPY) {
-        if (ok) {
-            uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
-            const uint4* B = A + p.slot_bytes / 16;
-            const uint4* C = A + 2 * (p.slot_bytes / 16);
-            for (uint32_t u = threadIdx.x; u < p.vec16_per_slot; u += blockDim.x) {
-                const uint4 va = A[u];
-                const uint4 vb = NIN > 1 ? B[u] : va;
-                const uint4 vc = NIN > 2 ? C[u] : va;
-                A[u] = op_vec16<DT, OP>(va, vb, vc);
-            }
-            // make this thread's generic-proxy writes visible to the TMA store
-            fence_proxy_async_smem();
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag)
+            return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            atomicCAS(p.status, TSX_OK, TSX_ERR_TIMEOUT);
+            return false;
         }
     }
-    if (__syncthreads_or(!ok))
-        return false;
-    if (producer)
-        store_tile(maps, p, base + s * p.stage_bytes, t);
     return true;
 }
 
@@ -152,71 +147,111 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
     uint8_t* const smem = smem_raw + (base - raw);
     const int S = p.stages;
-    const uint32_t bars = base + static_cast<uint32_t>(S) * p.stage_bytes;
+    const uint32_t full = base + static_cast<uint32_t>(S) * p.stage_bytes;   // S barriers each
+    const uint32_t computed = full + 8u * S;
+    const uint32_t empty = computed + 8u * S;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 8u * S - base));
 
+    const int warp = threadIdx.x / 32;
+    const int compute_warps = blockDim.x / 32 - 2;
     const int64_t G = gridDim.x;
     const int64_t cta = blockIdx.x;
     const int64_t N = cta < p.tiles ? (p.tiles - 1 - cta) / G + 1 : 0;
-    const bool producer = threadIdx.x < 32 && elect_one();
+    const bool elected = warp < 2 && elect_one();   // one lane of warp 0 and of warp 1
 
-    // Pre-prologue: one barrier per stage, a single arrival each.
-    if (producer) {
-        for (int s = 0; s < S; ++s)
-            mbar_init(bars + 8u * s, 1);
+    // Pre-prologue: the barriers of every stage; descriptor prefetch.
+    if (warp == 0 && elected) {
+        for (int j = 0; j < NIN; ++j)
+            prefetch_tensormap(&maps.m[j]);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + 8u * s, 1);
+            mbar_init(computed + 8u * s, static_cast<uint32_t>(compute_warps));
+            mbar_init(empty + 8u * s, 1);
+        }
+        *abort_flag = 0;
         fence_proxy_async_smem();
     }
+    if (warp == 1 && elected)
+        prefetch_tensormap(&maps.m[3]);
     __syncthreads();
 
-    // Prologue: loads of the first S - 1 tiles.
-    int64_t issued = 0;
-    if (producer) {
-        const int64_t pro = N < S - 1 ? N : S - 1;
-        for (; issued < pro; ++issued)
-            issue_tile<NIN>(maps, p, base + (issued % S) * p.stage_bytes, bars + 8u * (issued % S),
-                            cta + issued * G);
-    }
-
-    // Main loop: issue tile i + S - 1, consume tile i.
-    const int64_t main_iters = N > S - 1 ? N - (S - 1) : 0;
-    int64_t i = 0;
-    bool failed = false;
-    for (; i < main_iters; ++i) {
-        if (producer) {
-            const int64_t k = i + S - 1;
-            // stage k mod S last held tile i - 1: its store must be done reading
-            bulk_wait_read_all();
-            issue_tile<NIN>(maps, p, base + (k % S) * p.stage_bytes, bars + 8u * (k % S), cta + k * G);
-            issued = k + 1;
-        }
-        if (!consume_tile<DT, OP, NIN>(maps, p, smem, base, bars, i, cta + i * G, producer)) {
-            failed = true;
-            break;
-        }
-    }
-    // Epilogue: consume the remaining tiles.
-    if (!failed) {
-        for (; i < N; ++i) {
-            if (!consume_tile<DT, OP, NIN>(maps, p, smem, base, bars, i, cta + i * G, producer)) {
-                failed = true;
-                break;
+    if (warp == 0) {
+        // ---------------------------------------------------- producer
+        if (elected) {
+            int64_t issued = 0;
+            const int64_t pro = N < S - 1 ? N : S - 1;
+            // Prologue: the first S - 1 tiles, into stages that start empty.
+            for (; issued < pro; ++issued)
+                issue_tile<NIN>(maps, p, base + (issued % S) * p.stage_bytes, full + 8u * (issued % S),
+                                cta + issued * G);
+            // Main loop: tile k = i + S - 1 into stage k mod S, once the
+            // store warp has released that stage's previous tile (k - S).
+            for (; issued < N; ++issued) {
+                const int64_t k = issued;
+                const uint32_t s = static_cast<uint32_t>(k % S);
+                if (k >= S && !wait_or_abort(empty + 8u * s, static_cast<uint32_t>((k / S - 1) & 1), p, abort_flag))
+                    break;
+                issue_tile<NIN>(maps, p, base + s * p.stage_bytes, full + 8u * s, cta + k * G);
             }
+            if (*abort_flag) {
+                // let the loads still in flight land before shared memory goes away
+                const int64_t first = issued > S ? issued - S : 0;
+                for (int64_t k = first; k < issued; ++k)
+                    (void)mbar_wait(full + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- store warp
+        if (elected) {
+            const int lag = p.store_lag < S - 1 ? p.store_lag : S - 1;
+            for (int64_t i = 0; i < N; ++i) {
+                const uint32_t s = static_cast<uint32_t>(i % S);
+                const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
+                // copy has no compute step: the loaded tile goes straight back
+                const uint32_t ready = OP == TSX_COPY ? full : computed;
+                if (!wait_or_abort(ready + 8u * s, parity, p, abort_flag))
+                    break;
+                store_tile(maps, p, base + s * p.stage_bytes, cta + i * G);
+                // release tile i - lag once its store has read shared memory
+                bulk_wait_read(lag);
+                if (i >= lag)
+                    mbar_arrive(empty + 8u * static_cast<uint32_t>((i - lag) % S));
+            }
+            bulk_wait_all();
+        }
+    } else if (OP != TSX_COPY) {
+        // ---------------------------------------------- compute warps
+        const uint32_t tid = threadIdx.x - 64;
+        const uint32_t threads = blockDim.x - 64;
+        for (int64_t i = 0; i < N; ++i) {
+            const uint32_t s = static_cast<uint32_t>(i % S);
+            if (!wait_or_abort(full + 8u * s, static_cast<uint32_t>((i / S) & 1), p, abort_flag))
+                break;
+            uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
+            const uint4* B = A + p.slot_bytes / 16;
+            const uint4* C = A + 2 * (p.slot_bytes / 16);
+            for (uint32_t u = tid; u < p.vec16_per_slot; u += threads) {
+                const uint4 va = A[u];
+                const uint4 vb = NIN > 1 ? B[u] : va;
+                const uint4 vc = NIN > 2 ? C[u] : va;
+                A[u] = op_vec16<DT, OP>(va, vb, vc);
+            }
+            // this thread's generic-proxy writes become visible to the TMA store
+            fence_proxy_async_smem();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0)
+                mbar_arrive(computed + 8u * s);
         }
     }
 
     // Post-epilogue.
-    if (producer) {
-        if (failed) {
-            atomicCAS(p.status, TSX_OK, TSX_ERR_TIMEOUT);
-            // let loads still in flight land before the CTA's shared memory goes away
-            for (int64_t k = i; k < issued; ++k)
-                (void)mbar_wait(bars + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
-        }
-        bulk_wait_all();
-    }
     __syncthreads();
-    if (producer) {
-        for (int s = 0; s < S; ++s)
-            mbar_inval(bars + 8u * s);
+    if (warp == 0 && elected) {
+        for (int s = 0; s < S; ++s) {
+            mbar_inval(full + 8u * s);
+            mbar_inval(computed + 8u * s);
+            mbar_inval(empty + 8u * s);
+        }
     }
 }
 

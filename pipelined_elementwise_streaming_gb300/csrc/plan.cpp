@@ -36,16 +36,33 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-int default_threads(int variant)
+int default_threads(int variant, uint32_t slot_bytes)
 {
-    // 256 threads for the TMA paths (8 warps share one elected producer
-    // lane); 128 for the cp.async / synchronous ablations, the thread count
-    // of the TVM ldgsts demonstration program.
-    const int fallback = (variant == TSX_TMA || variant == TSX_TMA_RANK3) ? 256 : 128;
+    // Threads of the elementwise stage.  TMA paths: about four 16-byte
+    // vectors of a slot per thread, between 2 and 8 compute warps (beside
+    // the producer and store warps) -- small tiles leave room for more CTAs
+    // per SM, large ones need the warps for the arithmetic.  The cp.async /
+    // synchronous ablations use 128, the thread count of the TVM ldgsts
+    // demonstration program.  TSX_THREADS overrides (a multiple of 32).
+    const bool tma = variant == TSX_TMA || variant == TSX_TMA_RANK3;
+    int fallback = 128;
+    if (tma) {
+        const int per_four = int(slot_bytes / 16 / 4);
+        fallback = per_four < 64 ? 64 : per_four > 256 ? 256 : (per_four + 31) / 32 * 32;
+    }
+    const int limit = tma ? kMaxThreads - 32 * kTmaRoleWarps : kMaxThreads;
     int t = env_int("TSX_THREADS", fallback);
-    if (t < 32 || t > kMaxThreads || t % 32)
+    if (t < 32 || t > limit || t % 32)
         t = fallback;
     return t;
+}
+
+int default_store_lag(int stages)
+{
+    // tiles between a store's issue and the release of its stage: one for
+    // shallow rings, two once there are enough stages to keep loads ahead
+    int lag = env_int("TSX_STORE_LAG", stages >= 6 ? 2 : 1);
+    return lag < 0 ? 0 : lag > 3 ? 3 : lag;
 }
 
 int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
@@ -77,7 +94,6 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
     g->tiles_r = rows == 0 ? 0 : (rows + box_rows - 1) / box_rows;
     g->tiles_c = cols == 0 ? 0 : (cols + box_cols - 1) / box_cols;
     g->tiles = g->tiles_r * g->tiles_c;
-    g->threads = default_threads(variant);
 
     const int64_t row_bytes = int64_t(box_cols) * es;
     const int64_t tile_bytes = row_bytes * box_rows;
@@ -150,6 +166,9 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
         g->copy_vec_bytes = vb;
         g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
     }
+    g->threads = default_threads(variant, g->slot_bytes);
+    g->block_threads = g->threads + ((variant == TSX_TMA || variant == TSX_TMA_RANK3) ? 32 * kTmaRoleWarps : 0);
+    g->store_lag = default_store_lag(stages);
     return TSX_OK;
 }
 
@@ -166,7 +185,8 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     if (tma) {
         // expect_tx of a stage: every load of every operand
         og->tx_bytes = uint32_t(og->n_in) * uint32_t(g.loads_per_operand) * uint32_t(g.bytes_per_load);
-        og->smem_bytes = size_t(stages) * og->stage_bytes + size_t(stages) * 8 + kSmemAlign;
+        // stages, three barriers per stage, the abort flag, alignment slack
+        og->smem_bytes = size_t(stages) * og->stage_bytes + size_t(stages) * kTmaBarrierBytes + 16 + kSmemAlign;
     } else {
         og->tx_bytes = 0;
         og->smem_bytes = size_t(stages) * og->stage_bytes;
@@ -207,6 +227,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->bytes_per_load = g.bytes_per_load;
     info->tx_bytes = int32_t(og.tx_bytes);
     info->threads = g.threads;
+    info->block_threads = g.block_threads;
     info->vec = og.vec;
     info->outer = og.outer;
     info->copy_vec_bytes = g.copy_vec_bytes;

@@ -15,7 +15,9 @@ struct Geometry {
     int64_t rows = 0, cols = 0;
     int box_rows = 0, box_cols = 0;
     int64_t tiles_r = 0, tiles_c = 0, tiles = 0;
-    int threads = 0;
+    int threads = 0;         // threads of the elementwise stage ([outer, threads, vec])
+    int block_threads = 0;   // threads of a CTA (TMA: + producer and store warps)
+    int store_lag = 1;       // TMA: tiles between a store's issue and its stage's release
     // TMA split
     int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
     int loads_per_operand = 0, bytes_per_load = 0, swizzle_bytes = 0;
@@ -42,7 +44,8 @@ struct TensorMapArgs {
     int swizzle = 0;   // CUtensorMapSwizzle value
 };
 
-int default_threads(int variant);
+int default_threads(int variant, uint32_t slot_bytes);
+int default_store_lag(int stages);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
                   Geometry* g, std::string* why);
 int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, std::string* why);

@@ -50,6 +50,11 @@ __device__ __forceinline__ void mbar_inval(uint32_t bar)
     asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // The single arrival of a stage: announces the bytes its loads will deliver.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
@@ -130,10 +135,25 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                  : "memory");
 }
 
+// Pull a tensor map into the TMA unit's descriptor cache ahead of its use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// All committed bulk stores have finished reading their shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// All but the n most recently committed bulk store groups have finished
+// reading their shared memory.
+__device__ __forceinline__ void bulk_wait_read(int n)
+{
+    switch (n) {
+    case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+    }
+}
 
 // All committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -188,6 +208,14 @@ __device__ __forceinline__ float op_f32(float a, float b, float c)
 __device__ __forceinline__ float u32_as_f32(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f32_as_u32(float x) { return __float_as_uint(x); }
 
+// exp of a 16-bit element, evaluated in fp32 with CUDA's fast intrinsic
+// __expf.  Its documented error is at most 2 + floor(|1.173 x|) fp32 ulps,
+// i.e. a relative error below 2^-14 for every |x| <= 100, where the results
+// of both 16-bit types are neither 0 nor infinite.  That is far below half
+// an ulp of fp16 (2^-11 relative) and bf16 (2^-8), so after rounding to the
+// element type the result is within 1 ulp of exp(x).
+__device__ __forceinline__ float exp_for_16bit(float x) { return __expf(x); }
+
 // Two 16-bit elements packed in 32 bits (low half first).
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
@@ -203,7 +231,10 @@ __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
             float2 fb = make_float2(0.f, 0.f);
             if constexpr (OP == TSX_ADD || OP == TSX_MUL)
                 fb = __half22float2(*reinterpret_cast<const __half2*>(&b));
-            r = __floats2half2_rn(op_f32<OP>(fa.x, fb.x, 0.f), op_f32<OP>(fa.y, fb.y, 0.f));
+            if constexpr (OP == TSX_EXP)
+                r = __floats2half2_rn(exp_for_16bit(fa.x), exp_for_16bit(fa.y));
+            else
+                r = __floats2half2_rn(op_f32<OP>(fa.x, fb.x, 0.f), op_f32<OP>(fa.y, fb.y, 0.f));
         }
         return *reinterpret_cast<uint32_t*>(&r);
     } else {
@@ -217,7 +248,10 @@ __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
             float2 fb = make_float2(0.f, 0.f);
             if constexpr (OP == TSX_ADD || OP == TSX_MUL)
                 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
-            r = __floats2bfloat162_rn(op_f32<OP>(fa.x, fb.x, 0.f), op_f32<OP>(fa.y, fb.y, 0.f));
+            if constexpr (OP == TSX_EXP)
+                r = __floats2bfloat162_rn(exp_for_16bit(fa.x), exp_for_16bit(fa.y));
+            else
+                r = __floats2bfloat162_rn(op_f32<OP>(fa.x, fb.x, 0.f), op_f32<OP>(fa.y, fb.y, 0.f));
         }
         return *reinterpret_cast<uint32_t*>(&r);
     }

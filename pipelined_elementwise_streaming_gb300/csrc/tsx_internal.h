@@ -23,6 +23,8 @@ constexpr int kSmemAlign = 1024;       // 128-B swizzle pattern period
 constexpr int kBoxMax = 256;           // per TMA box dimension
 constexpr int kSwizzleAtom = 128;      // bytes
 constexpr int kMaxDynSmem = 232448;    // 227 KiB opt-in per CTA on sm_100 / sm_103
+constexpr int kTmaRoleWarps = 2;       // producer warp + store warp ahead of the compute warps
+constexpr int kTmaBarrierBytes = 24;   // full, computed and empty mbarriers of one stage
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
 TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }
@@ -34,6 +36,7 @@ struct TmaArgs {
     int64_t fault_tile;     // test hook: the producer skips this tile's loads (-1: none)
     int* status;            // device status word (TSX_OK until a wait gives up)
     uint64_t timeout_ns;    // limit of every mbarrier wait
+    int store_lag;          // tiles between a store's issue and its stage's release
     int rows, cols;         // tensor extent (< 2^31)
     int box_rows, box_cols;
     int stages;

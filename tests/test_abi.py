@@ -98,7 +98,24 @@ def test_query_workload_plans(tsx):
     q = tsx.query("bf16", 16384, 16384, (128, 128), 4, "tma", "exp")
     assert (q["loads_per_operand"], q["tx_bytes"], q["box_dim"][:2]) == (2, 32768, [64, 128])
     q = tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")
-    assert (q["vec"], q["outer"], q["threads"], q["tiles"]) == (4, 1, 256, 16 * 128)
+    assert (q["vec"], q["tiles"]) == (4, 16 * 128)
+    assert q["block_threads"] == q["threads"] + 64        # + producer warp and store warp
+
+
+def test_query_partition_of_the_smem_sqrt_demo(tsx, monkeypatch):
+    """With 256 elementwise threads, a 32x32 float32 tile is one round of
+    float4 vectors (TVM "elementwise -> smem", Algorithm step 2)."""
+    monkeypatch.setenv("TSX_THREADS", "256")
+    q = tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")
+    assert (q["vec"], q["outer"], q["threads"]) == (4, 1, 256)
+
+
+def test_query_default_threads_follow_the_slot(tsx):
+    """About four 16-byte vectors of a slot per thread, 2 to 8 warps."""
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma")["threads"] == 64
+    assert tsx.query("f16", 1024, 8192, (64, 64), 2, "tma", "add")["threads"] == 128
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "exp")["threads"] == 256
+    assert tsx.query("f16", 500, 4096, (128, 32), 2, "ldgsts", "sqrt")["threads"] == 128
 
 
 def test_query_partition_matches_oracle(tsx):

@@ -220,6 +220,7 @@ class Workload:
     stages: tuple = (2,)
     variant: str = "tma"
     note: str = field(default="", compare=False)
+    bench_stages: int = 0     # the stage count the benchmark uses (0: the last stated one)
 
     @property
     def n_in(self) -> int:
@@ -233,6 +234,16 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Bytes read plus bytes written by one pass: (n_in + 1) * elems * es."""
         return (self.n_in + 1) * self.elems * ELEM_SIZE[self.dtype]
+
+    def with_rows(self, rows: int) -> "Workload":
+        """The same workload over its first ``rows`` rows (a smaller case)."""
+        from dataclasses import replace
+
+        return replace(self, rows=int(rows))
+
+    @property
+    def default_stages(self) -> int:
+        return self.bench_stages or self.stages[-1]
 
     def inputs(self) -> list:
         return [generate(self.rows, self.cols, self.dtype, self.dist, self.seed, t) for t in range(self.n_in)]
@@ -255,6 +266,6 @@ WORKLOADS = {
         Workload("fma_128x1048576_f32", "f32", 128, 1 << 20, "fma", Dist("uniform", -2.0, 2.0), 3, 8, 128, (4,),
                  note="stage tile 8x128 = four 8x32 TMA boxes per operand"),
         Workload("exp_16384x16384_bf16", "bf16", 16384, 16384, "exp", Dist("uniform", -8.0, 8.0), 4, 128, 128, (2, 3, 4),
-                 note="128x128 stage tile = two 128x64 TMA boxes"),
+                 note="128x128 stage tile = two 128x64 TMA boxes", bench_stages=3),
     )
 }
