@@ -18,17 +18,31 @@ namespace tsx {
 
 namespace {
 
-thread_local std::string g_last_error;
+// The last error message of the calling thread, in a fixed buffer so that
+// reporting an error never allocates (longer messages are cut short).
+thread_local char g_last_error[512];
+
+void store_message(const char* a, const char* b = nullptr)
+{
+    std::snprintf(g_last_error, sizeof g_last_error, "%s%s%s", a ? a : "", b ? ": " : "", b ? b : "");
+}
 
 int set_error(int rc, const std::string& msg)
 {
-    g_last_error = msg;
+    store_message(msg.c_str());
+    return rc;
+}
+
+int set_error(int rc, const char* msg)
+{
+    store_message(msg);
     return rc;
 }
 
 int cuda_error(cudaError_t e, const char* what)
 {
-    return set_error(TSX_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    store_message(what, cudaGetErrorString(e));
+    return TSX_ERR_CUDA;
 }
 
 int64_t env_i64(const char* name, int64_t fallback)
@@ -75,7 +89,7 @@ CUtensorMapDataType map_dtype(int dtype)
 
 }  // namespace
 
-void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+void set_last_error(const char* msg) { store_message(msg); }
 
 }  // namespace tsx
 
@@ -289,7 +303,7 @@ int tsx_plan_status(tsx_plan_t p)
     return read_status(p, true);
 }
 
-const char* tsx_last_error(void) { return g_last_error.c_str(); }
+const char* tsx_last_error(void) { return g_last_error; }
 
 int tsx_plan_get_info(tsx_plan_t p, tsx_op op, tsx_plan_info* info)
 {
