@@ -171,6 +171,40 @@ int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, in
  * device (occupancy-derived CTAs per SM and grid). */
 int tsx_plan_get_info(tsx_plan_t plan, tsx_op op, tsx_plan_info *info);
 
+/* tsx_ewise for callers that may not allocate device memory.  The paper has
+ * no counterpart of this entry point: it is an addition for such callers.
+ * Some callers cannot call cudaMalloc: a plugin that may only use the memory
+ * its host engine hands it, a framework whose pooling allocator has reserved
+ * the device memory, a latency-critical loop that cannot afford the device
+ * synchronisation cudaMalloc / cudaFree may cause.  tsx_plan_create
+ * allocates a device status word, so this one call does the whole job
+ * without a plan and allocates nothing, host or device.
+ *
+ * It runs the same TMA kernel as tsx_ewise (variant TSX_TMA or
+ * TSX_TMA_RANK3 only, else TSX_ERR_INVALID) with the same argument rules and
+ * results: `a`..`out` as in tsx_ewise; dtype, shape, box, stages and variant
+ * as in tsx_plan_create (TSX_ERR_UNSUPPORTED when no plan would be legal).
+ * Tensor maps are encoded on every call.
+ *
+ * Scratch: the kernel's device status word lives in a file-scope device
+ * array of 256 bytes, which every GPU that loads the library holds until the
+ * process exits; a call needs 4 bytes of it, and a call that needed more
+ * would be rejected with TSX_ERR_UNSUPPORTED.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Every
+ * call on a device shares the array: each call clears the status word on
+ * `stream` before its kernel, so calls whose work overlaps on the GPU (other
+ * streams, or other host threads) race on it and may report each other's
+ * status.
+ *
+ * Returns once the work is queued on `stream`, or an error code for a
+ * host-side / launch failure (tsx_last_error() says why).  If `status_out`
+ * is not NULL the call also waits for `stream` and stores the device status
+ * there (TSX_OK, or TSX_ERR_TIMEOUT if a device-side wait gave up). */
+int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
+                      tsx_variant variant, tsx_op op, const void *a, const void *b, const void *c, void *out,
+                      tsx_stream_t stream, int *status_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -82,6 +82,10 @@ def _load():
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
     L.tsx_plan_get_info.restype = ctypes.c_int
     L.tsx_plan_get_info.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
+    L.tsx_ewise_noalloc.restype = ctypes.c_int
+    L.tsx_ewise_noalloc.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5 + \
+                                   [ctypes.POINTER(ctypes.c_int)]
     return L
 
 
@@ -94,6 +98,9 @@ tsx_plan_destroy = lib.tsx_plan_destroy
 tsx_plan_status = lib.tsx_plan_status
 tsx_plan_query = lib.tsx_plan_query
 tsx_plan_get_info = lib.tsx_plan_get_info
+# The plan-free, allocation-free form of tsx_ewise (device status word in a
+# static device array; see include/tsx.h for who needs it and its limits).
+tsx_ewise_noalloc = lib.tsx_ewise_noalloc
 
 
 def tsx_last_error() -> str:

@@ -164,14 +164,20 @@ int prepare_op(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
     return TSX_OK;
 }
 
-int encode_map(tsx_plan* p, const void* ptr, CUtensorMap* map)
+int encode_map(tsx_plan* p, const void* ptr, CUtensorMap* map) { return encode_tensor_map(p->g, ptr, map); }
+
+}  // namespace
+
+namespace tsx {
+
+int encode_tensor_map(const Geometry& g, const void* ptr, CUtensorMap* map)
 {
     std::string why;
     EncodeTiledFn fn = encode_fn(&why);
     if (!fn)
         return set_error(TSX_ERR_CUDA, why);
     TensorMapArgs m;
-    tensor_map_args(p->g, &m);
+    tensor_map_args(g, &m);
     cuuint64_t dims[5], strides[4];
     cuuint32_t box[5], estr[5];
     for (int d = 0; d < m.rank; ++d) {
@@ -181,7 +187,7 @@ int encode_map(tsx_plan* p, const void* ptr, CUtensorMap* map)
     }
     for (int d = 0; d + 1 < m.rank; ++d)
         strides[d] = m.strides[d];
-    const CUresult r = fn(map, map_dtype(p->g.dtype), cuuint32_t(m.rank), const_cast<void*>(ptr), dims, strides, box,
+    const CUresult r = fn(map, map_dtype(g.dtype), cuuint32_t(m.rank), const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(m.swizzle),
                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -191,6 +197,10 @@ int encode_map(tsx_plan* p, const void* ptr, CUtensorMap* map)
     }
     return TSX_OK;
 }
+
+}  // namespace tsx
+
+namespace {
 
 // The tensor map of `ptr`, from the plan's cache or freshly encoded.
 int get_map(tsx_plan* p, const void* ptr, CUtensorMap* out)

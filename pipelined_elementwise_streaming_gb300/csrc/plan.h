@@ -55,4 +55,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info);
 // Thread-local message behind tsx_last_error (capi.cpp).
 void set_last_error(const char* msg);
 
+// Encode the tensor map of base pointer `ptr` for geometry g (capi.cpp).
+int encode_tensor_map(const Geometry& g, const void* ptr, CUtensorMap* map);
+
 }  // namespace tsx
