@@ -147,7 +147,7 @@ int prepare_op(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         if (e != cudaSuccess)
             return cuda_error(e, "cudaFuncSetAttribute");
         int blocks = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, p->g.block_threads, L.og.smem_bytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, L.og.block_threads, L.og.smem_bytes);
         if (e != cudaSuccess)
             return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (blocks < 1)
@@ -396,7 +396,7 @@ int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void*
         args.bytes_per_load = uint32_t(g.bytes_per_load);
         args.vec16_per_slot = L->og.vec16_per_slot;
         args.store_lag = g.store_lag;
-        e = launch_tma(g.dtype, op, L->grid, g.block_threads, L->og.smem_bytes, st, maps, args);
+        e = launch_tma(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args);
     } else {
         int vb = g.copy_vec_bytes < align ? g.copy_vec_bytes : align;
         if (vb < 4)
@@ -416,8 +416,8 @@ int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void*
         args.chunks_per_slot = args.tile_bytes / uint32_t(vb);
         args.vec16_per_slot = L->og.vec16_per_slot;
         e = g.variant == TSX_LDGSTS
-                ? launch_ldgsts(g.dtype, op, L->grid, g.block_threads, L->og.smem_bytes, st, a, b, c, out, args)
-                : launch_sync(g.dtype, op, L->grid, g.block_threads, L->og.smem_bytes, st, a, b, c, out, args);
+                ? launch_ldgsts(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, a, b, c, out, args)
+                : launch_sync(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, a, b, c, out, args);
     }
     if (e != cudaSuccess)
         return cuda_error(e, "kernel launch");

@@ -36,19 +36,21 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-int default_threads(int variant, uint32_t slot_bytes)
+int default_threads(int variant, size_t smem_bytes)
 {
-    // Threads of the elementwise stage.  TMA paths: about four 16-byte
-    // vectors of a slot per thread, between 2 and 8 compute warps (beside
-    // the producer and store warps) -- small tiles leave room for more CTAs
-    // per SM, large ones need the warps for the arithmetic.  The cp.async /
-    // synchronous ablations use 128, the thread count of the TVM ldgsts
-    // demonstration program.  TSX_THREADS overrides (a multiple of 32).
+    // Threads of the elementwise stage.  TMA paths: about 256 compute
+    // threads per SM in all, shared by the CTAs that fit in its shared
+    // memory, between 2 and 8 compute warps per CTA (beside the producer
+    // and store warps).  The cp.async / synchronous ablations use 128, the
+    // thread count of the TVM ldgsts demonstration program.  TSX_THREADS
+    // overrides (a multiple of 32).
     const bool tma = variant == TSX_TMA || variant == TSX_TMA_RANK3;
     int fallback = 128;
     if (tma) {
-        const int per_four = int(slot_bytes / 16 / 4);
-        fallback = per_four < 64 ? 64 : per_four > 256 ? 256 : (per_four + 31) / 32 * 32;
+        const size_t per_cta = smem_bytes + kSmemPerCtaReserved;
+        const int ctas = per_cta ? int(kSmemPerSm / per_cta) : 1;
+        const int share = 256 / (ctas < 1 ? 1 : ctas);
+        fallback = share < 64 ? 64 : share > 256 ? 256 : share / 32 * 32;
     }
     const int limit = tma ? kMaxThreads - 32 * kTmaRoleWarps : kMaxThreads;
     int t = env_int("TSX_THREADS", fallback);
@@ -166,8 +168,6 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
         g->copy_vec_bytes = vb;
         g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
     }
-    g->threads = default_threads(variant, g->slot_bytes);
-    g->block_threads = g->threads + ((variant == TSX_TMA || variant == TSX_TMA_RANK3) ? 32 * kTmaRoleWarps : 0);
     g->store_lag = default_store_lag(stages);
     return TSX_OK;
 }
@@ -194,10 +194,12 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     if (og->smem_bytes > size_t(max_smem))
         return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
                TSX_ERR_UNSUPPORTED;
+    og->threads = default_threads(g.variant, og->smem_bytes);
+    og->block_threads = og->threads + (tma ? 32 * kTmaRoleWarps : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;
     const uint32_t units = g.slot_bytes / 16;
-    og->outer = int((units + g.threads - 1) / g.threads);
+    og->outer = int((units + og->threads - 1) / og->threads);
     og->vec16_per_slot = units;
     return TSX_OK;
 }
@@ -226,8 +228,8 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->loads_per_operand = g.loads_per_operand;
     info->bytes_per_load = g.bytes_per_load;
     info->tx_bytes = int32_t(og.tx_bytes);
-    info->threads = g.threads;
-    info->block_threads = g.block_threads;
+    info->threads = og.threads;
+    info->block_threads = og.block_threads;
     info->vec = og.vec;
     info->outer = og.outer;
     info->copy_vec_bytes = g.copy_vec_bytes;

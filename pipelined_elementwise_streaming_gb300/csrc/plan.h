@@ -15,8 +15,6 @@ struct Geometry {
     int64_t rows = 0, cols = 0;
     int box_rows = 0, box_cols = 0;
     int64_t tiles_r = 0, tiles_c = 0, tiles = 0;
-    int threads = 0;         // threads of the elementwise stage ([outer, threads, vec])
-    int block_threads = 0;   // threads of a CTA (TMA: + producer and store warps)
     int store_lag = 1;       // TMA: tiles between a store's issue and its stage's release
     // TMA split
     int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
@@ -33,6 +31,8 @@ struct OpGeometry {
     int op = 0, n_in = 0;
     uint32_t stage_bytes = 0, tx_bytes = 0, vec16_per_slot = 0;
     size_t smem_bytes = 0;
+    int threads = 0;         // threads of the elementwise stage ([outer, threads, vec])
+    int block_threads = 0;   // threads of a CTA (TMA: + producer and store warps)
     int vec = 0, outer = 0;
 };
 
@@ -44,7 +44,7 @@ struct TensorMapArgs {
     int swizzle = 0;   // CUtensorMapSwizzle value
 };
 
-int default_threads(int variant, uint32_t slot_bytes);
+int default_threads(int variant, size_t smem_bytes);
 int default_store_lag(int stages);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
                   Geometry* g, std::string* why);

@@ -23,6 +23,8 @@ constexpr int kSmemAlign = 1024;       // 128-B swizzle pattern period
 constexpr int kBoxMax = 256;           // per TMA box dimension
 constexpr int kSwizzleAtom = 128;      // bytes
 constexpr int kMaxDynSmem = 232448;    // 227 KiB opt-in per CTA on sm_100 / sm_103
+constexpr int kSmemPerSm = 233472;     // 228 KiB of shared memory per SM
+constexpr int kSmemPerCtaReserved = 1024;  // the system's share of each resident CTA
 constexpr int kTmaRoleWarps = 2;       // producer warp + store warp ahead of the compute warps
 constexpr int kTmaBarrierBytes = 24;   // full, computed and empty mbarriers of one stage
 

@@ -110,11 +110,14 @@ def test_query_partition_of_the_smem_sqrt_demo(tsx, monkeypatch):
     assert (q["vec"], q["outer"], q["threads"]) == (4, 1, 256)
 
 
-def test_query_default_threads_follow_the_slot(tsx):
-    """About four 16-byte vectors of a slot per thread, 2 to 8 warps."""
-    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma")["threads"] == 64
-    assert tsx.query("f16", 1024, 8192, (64, 64), 2, "tma", "add")["threads"] == 128
-    assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "exp")["threads"] == 256
+def test_query_default_threads_share_the_sm(tsx):
+    """About 256 elementwise threads per SM, split over the CTAs that fit in
+    its shared memory, 2 to 8 compute warps per CTA."""
+    q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma")      # 4 CTAs / SM
+    assert (q["threads"], q["block_threads"]) == (64, 128)
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "exp")["threads"] == 128   # 2 CTAs / SM
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 4, "tma", "exp")["threads"] == 256   # 1 CTA / SM
+    assert tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")["threads"] == 64          # many small CTAs
     assert tsx.query("f16", 500, 4096, (128, 32), 2, "ldgsts", "sqrt")["threads"] == 128
 
 
