@@ -60,8 +60,13 @@ typedef enum { TSX_F16 = 0, TSX_BF16 = 1, TSX_F32 = 2 } tsx_dtype;
  *                stage; ablation (stages is ignored beyond validation).
  *  TSX_TMA_RANK3 as TSX_TMA, but one rank-3 box covers all 128-byte atoms of
  *                a row chunk ("copy_async -> tma", "Generated TIRx IR");
- *                needs cols to be a whole number of atoms. */
-typedef enum { TSX_TMA = 0, TSX_LDGSTS = 1, TSX_SYNC = 2, TSX_TMA_RANK3 = 3 } tsx_variant;
+ *                needs cols to be a whole number of atoms.
+ *  TSX_TMA_MIXED as TSX_TMA for a (and c), while b is read by the compute
+ *                threads with plain vector loads from global memory: one
+ *                operand through the TMA circular buffer, the other through
+ *                ordinary loads (nvFuser PR #2833, "Testing Setup",
+ *                Pointwise).  Unary ops run as TSX_TMA. */
+typedef enum { TSX_TMA = 0, TSX_LDGSTS = 1, TSX_SYNC = 2, TSX_TMA_RANK3 = 3, TSX_TMA_MIXED = 4 } tsx_variant;
 
 /* Elementwise ops ("elementwise -> smem", table under "How inputs change
  * the algorithm").  copy moves bits unchanged; sqrt and add/mul/fma are

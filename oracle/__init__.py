@@ -16,9 +16,11 @@ Contents
 
 Every function here is pinned by a ``-m "not gpu"`` test against something
 other than itself (printed values, library routines, exact rational
-arithmetic, brute force).  One part is "parity unpinned": the 128-byte
-swizzle layout of shared memory is not modelled here at all (the pages print
-no swizzled address), so only the round-trip identity covers it.
+arithmetic, brute force).  The swizzled shared-memory layout is not modelled
+here at all (the pages print no swizzled address): no oracle function stands
+for it.  The CUDA path's handling of it is checked end to end instead, by the
+copy round trip and by the mixed-load variant, whose directly loaded operand
+pairs with the wrong elements unless the swizzle is read correctly.
 """
 
 from __future__ import annotations

@@ -24,7 +24,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtsx.so")
 
 DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
-VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3}
+VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3, "tma_mixed": 4}
 OPS = {"copy": 0, "sqrt": 1, "exp": 2, "add": 3, "mul": 4, "fma": 5}
 ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
 STATUS = {0: "TSX_OK", -1: "TSX_ERR_INVALID", -2: "TSX_ERR_UNSUPPORTED", -3: "TSX_ERR_ALIGN",

@@ -124,13 +124,16 @@ struct tsx_plan {
 
 namespace {
 
+// The mixed variant runs its own instantiation only for ops with a b operand.
+bool mixed_launch(int variant, int op) { return variant == TSX_TMA_MIXED && op_arity(op) >= 2; }
+
 const void* kernel_of(int variant, int dtype, int op)
 {
     if (variant == TSX_LDGSTS)
         return ldgsts_kernel(dtype, op);
     if (variant == TSX_SYNC)
         return sync_kernel(dtype, op);
-    return tma_kernel(dtype, op);
+    return tma_kernel(dtype, op, mixed_launch(variant, op));
 }
 
 // Geometry, kernel attributes, occupancy and grid for one op (cached).
@@ -362,15 +365,22 @@ int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void*
         return rc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (g.variant == TSX_TMA || g.variant == TSX_TMA_RANK3) {
+    if (is_tma_variant(g.variant)) {
         if (align < 16)
             return set_error(TSX_ERR_ALIGN, "TMA needs 16-byte aligned base pointers");
+        const bool mixed = mixed_launch(g.variant, op);
+        // operands of the TMA ring in slot order; b is read directly when mixed
+        const void* staged[4] = {a, b, c, out};
+        if (mixed) {
+            staged[1] = c;
+            staged[2] = nullptr;
+        }
         CUtensorMap maps[4];
         std::memset(maps, 0, sizeof maps);
         for (int j = 0; j < 4; ++j) {
-            if (!ops[j])
+            if (!staged[j])
                 continue;
-            rc = get_map(p, ops[j], &maps[j]);
+            rc = get_map(p, staged[j], &maps[j]);
             if (rc != TSX_OK)
                 return rc;
         }
@@ -396,7 +406,10 @@ int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void*
         args.bytes_per_load = uint32_t(g.bytes_per_load);
         args.vec16_per_slot = L->og.vec16_per_slot;
         args.store_lag = g.store_lag;
-        e = launch_tma(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args);
+        args.set_operand = mixed ? b : nullptr;
+        args.box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
+        args.swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
+        e = launch_tma(g.dtype, op, mixed, L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args);
     } else {
         int vb = g.copy_vec_bytes < align ? g.copy_vec_bytes : align;
         if (vb < 4)

@@ -19,7 +19,12 @@
 //               their i-th tile), apply the op to 16-byte vectors (f *
 //               threads + tid) of each operand's slot, write the result over
 //               operand a's slot and arrive on `computed` (TVM docs
-//               "elementwise -> smem", "Algorithm").
+//               "elementwise -> smem", "Algorithm").  In the mixed variant
+//               operand b is not staged: the compute warps read it from
+//               global memory with plain vector loads at the positions of
+//               the staged vectors (nvFuser PR #2833, "Testing Setup",
+//               Pointwise: one tensor by TMA circular buffering, the other
+//               by ordinary loads).
 //
 // The producer follows the loop structure of the nvFuser page ("Loop
 // Structure", "Detailed Pseudo-Code"): a pre-prologue that initialises the
@@ -118,6 +123,44 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
     bulk_commit();
 }
 
+// Offset inside one TMA box in shared memory -> offset in the box's
+// row-major image.  The 128-, 64- and 32-byte swizzles exchange the 16-byte
+// chunks of a 128-byte line by XOR-ing the chunk index (address bits 4..6)
+// with address bits 7..9 (as many bits as the mode has), for boxes that
+// start on a 1024-byte boundary, as ours do; the map is its own inverse.
+__device__ __forceinline__ uint32_t unswizzle(uint32_t off, int mask)
+{
+    return off ^ (((off >> 7) & static_cast<uint32_t>(mask)) << 4);
+}
+
+// The op on one staged tile of the mixed variant: a (and c) from the slots,
+// b from global memory at the element the staged vector holds.
+template <int DT, int OP>
+__device__ __forceinline__ void compute_tile_mixed(const TmaArgs& p, uint4* A, const uint4* C, int64_t t,
+                                                   uint32_t tid, uint32_t threads)
+{
+    constexpr int ES = DT == TSX_F32 ? 4 : 2;
+    const TileBoxes tb = tile_boxes(p, t);
+    const char* Bg = static_cast<const char*>(p.set_operand);
+    const uint32_t inner_bytes = static_cast<uint32_t>(p.inner_elems) * ES;
+    for (uint32_t u = tid; u < p.vec16_per_slot; u += threads) {
+        const uint32_t off = u * 16;
+        const uint32_t load = off / p.load_smem_bytes;
+        const uint32_t within = off - load * p.load_smem_bytes;
+        uint4 vb = make_uint4(0, 0, 0, 0);
+        if (within < p.box_bytes) {
+            const uint32_t lo = unswizzle(within, p.swizzle_mask);
+            const int64_t row = tb.row0 + static_cast<int64_t>(load / p.atoms) * p.rows_per_load + lo / inner_bytes;
+            const int64_t col = tb.col0 + static_cast<int64_t>(load % p.atoms) * p.inner_elems + (lo % inner_bytes) / ES;
+            if (row < p.rows && col < p.cols)
+                vb = *reinterpret_cast<const uint4*>(Bg + (row * p.cols + col) * ES);
+        }
+        const uint4 va = A[u];
+        const uint4 vc = op_arity(OP) > 2 ? C[u] : va;
+        A[u] = op_vec16<DT, OP>(va, vb, vc);
+    }
+}
+
 // Bounded wait that also gives up when the CTA's abort flag is raised.  A
 // wait that runs out of time raises the flag and records the timeout.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const TmaArgs& p,
@@ -138,10 +181,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     return true;
 }
 
-template <int DT, int OP>
+template <int DT, int OP, bool MIXED>
 __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__ TmaMaps maps, const TmaArgs p)
 {
     constexpr int NIN = op_arity(OP);
+    // operands in the stage: all of them, or all but b in the mixed variant
+    constexpr int NT = MIXED ? tma_operands(TSX_TMA_MIXED, OP) : NIN;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
@@ -161,7 +206,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
 
     // Pre-prologue: the barriers of every stage; descriptor prefetch.
     if (warp == 0 && elected) {
-        for (int j = 0; j < NIN; ++j)
+        for (int j = 0; j < NT; ++j)
             prefetch_tensormap(&maps.m[j]);
         for (int s = 0; s < S; ++s) {
             mbar_init(full + 8u * s, 1);
@@ -182,7 +227,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             const int64_t pro = N < S - 1 ? N : S - 1;
             // Prologue: the first S - 1 tiles, into stages that start empty.
             for (; issued < pro; ++issued)
-                issue_tile<NIN>(maps, p, base + (issued % S) * p.stage_bytes, full + 8u * (issued % S),
+                issue_tile<NT>(maps, p, base + (issued % S) * p.stage_bytes, full + 8u * (issued % S),
                                 cta + issued * G);
             // Main loop: tile k = i + S - 1 into stage k mod S, once the
             // store warp has released that stage's previous tile (k - S).
@@ -191,7 +236,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
                 const uint32_t s = static_cast<uint32_t>(k % S);
                 if (k >= S && !wait_or_abort(empty + 8u * s, static_cast<uint32_t>((k / S - 1) & 1), p, abort_flag))
                     break;
-                issue_tile<NIN>(maps, p, base + s * p.stage_bytes, full + 8u * s, cta + k * G);
+                issue_tile<NT>(maps, p, base + s * p.stage_bytes, full + 8u * s, cta + k * G);
             }
             if (*abort_flag) {
                 // let the loads still in flight land before shared memory goes away
@@ -228,13 +273,17 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             if (!wait_or_abort(full + 8u * s, static_cast<uint32_t>((i / S) & 1), p, abort_flag))
                 break;
             uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
-            const uint4* B = A + p.slot_bytes / 16;
-            const uint4* C = A + 2 * (p.slot_bytes / 16);
-            for (uint32_t u = tid; u < p.vec16_per_slot; u += threads) {
-                const uint4 va = A[u];
-                const uint4 vb = NIN > 1 ? B[u] : va;
-                const uint4 vc = NIN > 2 ? C[u] : va;
-                A[u] = op_vec16<DT, OP>(va, vb, vc);
+            if constexpr (MIXED && NIN >= 2) {
+                compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, cta + i * G, tid, threads);
+            } else {
+                const uint4* B = A + p.slot_bytes / 16;
+                const uint4* C = A + 2 * (p.slot_bytes / 16);
+                for (uint32_t u = tid; u < p.vec16_per_slot; u += threads) {
+                    const uint4 va = A[u];
+                    const uint4 vb = NIN > 1 ? B[u] : va;
+                    const uint4 vc = NIN > 2 ? C[u] : va;
+                    A[u] = op_vec16<DT, OP>(va, vb, vc);
+                }
             }
             // this thread's generic-proxy writes become visible to the TMA store
             fence_proxy_async_smem();
@@ -255,17 +304,19 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     }
 }
 
-#define TSX_ROW(DT) \
-    {(const void*)tma_ewise<DT, 0>, (const void*)tma_ewise<DT, 1>, (const void*)tma_ewise<DT, 2>, \
-     (const void*)tma_ewise<DT, 3>, (const void*)tma_ewise<DT, 4>, (const void*)tma_ewise<DT, 5>}
-const void* const kKernels[3][6] = {TSX_ROW(TSX_F16), TSX_ROW(TSX_BF16), TSX_ROW(TSX_F32)};
+#define TSX_ROW(DT, M) \
+    {(const void*)tma_ewise<DT, 0, M>, (const void*)tma_ewise<DT, 1, M>, (const void*)tma_ewise<DT, 2, M>, \
+     (const void*)tma_ewise<DT, 3, M>, (const void*)tma_ewise<DT, 4, M>, (const void*)tma_ewise<DT, 5, M>}
+const void* const kKernels[2][3][6] = {
+    {TSX_ROW(TSX_F16, false), TSX_ROW(TSX_BF16, false), TSX_ROW(TSX_F32, false)},
+    {TSX_ROW(TSX_F16, true), TSX_ROW(TSX_BF16, true), TSX_ROW(TSX_F32, true)}};
 #undef TSX_ROW
 
 }  // namespace
 
-const void* tma_kernel(int dtype, int op) { return kKernels[dtype][op]; }
+const void* tma_kernel(int dtype, int op, bool mixed) { return kKernels[mixed ? 1 : 0][dtype][op]; }
 
-cudaError_t launch_tma(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
+cudaError_t launch_tma(int dtype, int op, bool mixed, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args)
 {
     TmaMaps m;
@@ -273,7 +324,7 @@ cudaError_t launch_tma(int dtype, int op, int grid, int threads, size_t smem, cu
         m.m[j] = maps[j];
     TmaArgs a = args;
     void* params[] = {&m, &a};
-    return cudaLaunchKernel(kKernels[dtype][op], dim3(grid), dim3(threads), params, smem, stream);
+    return cudaLaunchKernel(kKernels[mixed ? 1 : 0][dtype][op], dim3(grid), dim3(threads), params, smem, stream);
 }
 
 }  // namespace tsx

@@ -41,16 +41,20 @@ int default_threads(int variant, size_t smem_bytes)
     // Threads of the elementwise stage.  TMA paths: about 256 compute
     // threads per SM in all, shared by the CTAs that fit in its shared
     // memory, between 2 and 8 compute warps per CTA (beside the producer
-    // and store warps).  The cp.async / synchronous ablations use 128, the
-    // thread count of the TVM ldgsts demonstration program.  TSX_THREADS
-    // overrides (a multiple of 32).
-    const bool tma = variant == TSX_TMA || variant == TSX_TMA_RANK3;
+    // and store warps); the mixed variant, whose compute threads also wait
+    // on global loads of b, aims at 1024 per SM and up to 16 warps per CTA.
+    // The cp.async / synchronous ablations use 128, the thread count of the
+    // TVM ldgsts demonstration program.  TSX_THREADS overrides (a multiple
+    // of 32).
+    const bool tma = is_tma_variant(variant);
     int fallback = 128;
     if (tma) {
+        const bool mixed = variant == TSX_TMA_MIXED;
         const size_t per_cta = smem_bytes + kSmemPerCtaReserved;
         const int ctas = per_cta ? int(kSmemPerSm / per_cta) : 1;
-        const int share = 256 / (ctas < 1 ? 1 : ctas);
-        fallback = share < 64 ? 64 : share > 256 ? 256 : share / 32 * 32;
+        const int share = (mixed ? 1024 : 256) / (ctas < 1 ? 1 : ctas);
+        const int cap = mixed ? 512 : 256;
+        fallback = share < 64 ? 64 : share > cap ? cap : share / 32 * 32;
     }
     const int limit = tma ? kMaxThreads - 32 * kTmaRoleWarps : kMaxThreads;
     int t = env_int("TSX_THREADS", fallback);
@@ -73,7 +77,7 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
     *g = Geometry{};
     if (dtype < TSX_F16 || dtype > TSX_F32)
         return fail(why, "unknown dtype %lld", dtype), TSX_ERR_INVALID;
-    if (variant < TSX_TMA || variant > TSX_TMA_RANK3)
+    if (variant < TSX_TMA || variant > TSX_TMA_MIXED)
         return fail(why, "unknown variant %lld", variant), TSX_ERR_INVALID;
     if (rows < 0 || cols < 0)
         return fail(why, "negative shape %lld x %lld", rows, cols), TSX_ERR_INVALID;
@@ -102,7 +106,7 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
     if (tile_bytes > kMaxDynSmem)
         return fail(why, "a %lld-byte stage tile cannot fit in shared memory", tile_bytes), TSX_ERR_UNSUPPORTED;
 
-    if (variant == TSX_TMA || variant == TSX_TMA_RANK3) {
+    if (is_tma_variant(variant)) {
         // Global strides of a tensor map are multiples of 16 bytes.
         if ((cols * es) % 16)
             return fail(why, "TMA needs a row pitch that is a multiple of 16 bytes (cols * elem = %lld)", cols * es),
@@ -128,7 +132,7 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
         g->rows_per_load = box_rows / chunks;
         g->swizzle_bytes = (inner_bytes == 32 || inner_bytes == 64 || inner_bytes == 128) ? inner_bytes : 0;
         const uint32_t atom_bytes = uint32_t(g->rows_per_load) * inner_bytes;
-        if (variant == TSX_TMA) {
+        if (variant != TSX_TMA_RANK3) {
             g->loads_per_operand = g->atoms * g->row_chunks;
             g->bytes_per_load = int(atom_bytes);
             // each box lands on its own 1024-byte boundary: the swizzle
@@ -179,12 +183,13 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         return fail(why, "unknown op %lld", op), TSX_ERR_INVALID;
     og->op = op;
     og->n_in = op_arity(op);
-    og->stage_bytes = g.slot_bytes * uint32_t(og->n_in);
-    const bool tma = g.variant == TSX_TMA || g.variant == TSX_TMA_RANK3;
+    const bool tma = is_tma_variant(g.variant);
+    og->n_tma = tma ? tma_operands(g.variant, op) : 0;
+    og->stage_bytes = g.slot_bytes * uint32_t(tma ? og->n_tma : og->n_in);
     const int stages = g.variant == TSX_SYNC ? 1 : g.stages;
     if (tma) {
         // expect_tx of a stage: every load of every operand
-        og->tx_bytes = uint32_t(og->n_in) * uint32_t(g.loads_per_operand) * uint32_t(g.bytes_per_load);
+        og->tx_bytes = uint32_t(og->n_tma) * uint32_t(g.loads_per_operand) * uint32_t(g.bytes_per_load);
         // stages, three barriers per stage, the abort flag, alignment slack
         og->smem_bytes = size_t(stages) * og->stage_bytes + size_t(stages) * kTmaBarrierBytes + 16 + kSmemAlign;
     } else {
@@ -236,7 +241,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->slot_bytes = int32_t(g.slot_bytes);
     info->stage_bytes = int32_t(og.stage_bytes);
     info->smem_bytes = int32_t(og.smem_bytes);
-    if (g.variant == TSX_TMA || g.variant == TSX_TMA_RANK3) {
+    if (is_tma_variant(g.variant)) {
         TensorMapArgs m;
         tensor_map_args(g, &m);
         info->rank = m.rank;

@@ -29,6 +29,7 @@ struct Geometry {
 // What additionally depends on the op (operand count).
 struct OpGeometry {
     int op = 0, n_in = 0;
+    int n_tma = 0;           // operands loaded through the TMA ring
     uint32_t stage_bytes = 0, tx_bytes = 0, vec16_per_slot = 0;
     size_t smem_bytes = 0;
     int threads = 0;         // threads of the elementwise stage ([outer, threads, vec])

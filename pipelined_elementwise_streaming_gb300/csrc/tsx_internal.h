@@ -30,6 +30,12 @@ constexpr int kTmaBarrierBytes = 24;   // full, computed and empty mbarriers of 
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
 TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }
+TSX_HD constexpr bool is_tma_variant(int v) { return v == TSX_TMA || v == TSX_TMA_RANK3 || v == TSX_TMA_MIXED; }
+// Operands that go through the TMA ring: all of them, except b for the mixed variant.
+TSX_HD constexpr int tma_operands(int variant, int op)
+{
+    return variant == TSX_TMA_MIXED && op_arity(op) >= 2 ? op_arity(op) - 1 : op_arity(op);
+}
 
 // Kernel arguments of the TMA circular-buffer kernel.
 struct TmaArgs {
@@ -52,6 +58,10 @@ struct TmaArgs {
     uint32_t stage_bytes;      // n_in slots
     uint32_t bytes_per_load;   // bytes one box delivers (out-of-bounds part zero-filled)
     uint32_t vec16_per_slot;   // 16-byte units of one slot
+    // mixed variant: operand b, read by the compute threads from global memory
+    const void* set_operand;
+    uint32_t box_bytes;        // rows_per_load * inner bytes: the data part of one load
+    int swizzle_mask;          // 7, 3, 1 for the 128/64/32-byte swizzle, 0 for none
 };
 
 // Kernel arguments of the cp.async and synchronous ablation kernels.
@@ -70,8 +80,10 @@ struct CopyArgs {
 
 // Kernel lookup and launch, one set per variant (k_tma.cu, k_ldgsts.cu,
 // k_sync.cu).  `maps` holds the tensor maps of a, b, c and out.
-const void* tma_kernel(int dtype, int op);
-cudaError_t launch_tma(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
+// `mixed`: the TSX_TMA_MIXED instantiation.  maps[0..2] are the TMA-loaded
+// operands in slot order, maps[3] the output.
+const void* tma_kernel(int dtype, int op, bool mixed = false);
+cudaError_t launch_tma(int dtype, int op, bool mixed, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args);
 const void* ldgsts_kernel(int dtype, int op);
 cudaError_t launch_ldgsts(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,

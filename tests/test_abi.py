@@ -83,6 +83,19 @@ def test_query_matches_oracle_split_and_encode(tsx, dtype):
         assert (q["interleave"], q["swizzle"], q["l2_promotion"], q["oob_fill"]) == enc[-4:]
 
 
+def test_query_mixed_variant_stages_all_but_b(tsx):
+    """The mixed variant stages a (and c) through TMA; b is read directly,
+    so expect_tx counts one operand fewer for binary ops and fma."""
+    for op, n_tma in (("copy", 1), ("sqrt", 1), ("add", 1), ("mul", 1), ("fma", 2)):
+        q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma_mixed", op)
+        sp = st.split("f32", 8, 128)
+        assert q["tx_bytes"] == sp.tx_bytes(n_tma)
+        assert q["stage_bytes"] == n_tma * q["slot_bytes"]
+        full = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", op)
+        assert (q["loads_per_operand"], q["box_dim"], q["swizzle"]) == \
+            (full["loads_per_operand"], full["box_dim"], full["swizzle"])
+
+
 def test_query_rank3_demo_tuple(tsx):
     """The 8x256 float16 tile with the 128-B swizzle: the encode arguments
     printed by the TVM page ("copy_async -> tma", Generated TIRx IR)."""

@@ -34,7 +34,7 @@ def _embedded(bits, dtype, pad):
     return buf, buf[pad:pad + bits.size].view(bits.shape)
 
 
-@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "ldgsts", "sync"])
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "tma_mixed", "ldgsts", "sync"])
 def test_canaries_and_inputs_untouched(tsx, variant):
     dtype, rows, cols, box = "f32", 77, 320, (16, 64)
     ins = [random_bits(dtype, (rows, cols), 40 + k) for k in range(3)]
@@ -53,7 +53,7 @@ def test_canaries_and_inputs_untouched(tsx, variant):
         assert np.array_equal(bits_of(d, dtype), x)
 
 
-@pytest.mark.parametrize("variant", ["tma", "ldgsts"])
+@pytest.mark.parametrize("variant", ["tma", "tma_mixed", "ldgsts"])
 @pytest.mark.parametrize("alias", ["a", "b", "c"])
 def test_out_may_alias_an_input(tsx, variant, alias):
     dtype, rows, cols = "bf16", 130, 256

@@ -51,7 +51,7 @@ SHAPES = {
 }
 
 
-@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "ldgsts", "sync"])
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "tma_mixed", "ldgsts", "sync"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("op", OPS)
 def test_parity_small_shapes(tsx, variant, dtype, op):
@@ -70,12 +70,33 @@ def test_parity_small_shapes(tsx, variant, dtype, op):
     assert n >= 8
 
 
+@pytest.mark.parametrize("variant", ["tma", "tma_mixed"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_every_swizzle_mode(tsx, variant, dtype):
+    """Inner boxes of 16, 32, 48, 64, 128 bytes and rows of several 128-byte
+    atoms: every swizzle mode of the tensor map (none, 32, 64, 128 bytes).
+    In the mixed variant b is read from global memory at the positions the
+    staged vectors hold, so a wrong reading of the swizzle pairs the wrong
+    elements and fails here."""
+    es = 4 if dtype == "f32" else 2
+    n = 0
+    for row_bytes in (16, 32, 48, 64, 128, 256, 384):
+        box_cols = row_bytes // es
+        for box_rows, rows in ((8, 45), (3, 10), (16, 33)):
+            cols = 3 * box_cols + (16 // es if box_cols > 16 // es else 0)
+            for op in ("add", "fma"):
+                run_and_check(tsx, dtype, rows, cols, (box_rows, box_cols), 3, variant, op,
+                              seed=zlib.crc32(f"swz/{variant}/{dtype}/{row_bytes}/{box_rows}/{op}".encode()))
+                n += 1
+    assert n == 42
+
+
 @pytest.mark.parametrize("stages", [1, 2, 3, 5, 8])
 def test_many_tiles_per_cta(tsx, stages):
     """More tiles than CTAs, so every CTA cycles through its stages many
     times (parity flips), with a ragged last row tile."""
     rows, cols = 1000, 2048
-    for variant, op in (("tma", "fma"), ("tma", "copy"), ("ldgsts", "add"), ("tma_rank3", "mul")):
+    for variant, op in (("tma", "fma"), ("tma", "copy"), ("ldgsts", "add"), ("tma_rank3", "mul"), ("tma_mixed", "fma")):
         run_and_check(tsx, "f32", rows, cols, (8, 128), stages, variant, op, seed=stages)
 
 
