@@ -71,8 +71,17 @@ typedef enum { TSX_TMA = 0, TSX_LDGSTS = 1, TSX_SYNC = 2, TSX_TMA_RANK3 = 3, TSX
 /* Elementwise ops ("elementwise -> smem", table under "How inputs change
  * the algorithm").  copy moves bits unchanged; sqrt and add/mul/fma are
  * correctly rounded; exp is within 2 ulp (fp32) or 1 ulp (fp16, bf16) of the
- * exact value. */
-typedef enum { TSX_COPY = 0, TSX_SQRT = 1, TSX_EXP = 2, TSX_ADD = 3, TSX_MUL = 4, TSX_FMA = 5 } tsx_op;
+ * exact value.
+ *
+ * TSX_ACCUMULATE, OR-ed into an op, turns the store into a TMA reduce-store
+ * ("copy_async -> tma", table under "How inputs change the algorithm":
+ * s2g with a reduce op): out = out + op(a, b, c), the sum rounded to nearest
+ * even into the element type and added by the TMA unit in global memory.
+ * Offered by TSX_TMA and TSX_TMA_RANK3 (else TSX_ERR_UNSUPPORTED). */
+typedef enum {
+    TSX_COPY = 0, TSX_SQRT = 1, TSX_EXP = 2, TSX_ADD = 3, TSX_MUL = 4, TSX_FMA = 5,
+    TSX_ACCUMULATE = 0x100
+} tsx_op;
 
 typedef enum {
     TSX_OK = 0,
@@ -132,7 +141,8 @@ typedef struct tsx_plan_info {
 tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols,
                            int stages, tsx_variant variant);
 
-/* out = op(a, b, c) element by element over the plan's [rows, cols].
+/* out = op(a, b, c) element by element over the plan's [rows, cols]
+ * (out += op(a, b, c) with TSX_ACCUMULATE).
  * a is required; b is required by add / mul / fma and must be NULL
  * otherwise; c is required by fma and must be NULL otherwise (else
  * TSX_ERR_INVALID).  out may be exactly a, b or c; any other overlap is
@@ -173,7 +183,8 @@ int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, in
                    tsx_variant variant, tsx_op op, tsx_plan_info *info);
 
 /* tsx_plan_query for an existing plan, including the launch it makes on its
- * device (occupancy-derived CTAs per SM and grid). */
+ * device (occupancy-derived CTAs per SM and grid).  Both accept an op with
+ * TSX_ACCUMULATE. */
 int tsx_plan_get_info(tsx_plan_t plan, tsx_op op, tsx_plan_info *info);
 
 /* tsx_ewise for callers that may not allocate device memory.  The paper has

@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libtsx.so")
 DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
 VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3, "tma_mixed": 4}
 OPS = {"copy": 0, "sqrt": 1, "exp": 2, "add": 3, "mul": 4, "fma": 5}
+TSX_ACCUMULATE = 0x100   # OR into an op: out += op(a, b, c) by TMA reduce-store
 ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
 STATUS = {0: "TSX_OK", -1: "TSX_ERR_INVALID", -2: "TSX_ERR_UNSUPPORTED", -3: "TSX_ERR_ALIGN",
           -4: "TSX_ERR_CUDA", -5: "TSX_ERR_TIMEOUT", -6: "TSX_ERR_NOMEM"}
@@ -153,15 +154,19 @@ class Plan:
         if rc != TSX_OK:
             raise TsxError(rc, tsx_last_error())
 
-    def ewise(self, op: str, a, b=None, c=None, out=None, stream=None):
-        """out = op(a[, b[, c]]) on the current (or given) torch CUDA stream."""
+    def ewise(self, op: str, a, b=None, c=None, out=None, stream=None, accumulate: bool = False):
+        """out = op(a[, b[, c]]) on the current (or given) torch CUDA stream;
+        with accumulate, out += op(...) (out must then be given)."""
         import torch
 
         if out is None:
+            if accumulate:
+                raise TsxError(TSX_ERR_INVALID, "accumulate needs an out tensor to add into")
             out = torch.empty_like(a)
         pa, pb, pc, po = (self._check(a, "a"), self._check(b, "b"), self._check(c, "c"), self._check(out, "out"))
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
-        self.ewise_ptr(op, pa, pb, pc, po, s.cuda_stream)
+        code = _code(OPS, op) | (TSX_ACCUMULATE if accumulate else 0)
+        self.ewise_ptr(code, pa, pb, pc, po, s.cuda_stream)
         return out
 
     def status(self) -> int:

@@ -111,7 +111,7 @@ struct tsx_plan {
         OpGeometry og;
         int ctas_per_sm = 0;
         int grid = 0;
-    } ops[6];
+    } ops[12];   // op + 6 * accumulate
 
     // tensor maps, keyed by base pointer (the shape is the plan's)
     struct MapEntry {
@@ -127,25 +127,33 @@ namespace {
 // The mixed variant runs its own instantiation only for ops with a b operand.
 bool mixed_launch(int variant, int op) { return variant == TSX_TMA_MIXED && op_arity(op) >= 2; }
 
-const void* kernel_of(int variant, int dtype, int op)
+int tma_kind(int variant, int op, bool accumulate)
+{
+    return accumulate ? kTmaAccumulate : mixed_launch(variant, op) ? kTmaMixed : kTmaPlain;
+}
+
+// The reduce-store is offered by the two all-TMA variants.
+bool accumulate_offered(int variant) { return variant == TSX_TMA || variant == TSX_TMA_RANK3; }
+
+const void* kernel_of(int variant, int dtype, int op, bool accumulate)
 {
     if (variant == TSX_LDGSTS)
         return ldgsts_kernel(dtype, op);
     if (variant == TSX_SYNC)
         return sync_kernel(dtype, op);
-    return tma_kernel(dtype, op, mixed_launch(variant, op));
+    return tma_kernel(dtype, op, tma_kind(variant, op, accumulate));
 }
 
 // Geometry, kernel attributes, occupancy and grid for one op (cached).
-int prepare_op(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
+int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
 {
-    tsx_plan::OpLaunch& L = p->ops[op];
+    tsx_plan::OpLaunch& L = p->ops[op + (accumulate ? 6 : 0)];
     if (!L.ready) {
         std::string why;
         const int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
         if (rc != TSX_OK)
             return set_error(rc, why);
-        const void* fn = kernel_of(p->g.variant, p->g.dtype, op);
+        const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate);
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.og.smem_bytes));
         if (e != cudaSuccess)
             return cuda_error(e, "cudaFuncSetAttribute");
@@ -318,14 +326,18 @@ int tsx_plan_status(tsx_plan_t p)
 
 const char* tsx_last_error(void) { return g_last_error; }
 
-int tsx_plan_get_info(tsx_plan_t p, tsx_op op, tsx_plan_info* info)
+int tsx_plan_get_info(tsx_plan_t p, tsx_op op_arg, tsx_plan_info* info)
 {
     if (!p || !info)
         return set_error(TSX_ERR_INVALID, "NULL plan or info");
-    if (op < TSX_COPY || op > TSX_FMA)
+    int op;
+    bool accumulate;
+    if (!split_op(op_arg, &op, &accumulate))
         return set_error(TSX_ERR_INVALID, "unknown op");
+    if (accumulate && !accumulate_offered(p->g.variant))
+        return set_error(TSX_ERR_UNSUPPORTED, "TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
     tsx_plan::OpLaunch* L = nullptr;
-    const int rc = prepare_op(p, op, &L);
+    const int rc = prepare_op(p, op, accumulate, &L);
     if (rc != TSX_OK)
         return rc;
     fill_info(p->g, L->og, info);
@@ -335,12 +347,17 @@ int tsx_plan_get_info(tsx_plan_t p, tsx_op op, tsx_plan_info* info)
     return TSX_OK;
 }
 
-int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void* c, void* out, tsx_stream_t stream)
+int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const void* c, void* out,
+              tsx_stream_t stream)
 {
     if (!p)
         return set_error(TSX_ERR_INVALID, "NULL plan");
-    if (op < TSX_COPY || op > TSX_FMA)
+    int op;
+    bool accumulate;
+    if (!split_op(op_arg, &op, &accumulate))
         return set_error(TSX_ERR_INVALID, "unknown op");
+    if (accumulate && !accumulate_offered(p->g.variant))
+        return set_error(TSX_ERR_UNSUPPORTED, "TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
     const int n_in = op_arity(op);
     const Geometry& g = p->g;
     if (g.tiles == 0) {
@@ -360,7 +377,7 @@ int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void*
             align = alignment_of(ops[j]);
 
     tsx_plan::OpLaunch* L = nullptr;
-    int rc = prepare_op(p, op, &L);
+    int rc = prepare_op(p, op, accumulate, &L);
     if (rc != TSX_OK)
         return rc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -409,7 +426,8 @@ int tsx_ewise(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void*
         args.set_operand = mixed ? b : nullptr;
         args.box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
         args.swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
-        e = launch_tma(g.dtype, op, mixed, L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args);
+        e = launch_tma(g.dtype, op, tma_kind(g.variant, op, accumulate), L->grid, L->og.block_threads,
+                       L->og.smem_bytes, st, maps, args);
     } else {
         int vb = g.copy_vec_bytes < align ? g.copy_vec_bytes : align;
         if (vb < 4)

@@ -106,18 +106,28 @@ __device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p
     }
 }
 
-// TMA store of tile t from the slot at shared address `slot`.
+// TMA store of tile t from the slot at shared address `slot`; with ACC a
+// reduce-store that adds the tile into global memory.
+template <bool ACC>
 __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, uint32_t slot, int64_t t)
 {
     const TileBoxes b = tile_boxes(p, t);
     for (int r = 0; r < b.chunks; ++r) {
         const int y = b.row0 + r * p.rows_per_load;
         if (p.rank3) {
-            tma_store_3d(&maps.m[3], slot + r * p.load_smem_bytes, 0, y, b.col0 / p.inner_elems);
+            const uint32_t src = slot + r * p.load_smem_bytes;
+            if constexpr (ACC)
+                tma_reduce_add_3d(&maps.m[3], src, 0, y, b.col0 / p.inner_elems);
+            else
+                tma_store_3d(&maps.m[3], src, 0, y, b.col0 / p.inner_elems);
         } else {
-            for (int a = 0; a < b.atoms; ++a)
-                tma_store_2d(&maps.m[3], slot + (r * p.atoms + a) * p.load_smem_bytes, b.col0 + a * p.inner_elems,
-                             y);
+            for (int a = 0; a < b.atoms; ++a) {
+                const uint32_t src = slot + (r * p.atoms + a) * p.load_smem_bytes;
+                if constexpr (ACC)
+                    tma_reduce_add_2d(&maps.m[3], src, b.col0 + a * p.inner_elems, y);
+                else
+                    tma_store_2d(&maps.m[3], src, b.col0 + a * p.inner_elems, y);
+            }
         }
     }
     bulk_commit();
@@ -181,7 +191,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     return true;
 }
 
-template <int DT, int OP, bool MIXED>
+template <int DT, int OP, bool MIXED, bool ACC>
 __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__ TmaMaps maps, const TmaArgs p)
 {
     constexpr int NIN = op_arity(OP);
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
                 const uint32_t ready = OP == TSX_COPY ? full : computed;
                 if (!wait_or_abort(ready + 8u * s, parity, p, abort_flag))
                     break;
-                store_tile(maps, p, base + s * p.stage_bytes, cta + i * G);
+                store_tile<ACC>(maps, p, base + s * p.stage_bytes, cta + i * G);
                 // release tile i - lag once its store has read shared memory
                 bulk_wait_read(lag);
                 if (i >= lag)
@@ -304,19 +314,20 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     }
 }
 
-#define TSX_ROW(DT, M) \
-    {(const void*)tma_ewise<DT, 0, M>, (const void*)tma_ewise<DT, 1, M>, (const void*)tma_ewise<DT, 2, M>, \
-     (const void*)tma_ewise<DT, 3, M>, (const void*)tma_ewise<DT, 4, M>, (const void*)tma_ewise<DT, 5, M>}
-const void* const kKernels[2][3][6] = {
-    {TSX_ROW(TSX_F16, false), TSX_ROW(TSX_BF16, false), TSX_ROW(TSX_F32, false)},
-    {TSX_ROW(TSX_F16, true), TSX_ROW(TSX_BF16, true), TSX_ROW(TSX_F32, true)}};
+#define TSX_ROW(DT, M, A) \
+    {(const void*)tma_ewise<DT, 0, M, A>, (const void*)tma_ewise<DT, 1, M, A>, (const void*)tma_ewise<DT, 2, M, A>, \
+     (const void*)tma_ewise<DT, 3, M, A>, (const void*)tma_ewise<DT, 4, M, A>, (const void*)tma_ewise<DT, 5, M, A>}
+#define TSX_KIND(M, A) {TSX_ROW(TSX_F16, M, A), TSX_ROW(TSX_BF16, M, A), TSX_ROW(TSX_F32, M, A)}
+// indexed by TmaKind: plain, mixed, accumulate
+const void* const kKernels[3][3][6] = {TSX_KIND(false, false), TSX_KIND(true, false), TSX_KIND(false, true)};
+#undef TSX_KIND
 #undef TSX_ROW
 
 }  // namespace
 
-const void* tma_kernel(int dtype, int op, bool mixed) { return kKernels[mixed ? 1 : 0][dtype][op]; }
+const void* tma_kernel(int dtype, int op, int kind) { return kKernels[kind][dtype][op]; }
 
-cudaError_t launch_tma(int dtype, int op, bool mixed, int grid, int threads, size_t smem, cudaStream_t stream,
+cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args)
 {
     TmaMaps m;
@@ -324,7 +335,7 @@ cudaError_t launch_tma(int dtype, int op, bool mixed, int grid, int threads, siz
         m.m[j] = maps[j];
     TmaArgs a = args;
     void* params[] = {&m, &a};
-    return cudaLaunchKernel(kKernels[mixed ? 1 : 0][dtype][op], dim3(grid), dim3(threads), params, smem, stream);
+    return cudaLaunchKernel(kKernels[kind][dtype][op], dim3(grid), dim3(threads), params, smem, stream);
 }
 
 }  // namespace tsx

@@ -182,7 +182,7 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
     e = cudaMemsetAsync(scratch, 0, kStatusWordBytes, st);
     if (e != cudaSuccess)
         return fail_cuda(e, "clearing the status word");
-    e = launch_tma(dtype, op, false, grid, og.block_threads, og.smem_bytes, st, maps, args);
+    e = launch_tma(dtype, op, kTmaPlain, grid, og.block_threads, og.smem_bytes, st, maps, args);
     if (e != cudaSuccess)
         return fail_cuda(e, "kernel launch");
     if (status_out) {

@@ -289,10 +289,20 @@ void tensor_map_args(const Geometry& g, TensorMapArgs* m)
 }  // namespace tsx
 
 extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
-                              tsx_variant variant, tsx_op op, tsx_plan_info* info)
+                              tsx_variant variant, tsx_op op_arg, tsx_plan_info* info)
 {
     std::string why;
     tsx::Geometry g;
+    int op;
+    bool accumulate;
+    if (!tsx::split_op(op_arg, &op, &accumulate)) {
+        tsx::set_last_error("unknown op");
+        return TSX_ERR_INVALID;
+    }
+    if (accumulate && variant != TSX_TMA && variant != TSX_TMA_RANK3) {
+        tsx::set_last_error("TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
+        return TSX_ERR_UNSUPPORTED;
+    }
     int rc = tsx::make_geometry(dtype, rows, cols, box_rows, box_cols, stages, variant, &g, &why);
     if (rc == TSX_OK) {
         tsx::OpGeometry og;

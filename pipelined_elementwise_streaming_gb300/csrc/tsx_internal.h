@@ -80,11 +80,22 @@ struct CopyArgs {
 
 // Kernel lookup and launch, one set per variant (k_tma.cu, k_ldgsts.cu,
 // k_sync.cu).  `maps` holds the tensor maps of a, b, c and out.
-// `mixed`: the TSX_TMA_MIXED instantiation.  maps[0..2] are the TMA-loaded
-// operands in slot order, maps[3] the output.
-const void* tma_kernel(int dtype, int op, bool mixed = false);
-cudaError_t launch_tma(int dtype, int op, bool mixed, int grid, int threads, size_t smem, cudaStream_t stream,
+// Instantiations of the TMA kernel: plain, mixed (b by plain loads), and
+// accumulate (the result reduce-added into out).  maps[0..2] are the
+// TMA-loaded operands in slot order, maps[3] the output.
+enum TmaKind { kTmaPlain = 0, kTmaMixed = 1, kTmaAccumulate = 2 };
+const void* tma_kernel(int dtype, int op, int kind = kTmaPlain);
+cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args);
+
+// Split an op argument into the op and the TSX_ACCUMULATE flag; false if it
+// holds anything else.
+inline bool split_op(int op_arg, int* op, bool* accumulate)
+{
+    *accumulate = (op_arg & TSX_ACCUMULATE) != 0;
+    *op = op_arg & ~TSX_ACCUMULATE;
+    return *op >= TSX_COPY && *op <= TSX_FMA;
+}
 const void* ldgsts_kernel(int dtype, int op);
 cudaError_t launch_ldgsts(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
                           const void* a, const void* b, const void* c, void* out, const CopyArgs& args);

@@ -172,6 +172,20 @@ def test_query_declines(tsx, args, code):
     assert tsx.tsx_last_error()
 
 
+def test_query_accumulate_flag(tsx):
+    acc = tsx.TSX_ACCUMULATE
+    q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", tsx.OPS["fma"] | acc)
+    assert q["tx_bytes"] == 12288 and q["op"] == tsx.OPS["fma"]
+    tsx.query("f16", 64, 256, (8, 256), 2, "tma_rank3", tsx.OPS["copy"] | acc)
+    for variant in ("ldgsts", "sync", "tma_mixed"):
+        with pytest.raises(tsx.TsxError) as ei:
+            tsx.query("f32", 64, 256, (8, 64), 2, variant, tsx.OPS["add"] | acc)
+        assert ei.value.code == tsx.TSX_ERR_UNSUPPORTED
+    with pytest.raises(tsx.TsxError) as ei:
+        tsx.query("f32", 64, 256, (8, 64), 2, "tma", tsx.OPS["add"] | 0x200)
+    assert ei.value.code == tsx.TSX_ERR_INVALID
+
+
 def test_query_empty_tensor_is_legal(tsx):
     q = tsx.query("f32", 0, 128, (8, 32), 2, "tma", "copy")
     assert q["tiles"] == 0
