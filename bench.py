@@ -43,6 +43,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 DTYPE_NAME = {"f32": "f32", "f16": "f16", "bf16": "bf16"}
 KERNEL_SOURCES = ["pipelined_elementwise_streaming_gb300/csrc/k_tma.cu",
+                  "pipelined_elementwise_streaming_gb300/csrc/tsx_tma_common.cuh",
                   "pipelined_elementwise_streaming_gb300/csrc/tsx_device.cuh",
                   "pipelined_elementwise_streaming_gb300/csrc/tsx_internal.h"]
 

@@ -71,6 +71,8 @@ def lib():
             L.tsxo_add_round_odd.argtypes = [ctypes.c_double, ctypes.c_double]
             L.tsxo_ewise.restype = ctypes.c_int
             L.tsxo_ewise.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64] + [ctypes.c_void_p] * 4
+            L.tsxo_decode.restype = ctypes.c_int
+            L.tsxo_decode.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -104,6 +106,44 @@ def ewise(op: str, dtype: str, a, b=None, c=None) -> np.ndarray:
     if rc != 0:
         raise RuntimeError("tsxo_ewise rejected its arguments")
     return out
+
+
+def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """The exact values (float64) of an array of element bits."""
+    b = _bits(bits, dtype)
+    out = np.empty(b.shape, dtype=np.float64)
+    if lib().tsxo_decode(DTYPE_CODE[dtype], int(b.size), b.ctypes.data, out.ctypes.data) != 0:
+        raise RuntimeError("tsxo_decode rejected its arguments")
+    return out
+
+
+def rowsum(op: str, dtype: str, a, b=None, c=None):
+    """Row sums of the element-type results x = op(a, b, c) of a [rows, cols]
+    problem: the reduction the nvFuser page schedules over staged tiles
+    ("Testing Setup", Reduction and InnerPersistent).
+
+    Returns ``(sums, abs_sums)``, float64 arrays of length rows: ``sums[r]``
+    is the exact sum of row r rounded once to float64 (``math.fsum``), and
+    ``abs_sums[r]`` the exact sum of |x| rounded the same way, which scales
+    the error bound of any floating-point summation order.
+    """
+    import math
+
+    x = decode(ewise(op, dtype, a, b, c), dtype)
+    x = x.reshape(x.shape[0], -1)
+    sums = np.array([math.fsum(row) for row in x], dtype=np.float64)
+    abs_sums = np.array([math.fsum(np.abs(row)) for row in x], dtype=np.float64)
+    return sums, abs_sums
+
+
+def summation_error_bound(n_terms: int, abs_sum: np.ndarray, unit_roundoff: float = 2.0 ** -24) -> np.ndarray:
+    """The forward error bound of a sum of n terms in a floating-point format
+    with unit roundoff u, in any order of additions: gamma(n-1) * sum |x_i|,
+    gamma(k) = k u / (1 - k u) (N. J. Higham, "Accuracy and Stability of
+    Numerical Algorithms", 2nd ed., section 4.2)."""
+    k = max(0, n_terms - 1)
+    gamma = k * unit_roundoff / (1.0 - k * unit_roundoff)
+    return gamma * np.asarray(abs_sum, dtype=np.float64)
 
 
 def value(bits: int, dtype: str) -> float:

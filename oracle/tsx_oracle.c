@@ -205,3 +205,13 @@ int tsxo_ewise(int dt, int op, int64_t n, const void *a, const void *b, const vo
     }
     return 0;
 }
+
+/* dst[i] = the exact value of element i (bits of type dt), i < n. */
+int tsxo_decode(int dt, int64_t n, const void *src, double *dst)
+{
+    if (dt < O_F16 || dt > O_F32 || !src || !dst)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = tsxo_value(load_bits(src, i, dt), dt);
+    return 0;
+}
