@@ -159,6 +159,22 @@ tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_
 int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, void *out,
               tsx_stream_t stream);
 
+/* Row sums: row_sums[r] = sum over c of op(a, b, c)[r, c] for the plan's
+ * [rows, cols]; each op result is rounded into the element type, then summed
+ * in fp32 (the reduction schedules of nvFuser PR #2833, "Testing Setup":
+ * Reduction, InnerPersistent).  row_sums: device fp32 [rows], 4-byte
+ * aligned, overwritten.  A persistent CTA owns whole row bands of box_rows
+ * rows and streams their tiles through the plan's TMA ring, so at most
+ * ceil(rows / box_rows) CTAs run: choose box_rows for enough bands.  The
+ * order of additions depends on the plan alone, so results repeat bit for
+ * bit; against the exact sum their error is at most gamma(cols - 1) *
+ * sum |x|, gamma(k) = k u / (1 - k u), u = 2^-24.  TSX_TMA / TSX_TMA_RANK3
+ * plans only (else TSX_ERR_UNSUPPORTED); TSX_ACCUMULATE is rejected.  rows =
+ * 0 does nothing; cols = 0 writes zeros.  Asynchronous on `stream`;
+ * device-side timeouts are reported as for tsx_ewise. */
+int tsx_reduce_rows(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, float *row_sums,
+                    tsx_stream_t stream);
+
 /* Release the plan, its tensor-map cache and its device status word.
  * NULL is ignored.  Work already queued must not need the plan's status
  * word afterwards (synchronize first). */

@@ -83,6 +83,8 @@ def _load():
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
     L.tsx_plan_get_info.restype = ctypes.c_int
     L.tsx_plan_get_info.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
+    L.tsx_reduce_rows.restype = ctypes.c_int
+    L.tsx_reduce_rows.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5
     L.tsx_ewise_noalloc.restype = ctypes.c_int
     L.tsx_ewise_noalloc.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5 + \
@@ -99,6 +101,7 @@ tsx_plan_destroy = lib.tsx_plan_destroy
 tsx_plan_status = lib.tsx_plan_status
 tsx_plan_query = lib.tsx_plan_query
 tsx_plan_get_info = lib.tsx_plan_get_info
+tsx_reduce_rows = lib.tsx_reduce_rows
 # The plan-free, allocation-free form of tsx_ewise (device status word in a
 # static device array; see include/tsx.h for who needs it and its limits).
 tsx_ewise_noalloc = lib.tsx_ewise_noalloc
@@ -167,6 +170,21 @@ class Plan:
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         code = _code(OPS, op) | (TSX_ACCUMULATE if accumulate else 0)
         self.ewise_ptr(code, pa, pb, pc, po, s.cuda_stream)
+        return out
+
+    def reduce_rows(self, op: str, a, b=None, c=None, out=None, stream=None):
+        """fp32 row sums of op(a[, b[, c]]) over the plan's [rows, cols]."""
+        import torch
+
+        if out is None:
+            out = torch.empty(self.rows, dtype=torch.float32, device=a.device)
+        if out.dtype != torch.float32 or not out.is_cuda or out.numel() != self.rows:
+            raise TsxError(TSX_ERR_INVALID, f"out must be a CUDA float32 tensor of {self.rows} elements")
+        pa, pb, pc = self._check(a, "a"), self._check(b, "b"), self._check(c, "c")
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        rc = tsx_reduce_rows(self.handle, _code(OPS, op), pa, pb, pc, out.data_ptr(), s.cuda_stream)
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
         return out
 
     def status(self) -> int:

@@ -111,7 +111,8 @@ struct tsx_plan {
         OpGeometry og;
         int ctas_per_sm = 0;
         int grid = 0;
-    } ops[12];   // op + 6 * accumulate
+    } ops[12],   // op + 6 * accumulate
+        rowsum_ops[6];
 
     // tensor maps, keyed by base pointer (the shape is the plan's)
     struct MapEntry {
@@ -238,6 +239,37 @@ int get_map(tsx_plan* p, const void* ptr, CUtensorMap* out)
     return TSX_OK;
 }
 
+// Kernel arguments of the TMA kernels for plan p and one op's geometry.
+void fill_tma_args(const tsx_plan* p, const OpGeometry& og, TmaArgs* args)
+{
+    const Geometry& g = p->g;
+    *args = TmaArgs{};
+    args->tiles = g.tiles;
+    args->tiles_c = g.tiles_c;
+    args->tiles_r = g.tiles_r;
+    args->fault_tile = p->fault_tile;
+    args->status = p->d_status;
+    args->timeout_ns = p->timeout_ns;
+    args->rows = int(g.rows);
+    args->cols = int(g.cols);
+    args->box_rows = g.box_rows;
+    args->box_cols = g.box_cols;
+    args->stages = g.stages;
+    args->inner_elems = g.inner_elems;
+    args->atoms = g.atoms;
+    args->rows_per_load = g.rows_per_load;
+    args->row_chunks = g.row_chunks;
+    args->rank3 = g.variant == TSX_TMA_RANK3;
+    args->load_smem_bytes = g.load_smem_bytes;
+    args->slot_bytes = g.slot_bytes;
+    args->stage_bytes = og.stage_bytes;
+    args->bytes_per_load = uint32_t(g.bytes_per_load);
+    args->vec16_per_slot = og.vec16_per_slot;
+    args->store_lag = g.store_lag;
+    args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
+    args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
+}
+
 int alignment_of(const void* ptr)
 {
     const uintptr_t v = reinterpret_cast<uintptr_t>(ptr);
@@ -259,6 +291,45 @@ int read_status(tsx_plan* p, bool clear)
             return cuda_error(e, "clearing the status word");
     }
     return h;
+}
+
+// Launch shape of the row reduction for one op (cached): the stages of the
+// elementwise geometry, two barriers per stage, the abort flag and one fp32
+// accumulator per band row; compute warps plus the producer warp.
+int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
+{
+    tsx_plan::OpLaunch& L = p->rowsum_ops[op];
+    if (!L.ready) {
+        std::string why;
+        int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
+        if (rc != TSX_OK)
+            return set_error(rc, why);
+        const size_t smem = size_t(p->g.stages) * L.og.stage_bytes + size_t(p->g.stages) * 16 + 16 + kSmemAlign +
+                            (size_t(p->g.box_rows) * 4 + 15) / 16 * 16;
+        if (smem > size_t(p->max_smem))
+            return set_error(TSX_ERR_UNSUPPORTED, "the row reduction's stages do not fit in shared memory");
+        L.og.smem_bytes = smem;
+        L.og.block_threads = L.og.threads + 32;
+        const void* fn = rowsum_kernel(p->g.dtype, op);
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaFuncSetAttribute");
+        int blocks = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, L.og.block_threads, smem);
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (blocks < 1)
+            return set_error(TSX_ERR_UNSUPPORTED, "the row reduction cannot be resident with this shared memory");
+        if (p->ctas_per_sm_cap > 0 && blocks > p->ctas_per_sm_cap)
+            blocks = p->ctas_per_sm_cap;
+        L.ctas_per_sm = blocks;
+        // one CTA per row band at most: a band is never split between CTAs
+        const int64_t slots = int64_t(p->sm_count) * blocks;
+        L.grid = int(p->g.tiles_r < slots ? p->g.tiles_r : slots);
+        L.ready = true;
+    }
+    *out = &L;
+    return TSX_OK;
 }
 
 }  // namespace
@@ -402,30 +473,8 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
                 return rc;
         }
         TmaArgs args{};
-        args.tiles = g.tiles;
-        args.tiles_c = g.tiles_c;
-        args.fault_tile = p->fault_tile;
-        args.status = p->d_status;
-        args.timeout_ns = p->timeout_ns;
-        args.rows = int(g.rows);
-        args.cols = int(g.cols);
-        args.box_rows = g.box_rows;
-        args.box_cols = g.box_cols;
-        args.stages = g.stages;
-        args.inner_elems = g.inner_elems;
-        args.atoms = g.atoms;
-        args.rows_per_load = g.rows_per_load;
-        args.row_chunks = g.row_chunks;
-        args.rank3 = g.variant == TSX_TMA_RANK3;
-        args.load_smem_bytes = g.load_smem_bytes;
-        args.slot_bytes = g.slot_bytes;
-        args.stage_bytes = L->og.stage_bytes;
-        args.bytes_per_load = uint32_t(g.bytes_per_load);
-        args.vec16_per_slot = L->og.vec16_per_slot;
-        args.store_lag = g.store_lag;
+        fill_tma_args(p, L->og, &args);
         args.set_operand = mixed ? b : nullptr;
-        args.box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
-        args.swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
         e = launch_tma(g.dtype, op, tma_kind(g.variant, op, accumulate), L->grid, L->og.block_threads,
                        L->og.smem_bytes, st, maps, args);
     } else {
@@ -450,6 +499,73 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
                 ? launch_ldgsts(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, a, b, c, out, args)
                 : launch_sync(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, a, b, c, out, args);
     }
+    if (e != cudaSuccess)
+        return cuda_error(e, "kernel launch");
+    if (p->checked) {
+        e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaStreamSynchronize");
+        const int s = read_status(p, true);
+        if (s != TSX_OK)
+            return set_error(s, "a device-side wait gave up");
+    }
+    set_last_error("");
+    return TSX_OK;
+}
+
+int tsx_reduce_rows(tsx_plan_t p, tsx_op op, const void* a, const void* b, const void* c, float* row_sums,
+                    tsx_stream_t stream)
+{
+    if (!p)
+        return set_error(TSX_ERR_INVALID, "NULL plan");
+    if (op < TSX_COPY || op > TSX_FMA)
+        return set_error(TSX_ERR_INVALID, "unknown op (TSX_ACCUMULATE does not apply to row sums)");
+    const Geometry& g = p->g;
+    if (g.variant != TSX_TMA && g.variant != TSX_TMA_RANK3)
+        return set_error(TSX_ERR_UNSUPPORTED, "row sums need a TSX_TMA or TSX_TMA_RANK3 plan");
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (g.rows == 0) {
+        set_last_error("");
+        return TSX_OK;
+    }
+    if (!row_sums)
+        return set_error(TSX_ERR_INVALID, "row_sums is required");
+    if (reinterpret_cast<uintptr_t>(row_sums) % 4)
+        return set_error(TSX_ERR_ALIGN, "row_sums must be 4-byte aligned");
+    if (g.cols == 0) {
+        // every row is an empty sum
+        const cudaError_t e = cudaMemsetAsync(row_sums, 0, size_t(g.rows) * sizeof(float), st);
+        if (e != cudaSuccess)
+            return cuda_error(e, "cudaMemsetAsync");
+        set_last_error("");
+        return TSX_OK;
+    }
+    const int n_in = op_arity(op);
+    if (!a)
+        return set_error(TSX_ERR_INVALID, "a is required");
+    if ((n_in >= 2) != (b != nullptr) || (n_in >= 3) != (c != nullptr))
+        return set_error(TSX_ERR_INVALID, "b / c must be given exactly when the op uses them");
+    const void* ops[3] = {a, b, c};
+    for (const void* q : ops)
+        if (q && alignment_of(q) < 16)
+            return set_error(TSX_ERR_ALIGN, "TMA needs 16-byte aligned base pointers");
+    tsx_plan::OpLaunch* L = nullptr;
+    int rc = prepare_rowsum(p, op, &L);
+    if (rc != TSX_OK)
+        return rc;
+    CUtensorMap maps[4];
+    std::memset(maps, 0, sizeof maps);
+    for (int j = 0; j < 3; ++j) {
+        if (!ops[j])
+            continue;
+        rc = get_map(p, ops[j], &maps[j]);
+        if (rc != TSX_OK)
+            return rc;
+    }
+    TmaArgs args{};
+    fill_tma_args(p, L->og, &args);
+    cudaError_t e = launch_rowsum(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args,
+                                  row_sums);
     if (e != cudaSuccess)
         return cuda_error(e, "kernel launch");
     if (p->checked) {

@@ -41,6 +41,7 @@ TSX_HD constexpr int tma_operands(int variant, int op)
 struct TmaArgs {
     int64_t tiles;          // T: tiles in the tensor
     int64_t tiles_c;        // tiles along a row
+    int64_t tiles_r;        // row bands
     int64_t fault_tile;     // test hook: the producer skips this tile's loads (-1: none)
     int* status;            // device status word (TSX_OK until a wait gives up)
     uint64_t timeout_ns;    // limit of every mbarrier wait
@@ -96,6 +97,10 @@ inline bool split_op(int op_arg, int* op, bool* accumulate)
     *op = op_arg & ~TSX_ACCUMULATE;
     return *op >= TSX_COPY && *op <= TSX_FMA;
 }
+// The row-reduction kernel (k_rowsum.cu): TMA ring, rows summed in fp32.
+const void* rowsum_kernel(int dtype, int op);
+cudaError_t launch_rowsum(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
+                          const CUtensorMap* maps, const TmaArgs& args, float* row_sums);
 const void* ldgsts_kernel(int dtype, int op);
 cudaError_t launch_ldgsts(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
                           const void* a, const void* b, const void* c, void* out, const CopyArgs& args);

@@ -1,0 +1,131 @@
+"""Row sums over staged tiles (tsx_reduce_rows) against the oracle: within
+the summation bound gamma(cols - 1) * sum |x| of the exact sum (plus the exp
+bound where the terms themselves carry it), exact for integer-valued rows,
+repeatable bit for bit, and blind to the zero-filled columns of ragged
+tiles."""
+
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import _gpu
+from tests._gpu import to_dev, torch
+
+pytestmark = pytest.mark.gpu
+
+OPS = ["copy", "sqrt", "exp", "add", "mul", "fma"]
+ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
+PRECISION = {"f16": 11, "bf16": 8, "f32": 24}
+
+
+@pytest.fixture(scope="module")
+def tsx():
+    _gpu.need_gpu()
+    import pipelined_elementwise_streaming_gb300 as m
+
+    return m
+
+
+def _values(dtype, shape, seed, lo=-2.0, hi=2.0):
+    rng = np.random.default_rng(seed)
+    x = rng.uniform(lo, hi, int(np.prod(shape)))
+    if dtype == "f32":
+        return x.astype(np.float32).view(np.uint32).reshape(shape)
+    if dtype == "f16":
+        return x.astype(np.float16).view(np.uint16).reshape(shape)
+    return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16).reshape(shape)
+
+
+def _rowsum(tsx, dtype, rows, cols, box, stages, variant, op, ins):
+    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant=variant) as plan:
+        out = plan.reduce_rows(op, *[to_dev(x, dtype) for x in ins])
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+    return out.cpu().numpy().astype(np.float64)
+
+
+def _check(got, op, dtype, ins, cols, what):
+    sums, abs_sums = oracle.rowsum(op, dtype, *ins)
+    bound = oracle.summation_error_bound(cols, abs_sums)
+    if op == "exp":
+        # every term may be off by the exp bound in ulps of the element type
+        bound = bound + abs_sums * oracle.EXP_ULP_BOUND[dtype] * 2.0 ** (1 - PRECISION[dtype])
+    err = np.abs(got - sums)
+    bad = np.nonzero(err > bound * (1 + 1e-9) + 1e-30)[0]
+    assert bad.size == 0, f"{what}: row {bad[0]}: got {got[bad[0]]!r} want {sums[bad[0]]!r} bound {bound[bad[0]]!r}"
+
+
+SHAPES = [(37, 700, (8, 128)), (5, 64, (4, 64)), (130, 1024, (16, 256)), (64, 2048, (32, 64))]
+
+
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("op", OPS)
+def test_rowsum_within_the_summation_bound(tsx, variant, dtype, op):
+    n = 0
+    for rows, cols, box in SHAPES:
+        es = 4 if dtype == "f32" else 2
+        if (cols * es) % 16:
+            continue
+        try:
+            tsx.query(dtype, rows, cols, box, 3, variant, op)
+        except tsx.TsxError:
+            continue
+        seed = zlib.crc32(f"rowsum/{variant}/{dtype}/{op}/{rows}/{cols}".encode())
+        lo = 0.0 if op == "sqrt" else -2.0
+        ins = [_values(dtype, (rows, cols), seed + k, lo=lo) for k in range(ARITY[op])]
+        got = _rowsum(tsx, dtype, rows, cols, box, 3, variant, op, ins)
+        _check(got, op, dtype, ins, cols, f"{variant} {dtype} {op} [{rows},{cols}] box {box}")
+        n += 1
+    assert n >= 2
+
+
+def test_rowsum_integer_rows_are_exact(tsx):
+    """Small integers: every partial sum is exact in fp32, so the result is
+    the exact sum whatever the order -- no element is missed or doubled."""
+    rows, cols = 45, 1000
+    rng = np.random.default_rng(4)
+    a = rng.integers(-64, 64, (rows, cols)).astype(np.float32)
+    for box, stages in (((8, 128), 3), ((16, 64), 2), ((1, 256), 4)):
+        got = _rowsum(tsx, "f32", rows, cols, box, stages, "tma", "copy", [a.view(np.uint32)])
+        assert np.array_equal(got, a.astype(np.float64).sum(axis=1)), box
+
+
+def test_rowsum_ignores_the_padding_of_ragged_tiles(tsx):
+    """exp of the zero fill would add 1 per padded element; the true sums
+    here are tiny, so any leak shows."""
+    rows, cols = 19, 200   # 200 = 3 * 64 + 8: the last column tile is mostly padding
+    a = np.full((rows, cols), -30.0, dtype=np.float32)
+    got = _rowsum(tsx, "f32", rows, cols, (8, 64), 2, "tma", "exp", [a.view(np.uint32)])
+    assert np.all(got < 1e-8) and np.all(got > 0)
+
+
+def test_rowsum_repeats_bit_for_bit(tsx):
+    rows, cols = 64, 4096
+    a = _values("bf16", (rows, cols), 5)
+    with tsx.Plan("bf16", rows, cols, box=(8, 128), stages=4) as plan:
+        da = to_dev(a, "bf16")
+        r1 = plan.reduce_rows("exp", da).cpu().numpy()
+        r2 = plan.reduce_rows("exp", da).cpu().numpy()
+    assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
+
+
+def test_rowsum_edges_and_declines(tsx):
+    with tsx.Plan("f32", 7, 0, box=(8, 32), stages=2) as plan:
+        out = torch.full((7,), 3.0, device="cuda")
+        plan.reduce_rows("copy", torch.empty(7, 0, device="cuda"), out=out)
+        torch.cuda.synchronize()
+        assert torch.all(out == 0)
+    a = torch.rand(16, 64, device="cuda")
+    for variant in ("ldgsts", "sync", "tma_mixed"):
+        with tsx.Plan("f32", 16, 64, box=(8, 32), stages=2, variant=variant) as plan:
+            with pytest.raises(tsx.TsxError) as ei:
+                plan.reduce_rows("copy", a)
+            assert ei.value.code == tsx.TSX_ERR_UNSUPPORTED
+    with tsx.Plan("f32", 16, 64, box=(8, 32), stages=2) as plan:
+        out = torch.empty(16, device="cuda")
+        rc = tsx.tsx_reduce_rows(plan.handle, tsx.OPS["copy"] | tsx.TSX_ACCUMULATE, a.data_ptr(), None, None,
+                                 out.data_ptr(), 0)
+        assert rc == tsx.TSX_ERR_INVALID
