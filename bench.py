@@ -59,7 +59,12 @@ def parse_args(argv=None):
     p.add_argument("--rows", type=int, default=None,
                    help="run the workload over its first ROWS rows only (a smaller case, e.g. for profiling)")
     p.add_argument("--variant", default=None, help="default: the workload's variant")
+    p.add_argument("--box", type=int, nargs=2, default=None, metavar=("ROWS", "COLS"),
+                   help="stage tile other than the workload's (row sums run one CTA per band of ROWS rows)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--mode", default="ewise", choices=["ewise", "accumulate", "rowsum"],
+                   help="ewise: out = op(...); accumulate: out += op(...) by TMA reduce-store; "
+                        "rowsum: fp32 row sums of op(...)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -242,6 +247,18 @@ def memcpy_ceiling(torch, nbytes=1 << 30, reps=20):
     return 2 * nbytes / statistics.median(times) / 1e9
 
 
+def step_bytes(w, mode: str) -> int:
+    """Algorithmic bytes of one step: every input read once, plus the output
+    written (ewise), read and written (accumulate), or one fp32 per row
+    (rowsum)."""
+    es = ti.ELEM_SIZE[w.dtype]
+    if mode == "accumulate":
+        return (w.n_in + 2) * w.elems * es
+    if mode == "rowsum":
+        return w.n_in * w.elems * es + 4 * w.rows
+    return w.algorithmic_bytes
+
+
 def run_ours(args, w, stages, variant):
     import torch
 
@@ -252,20 +269,30 @@ def run_ours(args, w, stages, variant):
 
     host = to_host_tensors(w, torch)
     dev_in = [h.to("cuda", non_blocking=False) for h in host]
-    out = torch.empty_like(dev_in[0])
+    out = torch.zeros_like(dev_in[0])
+    row_sums = torch.empty(w.rows, dtype=torch.float32, device="cuda")
+    mode = args.mode
+    nbytes = step_bytes(w, mode)
     plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant)
     info = plan.info(w.op)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))
     po = out.data_ptr()
-    small = w.algorithmic_bytes < 4 * L2_BYTES
+    small = nbytes < 4 * L2_BYTES
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
 
     ceiling = memcpy_ceiling(torch)
 
+    op_code = tsx.OPS[w.op] | (tsx.TSX_ACCUMULATE if mode == "accumulate" else 0)
+
     def step():
-        plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], po, sh)
+        if mode == "rowsum":
+            rc = tsx.tsx_reduce_rows(plan.handle, op_code, ptrs[0], ptrs[1], ptrs[2], row_sums.data_ptr(), sh)
+            if rc != tsx.TSX_OK:
+                raise tsx.TsxError(rc, tsx.tsx_last_error())
+        else:
+            plan.ewise_ptr(op_code, ptrs[0], ptrs[1], ptrs[2], po, sh)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -303,17 +330,24 @@ def run_ours(args, w, stages, variant):
     kernel_total = sum(launch_s)
     region_s = region0.elapsed_time(region1) / 1e3
     step_s = kernel_total if small else region_s   # with flushes, only the kernels are counted
-    max_s, total_bytes = aggregate(td, step_s, float(w.algorithmic_bytes) * K)
+    max_s, total_bytes = aggregate(td, step_s, float(nbytes) * K)
     value = total_bytes / max_s / 1e9
     avg_launch = kernel_total / K
-    achieved = w.algorithmic_bytes / avg_launch / 1e9
+    achieved = nbytes / avg_launch / 1e9
     peak, peak_kind = measured_peak()
 
     # end to end: pinned host inputs in, host result out, every step
     E = max(1, args.e2e_steps)
-    e2e_s, h2d, d2h, bands = run_e2e(torch, tsx, w, stages, variant, host, dev_in, out, E, td)
-    e2e_bytes = float(w.algorithmic_bytes) * E
-    e2e_s, e2e_bytes = aggregate(td, e2e_s, e2e_bytes)
+    if mode == "ewise":
+        e2e_s, h2d, d2h, bands = run_e2e(torch, tsx, w, stages, variant, host, dev_in, out, E, td)
+        e2e_bytes = float(nbytes) * E
+        e2e_s, e2e_bytes = aggregate(td, e2e_s, e2e_bytes)
+        e2e = {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "steps": E,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "method": f"{bands} row bands per step through tsx_ewise; each band's H2D copies (two "
+                         "alternating copy streams), kernel and D2H copy overlap the neighbouring bands'"}
+    else:
+        e2e = {"value": None, "unit": "GB/s", "note": f"the end-to-end leg runs in ewise mode only, not {mode}"}
     plan.close()
 
     result = {
@@ -333,25 +367,23 @@ def run_ours(args, w, stages, variant):
             "workload": w.name + ("" if args.rows is None else f" (first {w.rows} rows)"), "op": w.op, "rows": w.rows, "cols": w.cols, "box": [w.box_rows, w.box_cols],
             "stages": stages, "variant": variant, "threads": info["threads"], "grid": info["grid"],
             "ctas_per_sm": info["ctas_per_sm"], "loads_per_operand": info["loads_per_operand"],
-            "algorithmic_bytes_per_step": w.algorithmic_bytes,
+            "mode": mode, "algorithmic_bytes_per_step": nbytes,
             "l2": "L2 flushed between timed steps (kernel time only)" if small
-                  else f"inputs larger than L2 ({w.algorithmic_bytes >> 20} MiB moved per step vs 129 MiB L2), "
+                  else f"inputs larger than L2 ({nbytes >> 20} MiB moved per step vs 129 MiB L2), "
                        "steps back to back",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "memcpy_ceiling_gbs": round(ceiling, 1),
         "frac_of_memcpy_ceiling": round(value / world / ceiling, 4),
         "clocks": clocks,
-        "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "steps": E,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "method": f"{bands} row bands per step through tsx_ewise; each band's H2D copies (two "
-                          "alternating copy streams), kernel and D2H copy overlap the neighbouring bands'"},
+        "e2e": e2e,
         "gpu_launches": K,
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-            "traffic": recorded_traffic(w.name, variant, stages),
-            "kernel": f"tma_ewise<{w.dtype},{w.op}>" if variant.startswith("tma") else f"{variant}_ewise",
+            "traffic": recorded_traffic(w.name, variant, stages) if mode == "ewise" else None,
+            "kernel": (f"tma_rowsum<{w.dtype},{w.op}>" if mode == "rowsum" else
+                       f"tma_ewise<{w.dtype},{w.op}>" if variant.startswith("tma") else f"{variant}_ewise"),
             "median_launch_ms": round(statistics.median(launch_s) * 1e3, 5),
         },
     }
@@ -508,6 +540,10 @@ def main(argv=None):
     w = ti.WORKLOADS[args.workload]
     if args.rows is not None:
         w = w.with_rows(args.rows)
+    if args.box is not None:
+        from dataclasses import replace
+
+        w = replace(w, box_rows=args.box[0], box_cols=args.box[1])
     stages = args.stages if args.stages is not None else w.default_stages
     variant = args.variant or w.variant
     if args.impl == "reference":

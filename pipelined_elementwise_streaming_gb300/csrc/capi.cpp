@@ -294,8 +294,10 @@ int read_status(tsx_plan* p, bool clear)
 }
 
 // Launch shape of the row reduction for one op (cached): the stages of the
-// elementwise geometry, two barriers per stage, the abort flag and one fp32
-// accumulator per band row; compute warps plus the producer warp.
+// elementwise geometry, two barriers per stage, two band barriers, the
+// abort flag and one fp32
+// partial per 16-byte unit of a staged slot; compute warps plus the
+// producer warp.
 int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
 {
     tsx_plan::OpLaunch& L = p->rowsum_ops[op];
@@ -304,12 +306,24 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
         if (rc != TSX_OK)
             return set_error(rc, why);
-        const size_t smem = size_t(p->g.stages) * L.og.stage_bytes + size_t(p->g.stages) * 16 + 16 + kSmemAlign +
-                            (size_t(p->g.box_rows) * 4 + 15) / 16 * 16;
+        // one fp32 partial per 16-byte unit of a staged slot
+        const size_t partials = size_t(L.og.vec16_per_slot) * 4;
+        const size_t smem = size_t(p->g.stages) * L.og.stage_bytes + size_t(p->g.stages) * 16 + 16 + 16 +
+                            kSmemAlign + partials;
         if (smem > size_t(p->max_smem))
             return set_error(TSX_ERR_UNSUPPORTED, "the row reduction's stages do not fit in shared memory");
         L.og.smem_bytes = smem;
-        L.og.block_threads = L.og.threads + 32;
+        // about 768 compute threads per SM, shared by the CTAs that fit (the
+        // row sums do more arithmetic per byte than the elementwise stage)
+        const int ctas = int(kSmemPerSm / (smem + kSmemPerCtaReserved));
+        int threads = 768 / (ctas < 1 ? 1 : ctas) / 32 * 32;
+        threads = threads < 64 ? 64 : threads > 512 ? 512 : threads;
+        const char* env = std::getenv("TSX_THREADS");
+        const int forced = env && *env ? std::atoi(env) : 0;
+        if (forced >= 32 && forced <= kMaxThreads - 32 && forced % 32 == 0)
+            threads = forced;
+        L.og.threads = threads;
+        L.og.block_threads = threads + 32;
         const void* fn = rowsum_kernel(p->g.dtype, op);
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess)

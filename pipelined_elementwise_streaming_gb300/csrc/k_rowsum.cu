@@ -9,15 +9,19 @@
 //   warp 0      the producer (as in the elementwise kernel): the CTA's k-th
 //               tile is tile (band(k), k mod tiles_c) of its k / tiles_c-th
 //               band; stage reuse waits on `empty`.
-//   warps 1..   the compute warps.  Row r of a band belongs to compute warp
-//               r mod W.  For each tile the warp's lanes take the row's
-//               16-byte vectors (lane, lane + 32, ...), apply the op, round
-//               it into the element type and add the elements into an fp32
-//               lane sum in order; a fixed butterfly of shuffles adds the 32
-//               lane sums; the tile's row sum is added to the row's fp32
-//               accumulator in shared memory; after the band's last tile
-//               the accumulator is the row's result.  Every warp then
-//               releases the stage (`empty`, one arrival per warp).
+//   warps 1..   the compute warps.  Every tile of a plan lands in shared
+//               memory with the same layout, so the 16-byte unit u of a
+//               staged slot holds the same (row, column within the tile) in
+//               every tile.  Compute thread tid always takes units tid, tid
+//               + threads, ...: it applies the op to the unit's vectors,
+//               rounds into the element type, adds the elements in order and
+//               adds that to the unit's fp32 partial in shared memory (set,
+//               on the band's first tile).  Only a band's last, ragged tile
+//               needs each unit's column, to leave out the columns past the
+//               tensor's end.  Every warp then releases the stage (`empty`,
+//               one arrival per warp).  After the band's last tile one
+//               thread per row adds the partials of the row's units, box by
+//               box in a fixed order, into the row's result.
 //
 // The order of additions is fixed by the shapes alone, so results repeat
 // bit for bit from run to run.  Columns past the end of the tensor (zero
@@ -30,14 +34,6 @@ namespace tsx {
 namespace {
 
 using namespace dev;
-
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 // Add the elements of one 16-byte vector of op results to `part`, in order.
 template <int DT>
@@ -60,38 +56,60 @@ __device__ __forceinline__ void add_vec(float& part, const uint4& r)
     }
 }
 
-// The op applied to one row of a staged tile, summed: this lane's share of
-// the row's in-bounds 16-byte vectors, then the warp total.
+// The op on the staged vectors of unit u, its elements added in order.
 template <int DT, int OP>
-__device__ __forceinline__ float row_of_tile(const TmaArgs& p, const uint8_t* stage, const TileBoxes& tb, int r,
-                                             int lane)
+__device__ __forceinline__ float unit_sum(const TmaArgs& p, const uint4* S, uint32_t u)
 {
     constexpr int NIN = op_arity(OP);
+    const uint4 va = S[u];
+    const uint4 vb = NIN > 1 ? S[p.slot_bytes / 16 + u] : va;
+    const uint4 vc = NIN > 2 ? S[2 * (p.slot_bytes / 16) + u] : va;
+    float part = 0.f;
+    add_vec<DT>(part, op_vec16<DT, OP>(va, vb, vc));
+    return part;
+}
+
+// Whether unit u of a staged slot holds columns inside the tensor (a ragged
+// tile's padding and the boxes skipped past its end do not).
+template <int DT>
+__device__ __forceinline__ bool unit_in_columns(const TmaArgs& p, const TileBoxes& tb, uint32_t u)
+{
     constexpr int ES = DT == TSX_F32 ? 4 : 2;
     const uint32_t inner_bytes = static_cast<uint32_t>(p.inner_elems) * ES;
-    const uint32_t per_atom = inner_bytes / 16;
-    const uint32_t total = static_cast<uint32_t>(p.atoms) * per_atom;
-    const int rc = r / p.rows_per_load;
+    const uint32_t off = u * 16;
+    uint32_t load = off / p.load_smem_bytes;
+    uint32_t within = off - load * p.load_smem_bytes;
+    uint32_t atom;
+    if (p.rank3) {
+        atom = within / p.box_bytes;
+        within -= atom * p.box_bytes;
+    } else {
+        atom = load % p.atoms;
+    }
+    if (within >= p.box_bytes || atom >= static_cast<uint32_t>(p.atoms))
+        return false;   // padding after a box
+    const uint32_t lo = unswizzle(within, p.swizzle_mask);
+    const int64_t col = tb.col0 + static_cast<int64_t>(atom) * p.inner_elems + (lo % inner_bytes) / ES;
+    return col < p.cols;
+}
+
+// Sum of the partials of row r (of the band): its units, box by box.
+template <int DT>
+__device__ __forceinline__ float row_total(const TmaArgs& p, const float* partial, int r)
+{
+    constexpr int ES = DT == TSX_F32 ? 4 : 2;
+    const uint32_t per_row = static_cast<uint32_t>(p.inner_elems) * ES / 16;   // units of one box row
+    const uint32_t rc = static_cast<uint32_t>(r / p.rows_per_load);
     const uint32_t rin = static_cast<uint32_t>(r % p.rows_per_load);
-    float part = 0.f;
-    for (uint32_t j = lane; j < total; j += 32) {
-        const uint32_t a = j / per_atom;
-        const uint32_t q = j % per_atom;
+    float v = 0.f;
+    for (int a = 0; a < p.atoms; ++a) {
         const uint32_t box = p.rank3 ? rc * p.load_smem_bytes + a * p.box_bytes
                                      : (rc * p.atoms + a) * p.load_smem_bytes;
-        const uint32_t within = rin * inner_bytes + q * 16;
-        const uint32_t lo = unswizzle(within, p.swizzle_mask);
-        const int64_t col = tb.col0 + static_cast<int64_t>(a) * p.inner_elems + (lo % inner_bytes) / ES;
-        if (col >= p.cols)
-            continue;
-        const uint32_t off = (box + within) / 16;
-        const uint4* S = reinterpret_cast<const uint4*>(stage);
-        const uint4 va = S[off];
-        const uint4 vb = NIN > 1 ? S[p.slot_bytes / 16 + off] : va;
-        const uint4 vc = NIN > 2 ? S[2 * (p.slot_bytes / 16) + off] : va;
-        add_vec<DT>(part, op_vec16<DT, OP>(va, vb, vc));
+        const uint32_t first = (box + rin * per_row * 16) / 16;
+        for (uint32_t q = 0; q < per_row; ++q)
+            v += partial[first + q];
     }
-    return warp_sum(part);
+    return v;
 }
 
 template <int DT, int OP>
@@ -106,11 +124,13 @@ __global__ void __launch_bounds__(kMaxThreads)
     const int S = p.stages;
     const uint32_t full = base + static_cast<uint32_t>(S) * p.stage_bytes;
     const uint32_t empty = full + 8u * S;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 8u * S - base));
-    float* acc = reinterpret_cast<float*>(smem + (empty + 8u * S + 16 - base));   // one per band row
+    // the compute warps' band barriers: partials complete / partials read
+    const uint32_t band_done = empty + 8u * S;
+    const uint32_t band_free = band_done + 8u;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (band_free + 8u - base));
+    float* partial = reinterpret_cast<float*>(smem + (band_free + 8u + 16 - base));   // one per item
 
     const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
     const int compute_warps = blockDim.x / 32 - 1;
     const int64_t G = gridDim.x;
     const int64_t cta = blockIdx.x;
@@ -128,6 +148,8 @@ __global__ void __launch_bounds__(kMaxThreads)
             mbar_init(full + 8u * s, 1);
             mbar_init(empty + 8u * s, static_cast<uint32_t>(compute_warps));
         }
+        mbar_init(band_done, static_cast<uint32_t>(compute_warps));
+        mbar_init(band_free, static_cast<uint32_t>(compute_warps));
         *abort_flag = 0;
         fence_proxy_async_smem();
     }
@@ -156,30 +178,61 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
     } else {
         // ---------------------------------------------- compute warps
-        const int cw = warp - 1;
+        const uint32_t tid = threadIdx.x - 32;
+        const uint32_t threads = blockDim.x - 32;
+        // stage, phase, band and column tile advance with the tile counter
+        // (no divisions in the loop)
+        uint32_t s = 0, phase = 0, band_parity = 0;
+        int64_t band = cta, ct = 0;
         for (int64_t i = 0; i < N; ++i) {
-            const uint32_t s = static_cast<uint32_t>(i % S);
-            if (!wait_or_abort(full + 8u * s, static_cast<uint32_t>((i / S) & 1), p, abort_flag))
+            if (!wait_or_abort(full + 8u * s, phase, p, abort_flag))
                 break;
-            const TileBoxes tb = tile_boxes(p, tile_of(i));
-            const bool first = i % p.tiles_c == 0;
-            const bool last = i % p.tiles_c == p.tiles_c - 1;
-            const uint8_t* stage = smem + static_cast<size_t>(s) * p.stage_bytes;
-            for (int r = cw; r < p.box_rows; r += compute_warps) {
-                const int64_t row = tb.row0 + r;
-                if (row >= p.rows)
-                    break;   // the rows after it are past the end too
-                const float t = row_of_tile<DT, OP>(p, stage, tb, r, lane);
-                if (lane == 0) {
-                    const float v = first ? t : acc[r] + t;
-                    acc[r] = v;
-                    if (last)
-                        row_sums[row] = v;
-                }
+            TileBoxes tb;
+            tb.row0 = static_cast<int>(band * p.box_rows);
+            tb.col0 = static_cast<int>(ct * p.box_cols);
+            tb.chunks = p.row_chunks;
+            tb.atoms = p.atoms;
+            const bool ragged = tb.col0 + p.box_cols > p.cols;
+            const uint4* stage = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
+            if (ct == 0) {
+                for (uint32_t u = tid; u < p.vec16_per_slot; u += threads)
+                    partial[u] = ragged && !unit_in_columns<DT>(p, tb, u) ? 0.f : unit_sum<DT, OP>(p, stage, u);
+            } else {
+                for (uint32_t u = tid; u < p.vec16_per_slot; u += threads)
+                    partial[u] += ragged && !unit_in_columns<DT>(p, tb, u) ? 0.f : unit_sum<DT, OP>(p, stage, u);
             }
             __syncwarp();
-            if (lane == 0)
+            if ((threadIdx.x & 31) == 0)
                 mbar_arrive(empty + 8u * s);
+            if (ct == p.tiles_c - 1) {
+                // the band is complete once every compute warp has added its
+                // last partials; then each row's partials, box by box
+                if ((threadIdx.x & 31) == 0)
+                    mbar_arrive(band_done);
+                if (!wait_or_abort(band_done, band_parity, p, abort_flag))
+                    break;
+                for (uint32_t r = tid; r < static_cast<uint32_t>(p.box_rows); r += threads) {
+                    const int64_t row = tb.row0 + r;
+                    if (row >= p.rows)
+                        break;
+                    row_sums[row] = row_total<DT>(p, partial, static_cast<int>(r));
+                }
+                // before the next band overwrites the partials
+                __syncwarp();
+                if ((threadIdx.x & 31) == 0)
+                    mbar_arrive(band_free);
+                if (!wait_or_abort(band_free, band_parity, p, abort_flag))
+                    break;
+                band_parity ^= 1;
+                band += G;
+                ct = 0;
+            } else {
+                ++ct;
+            }
+            if (++s == static_cast<uint32_t>(S)) {
+                s = 0;
+                phase ^= 1;
+            }
         }
     }
 
@@ -190,6 +243,8 @@ __global__ void __launch_bounds__(kMaxThreads)
             mbar_inval(full + 8u * s);
             mbar_inval(empty + 8u * s);
         }
+        mbar_inval(band_done);
+        mbar_inval(band_free);
     }
 }
 

@@ -129,3 +129,25 @@ def test_rowsum_edges_and_declines(tsx):
         rc = tsx.tsx_reduce_rows(plan.handle, tsx.OPS["copy"] | tsx.TSX_ACCUMULATE, a.data_ptr(), None, None,
                                  out.data_ptr(), 0)
         assert rc == tsx.TSX_ERR_INVALID
+
+
+def test_rowsum_wait_timeout_is_reported(tsx, monkeypatch):
+    """The producer is told to skip one tile's loads: the compute warps'
+    bounded wait gives up, TSX_ERR_TIMEOUT is recorded, and the GPU stays
+    usable."""
+    rows, cols = 64, 1024
+    a = _values("f32", (rows, cols), 6)
+    monkeypatch.setenv("TSX_FAULT_SKIP_TILE", "9")
+    monkeypatch.setenv("TSX_TIMEOUT_MS", "50")
+    bad = tsx.Plan("f32", rows, cols, box=(8, 128), stages=3)
+    monkeypatch.delenv("TSX_FAULT_SKIP_TILE")
+    monkeypatch.delenv("TSX_TIMEOUT_MS")
+    da = to_dev(a, "f32")
+    try:
+        bad.reduce_rows("copy", da)
+        torch.cuda.synchronize()
+        assert bad.status() == tsx.TSX_ERR_TIMEOUT
+    finally:
+        bad.close()
+    got = _rowsum(tsx, "f32", rows, cols, (8, 128), 3, "tma", "copy", [a])
+    _check(got, "copy", "f32", [a], cols, "after the timeout")
