@@ -128,6 +128,8 @@ typedef struct tsx_plan_info {
     /* threads of one CTA: for the TMA variants the elementwise threads plus
      * a producer warp and a store warp */
     int32_t block_threads;
+    /* elements between the starts of consecutive rows (cols for dense rows) */
+    int64_t pitch;
 } tsx_plan_info;
 
 /* Create a plan for [rows, cols] tensors of `dtype`, streamed in stage
@@ -140,6 +142,17 @@ typedef struct tsx_plan_info {
  * Returns NULL on failure (tsx_last_error() says why). */
 tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols,
                            int stages, tsx_variant variant);
+
+/* tsx_plan_create for tensors whose rows start `pitch` elements apart
+ * (pitch >= cols; the elements between a row's end and the next row's start
+ * are neither read nor written): element (r, c) is at byte offset
+ * (r * pitch + c) * element_size.  Every operand and the output use this
+ * pitch.  TMA variants need pitch * element_size to be a multiple of 16
+ * bytes; TSX_LDGSTS / TSX_SYNC narrow their copy width to what divides it.
+ * This is the strided form of the tensors of TVM docs "copy_async -> tma"
+ * ("Algorithm" step 3: the global strides passed to the tensor map). */
+tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                   int box_cols, int stages, tsx_variant variant);
 
 /* out = op(a, b, c) element by element over the plan's [rows, cols]
  * (out += op(a, b, c) with TSX_ACCUMULATE).
@@ -197,6 +210,10 @@ const char *tsx_last_error(void);
  * tsx_plan_create / tsx_ewise would return. */
 int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
                    tsx_variant variant, tsx_op op, tsx_plan_info *info);
+
+/* tsx_plan_query for rows `pitch` elements apart (see tsx_plan_create_pitched). */
+int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols,
+                           int stages, tsx_variant variant, tsx_op op, tsx_plan_info *info);
 
 /* tsx_plan_query for an existing plan, including the launch it makes on its
  * device (occupancy-derived CTAs per SM and grid).  Both accept an op with

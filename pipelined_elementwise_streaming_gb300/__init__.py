@@ -52,7 +52,8 @@ class tsx_plan_info(ctypes.Structure):
                [(n, ctypes.c_int32) for n in ("interleave", "swizzle", "l2_promotion", "oob_fill",
                                                "threads", "vec", "outer", "copy_vec_bytes",
                                                "slot_bytes", "stage_bytes", "smem_bytes",
-                                               "ctas_per_sm", "grid", "sm_count", "block_threads")]
+                                               "ctas_per_sm", "grid", "sm_count", "block_threads")] + \
+               [("pitch", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         d = {}
@@ -72,6 +73,13 @@ def _load():
                                   ctypes.c_int, ctypes.c_int]
     L.tsx_ewise.restype = ctypes.c_int
     L.tsx_ewise.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5
+    L.tsx_plan_create_pitched.restype = ctypes.c_void_p
+    L.tsx_plan_create_pitched.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.tsx_plan_query_pitched.restype = ctypes.c_int
+    L.tsx_plan_query_pitched.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(tsx_plan_info)]
     L.tsx_plan_destroy.restype = None
     L.tsx_plan_destroy.argtypes = [ctypes.c_void_p]
     L.tsx_plan_status.restype = ctypes.c_int
@@ -96,6 +104,8 @@ lib = _load()
 
 # The C entry points under their own names (plain integers / addresses).
 tsx_plan_create = lib.tsx_plan_create
+tsx_plan_create_pitched = lib.tsx_plan_create_pitched
+tsx_plan_query_pitched = lib.tsx_plan_query_pitched
 tsx_ewise = lib.tsx_ewise
 tsx_plan_destroy = lib.tsx_plan_destroy
 tsx_plan_status = lib.tsx_plan_status
@@ -115,11 +125,11 @@ def _code(table: dict, key) -> int:
     return table[key] if isinstance(key, str) else int(key)
 
 
-def query(dtype, rows, cols, box, stages, variant="tma", op="copy") -> dict:
+def query(dtype, rows, cols, box, stages, variant="tma", op="copy", pitch=None) -> dict:
     """The plan and launch shape the library would use (host only, no GPU)."""
     info = tsx_plan_info()
-    rc = tsx_plan_query(_code(DTYPES, dtype), rows, cols, box[0], box[1], stages, _code(VARIANTS, variant),
-                        _code(OPS, op), ctypes.byref(info))
+    rc = tsx_plan_query_pitched(_code(DTYPES, dtype), rows, cols, cols if pitch is None else pitch, box[0], box[1],
+                                stages, _code(VARIANTS, variant), _code(OPS, op), ctypes.byref(info))
     if rc != TSX_OK:
         raise TsxError(rc, tsx_last_error())
     return info.as_dict()
@@ -131,11 +141,13 @@ _TORCH_DTYPE_NAME = {"torch.float16": "f16", "torch.bfloat16": "bf16", "torch.fl
 class Plan:
     """A tsx plan bound to the current CUDA device."""
 
-    def __init__(self, dtype: str, rows: int, cols: int, box=(32, 32), stages: int = 2, variant: str = "tma"):
+    def __init__(self, dtype: str, rows: int, cols: int, box=(32, 32), stages: int = 2, variant: str = "tma",
+                 pitch: int | None = None):
         self.dtype, self.rows, self.cols = dtype, int(rows), int(cols)
+        self.pitch = self.cols if pitch is None else int(pitch)
         self.box, self.stages, self.variant = (int(box[0]), int(box[1])), int(stages), variant
-        h = tsx_plan_create(_code(DTYPES, dtype), self.rows, self.cols, self.box[0], self.box[1], self.stages,
-                            _code(VARIANTS, variant))
+        h = tsx_plan_create_pitched(_code(DTYPES, dtype), self.rows, self.cols, self.pitch, self.box[0], self.box[1],
+                                    self.stages, _code(VARIANTS, variant))
         if not h:
             raise TsxError(TSX_ERR_UNSUPPORTED, tsx_last_error())
         self.handle = h
@@ -147,8 +159,13 @@ class Plan:
             raise TsxError(TSX_ERR_INVALID, f"{name} must be a CUDA tensor")
         if _TORCH_DTYPE_NAME.get(str(t.dtype)) != self.dtype:
             raise TsxError(TSX_ERR_INVALID, f"{name} has dtype {t.dtype}, the plan is {self.dtype}")
-        if t.numel() != self.rows * self.cols or not t.is_contiguous():
-            raise TsxError(TSX_ERR_INVALID, f"{name} must be a contiguous [{self.rows}, {self.cols}] tensor")
+        if self.pitch == self.cols:
+            if t.numel() != self.rows * self.cols or not t.is_contiguous():
+                raise TsxError(TSX_ERR_INVALID, f"{name} must be a contiguous [{self.rows}, {self.cols}] tensor")
+        elif (tuple(t.shape) != (self.rows, self.cols) or t.stride(-1) != 1
+              or (self.rows > 1 and t.stride(0) != self.pitch)):
+            raise TsxError(TSX_ERR_INVALID, f"{name} must be a [{self.rows}, {self.cols}] view with row stride "
+                                            f"{self.pitch}")
         return t.data_ptr()
 
     def ewise_ptr(self, op, a: int, b: int | None, c: int | None, out: int, stream: int = 0) -> None:
@@ -165,7 +182,10 @@ class Plan:
         if out is None:
             if accumulate:
                 raise TsxError(TSX_ERR_INVALID, "accumulate needs an out tensor to add into")
-            out = torch.empty_like(a)
+            if self.pitch == self.cols:
+                out = torch.empty_like(a)
+            else:
+                out = torch.empty(self.rows, self.pitch, dtype=a.dtype, device=a.device)[:, : self.cols]
         pa, pb, pc, po = (self._check(a, "a"), self._check(b, "b"), self._check(c, "c"), self._check(out, "out"))
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         code = _code(OPS, op) | (TSX_ACCUMULATE if accumulate else 0)

@@ -247,6 +247,7 @@ void fill_tma_args(const tsx_plan* p, const OpGeometry& og, TmaArgs* args)
     args->tiles = g.tiles;
     args->tiles_c = g.tiles_c;
     args->tiles_r = g.tiles_r;
+    args->pitch = g.pitch;
     args->fault_tile = p->fault_tile;
     args->status = p->d_status;
     args->timeout_ns = p->timeout_ns;
@@ -353,9 +354,15 @@ extern "C" {
 tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
                            tsx_variant variant)
 {
+    return tsx_plan_create_pitched(dtype, rows, cols, cols, box_rows, box_cols, stages, variant);
+}
+
+tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                   int box_cols, int stages, tsx_variant variant)
+{
     std::string why;
     Geometry g;
-    int rc = make_geometry(dtype, rows, cols, box_rows, box_cols, stages, variant, &g, &why);
+    int rc = make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, &g, &why);
     if (rc != TSX_OK) {
         set_error(rc, why);
         return nullptr;
@@ -498,6 +505,7 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
         CopyArgs args{};
         args.rows = g.rows;
         args.cols = g.cols;
+        args.pitch = g.pitch;
         args.tiles = g.tiles;
         args.tiles_c = g.tiles_c;
         args.box_rows = g.box_rows;

@@ -35,7 +35,7 @@ __device__ __forceinline__ void issue_tile_cp_async(const CopyArgs& p, uint8_t* 
             int64_t row, col;
             chunk_position<ES>(p, row0, col0, q * p.vec_bytes, row, col);
             const bool in = row < p.rows && col < p.cols;
-            const char* gp = in ? g + (row * p.cols + col) * ES : g;
+            const char* gp = in ? g + (row * p.pitch + col) * ES : g;
             cp_async(slot + q * p.vec_bytes, gp, p.vec_bytes, in ? p.vec_bytes : 0u);
         }
     }

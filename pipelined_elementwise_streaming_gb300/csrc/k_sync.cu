@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kMaxThreads)
                 int64_t row, col;
                 chunk_position<ES>(p, row0, col0, q * p.vec_bytes, row, col);
                 const bool in = row < p.rows && col < p.cols;
-                load_piece(slot + q * p.vec_bytes, in ? g + (row * p.cols + col) * ES : g, p.vec_bytes, in);
+                load_piece(slot + q * p.vec_bytes, in ? g + (row * p.pitch + col) * ES : g, p.vec_bytes, in);
             }
         }
         __syncthreads();

@@ -97,7 +97,7 @@ __device__ __forceinline__ void compute_tile_mixed(const TmaArgs& p, uint4* A, c
             const int64_t row = tb.row0 + static_cast<int64_t>(load / p.atoms) * p.rows_per_load + lo / inner_bytes;
             const int64_t col = tb.col0 + static_cast<int64_t>(load % p.atoms) * p.inner_elems + (lo % inner_bytes) / ES;
             if (row < p.rows && col < p.cols)
-                vb = *reinterpret_cast<const uint4*>(Bg + (row * p.cols + col) * ES);
+                vb = *reinterpret_cast<const uint4*>(Bg + (row * p.pitch + col) * ES);
         }
         const uint4 va = A[u];
         const uint4 vc = op_arity(OP) > 2 ? C[u] : va;

@@ -155,6 +155,7 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
     TmaArgs args{};
     args.tiles = g.tiles;
     args.tiles_c = g.tiles_c;
+    args.pitch = g.pitch;
     args.fault_tile = -1;
     args.status = scratch;
     const char* ms = std::getenv("TSX_TIMEOUT_MS");

@@ -71,8 +71,8 @@ int default_store_lag(int stages)
     return lag < 0 ? 0 : lag > 3 ? 3 : lag;
 }
 
-int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
-                  Geometry* g, std::string* why)
+int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,
+                  int variant, Geometry* g, std::string* why)
 {
     *g = Geometry{};
     if (dtype < TSX_F16 || dtype > TSX_F32)
@@ -81,7 +81,9 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
         return fail(why, "unknown variant %lld", variant), TSX_ERR_INVALID;
     if (rows < 0 || cols < 0)
         return fail(why, "negative shape %lld x %lld", rows, cols), TSX_ERR_INVALID;
-    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31))
+    if (pitch < cols)
+        return fail(why, "the row pitch (%lld) is shorter than a row (%lld)", pitch, cols), TSX_ERR_INVALID;
+    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31) || pitch >= (int64_t(1) << 40))
         return fail(why, "rows and cols must be < 2^31 (got %lld x %lld)", rows, cols), TSX_ERR_UNSUPPORTED;
     if (box_rows < 1 || box_cols < 1)
         return fail(why, "box dims must be >= 1 (got %lld x %lld)", box_rows, box_cols), TSX_ERR_UNSUPPORTED;
@@ -94,6 +96,7 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
     g->variant = variant;
     g->rows = rows;
     g->cols = cols;
+    g->pitch = pitch;
     g->box_rows = box_rows;
     g->box_cols = box_cols;
     g->stages = stages;
@@ -108,8 +111,9 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
 
     if (is_tma_variant(variant)) {
         // Global strides of a tensor map are multiples of 16 bytes.
-        if ((cols * es) % 16)
-            return fail(why, "TMA needs a row pitch that is a multiple of 16 bytes (cols * elem = %lld)", cols * es),
+        if ((pitch * es) % 16)
+            return fail(why, "TMA needs a row pitch that is a multiple of 16 bytes (pitch * elem = %lld)",
+                        pitch * es),
                    TSX_ERR_UNSUPPORTED;
         // The innermost box spans at most one 128-byte swizzle atom and a
         // whole number of 16-byte units; a wider tile row is several atoms.
@@ -161,7 +165,7 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_c
         // row is taken (base pointers are checked per call).
         int vb = 0;
         for (int cand : {16, 8, 4}) {
-            if ((cols * es) % cand == 0 && row_bytes % cand == 0) {
+            if ((pitch * es) % cand == 0 && row_bytes % cand == 0) {
                 vb = cand;
                 break;
             }
@@ -222,6 +226,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->stages = g.stages;
     info->rows = g.rows;
     info->cols = g.cols;
+    info->pitch = g.pitch;
     info->tiles = g.tiles;
     info->tiles_r = g.tiles_r;
     info->tiles_c = g.tiles_c;
@@ -271,7 +276,7 @@ void tensor_map_args(const Geometry& g, TensorMapArgs* m)
         m->dims[0] = uint64_t(g.inner_elems);
         m->dims[1] = rows;
         m->dims[2] = cols / uint64_t(g.inner_elems);
-        m->strides[0] = cols * uint64_t(g.es);
+        m->strides[0] = uint64_t(g.pitch) * uint64_t(g.es);
         m->strides[1] = uint64_t(g.inner_bytes);
         m->box[0] = uint32_t(g.inner_elems);
         m->box[1] = uint32_t(g.rows_per_load);
@@ -280,7 +285,7 @@ void tensor_map_args(const Geometry& g, TensorMapArgs* m)
         m->rank = 2;
         m->dims[0] = cols;
         m->dims[1] = rows;
-        m->strides[0] = cols * uint64_t(g.es);
+        m->strides[0] = uint64_t(g.pitch) * uint64_t(g.es);
         m->box[0] = uint32_t(g.inner_elems);
         m->box[1] = uint32_t(g.rows_per_load);
     }
@@ -288,8 +293,9 @@ void tensor_map_args(const Geometry& g, TensorMapArgs* m)
 
 }  // namespace tsx
 
-extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
-                              tsx_variant variant, tsx_op op_arg, tsx_plan_info* info)
+extern "C" int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                      int box_cols, int stages, tsx_variant variant, tsx_op op_arg,
+                                      tsx_plan_info* info)
 {
     std::string why;
     tsx::Geometry g;
@@ -303,7 +309,7 @@ extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int b
         tsx::set_last_error("TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
         return TSX_ERR_UNSUPPORTED;
     }
-    int rc = tsx::make_geometry(dtype, rows, cols, box_rows, box_cols, stages, variant, &g, &why);
+    int rc = tsx::make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, &g, &why);
     if (rc == TSX_OK) {
         tsx::OpGeometry og;
         rc = tsx::make_op_geometry(g, op, tsx::kMaxDynSmem, &og, &why);
@@ -312,4 +318,10 @@ extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int b
     }
     tsx::set_last_error(rc == TSX_OK ? "" : why.c_str());
     return rc;
+}
+
+extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
+                              tsx_variant variant, tsx_op op, tsx_plan_info* info)
+{
+    return tsx_plan_query_pitched(dtype, rows, cols, cols, box_rows, box_cols, stages, variant, op, info);
 }

@@ -13,6 +13,7 @@ namespace tsx {
 struct Geometry {
     int dtype = 0, es = 0, variant = 0, stages = 0;
     int64_t rows = 0, cols = 0;
+    int64_t pitch = 0;       // elements between row starts (>= cols)
     int box_rows = 0, box_cols = 0;
     int64_t tiles_r = 0, tiles_c = 0, tiles = 0;
     int store_lag = 1;       // TMA: tiles between a store's issue and its stage's release
@@ -47,8 +48,14 @@ struct TensorMapArgs {
 
 int default_threads(int variant, size_t smem_bytes);
 int default_store_lag(int stages);
-int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages, int variant,
-                  Geometry* g, std::string* why);
+int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,
+                  int variant, Geometry* g, std::string* why);
+// Dense rows: pitch = cols.
+inline int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
+                         int variant, Geometry* g, std::string* why)
+{
+    return make_geometry(dtype, rows, cols, cols, box_rows, box_cols, stages, variant, g, why);
+}
 int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, std::string* why);
 void tensor_map_args(const Geometry& g, TensorMapArgs* m);
 void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info);

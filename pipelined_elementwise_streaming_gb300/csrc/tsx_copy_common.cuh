@@ -58,7 +58,7 @@ __device__ __forceinline__ void ewise_tile_to_global(const CopyArgs& p, const ui
             int64_t row, col;
             chunk_position<ES>(p, row0, col0, byte, row, col);
             if (row < p.rows && col < p.cols)
-                store_piece(static_cast<char*>(out) + (row * p.cols + col) * ES, r, piece, p.vec_bytes);
+                store_piece(static_cast<char*>(out) + (row * p.pitch + col) * ES, r, piece, p.vec_bytes);
         }
     }
 }

@@ -42,6 +42,7 @@ struct TmaArgs {
     int64_t tiles;          // T: tiles in the tensor
     int64_t tiles_c;        // tiles along a row
     int64_t tiles_r;        // row bands
+    int64_t pitch;          // elements between the starts of consecutive rows
     int64_t fault_tile;     // test hook: the producer skips this tile's loads (-1: none)
     int* status;            // device status word (TSX_OK until a wait gives up)
     uint64_t timeout_ns;    // limit of every mbarrier wait
@@ -68,6 +69,7 @@ struct TmaArgs {
 // Kernel arguments of the cp.async and synchronous ablation kernels.
 struct CopyArgs {
     int64_t rows, cols;
+    int64_t pitch;            // elements between the starts of consecutive rows
     int64_t tiles, tiles_c;
     int box_rows, box_cols;
     int stages;

@@ -186,6 +186,25 @@ def test_query_accumulate_flag(tsx):
     assert ei.value.code == tsx.TSX_ERR_INVALID
 
 
+def test_query_pitched_rows(tsx):
+    """Rows `pitch` elements apart: the tensor map's row stride is the pitch,
+    which TMA needs to be a multiple of 16 bytes; the copy variants narrow
+    their width to what divides it."""
+    q = tsx.query("f32", 100, 100, (8, 32), 2, "tma", "copy", pitch=104)
+    assert q["pitch"] == 104 and q["global_stride_bytes"][0] == 416 and q["global_dim"][:2] == [100, 100]
+    q = tsx.query("f16", 8, 256, (8, 256), 1, "tma_rank3", "copy", pitch=320)
+    assert q["global_stride_bytes"][:2] == [640, 128]
+    with pytest.raises(tsx.TsxError) as ei:
+        tsx.query("f32", 100, 100, (8, 32), 2, "tma", "copy", pitch=102)        # 408-byte rows
+    assert ei.value.code == tsx.TSX_ERR_UNSUPPORTED
+    with pytest.raises(tsx.TsxError) as ei:
+        tsx.query("f32", 100, 100, (8, 32), 2, "tma", "copy", pitch=96)         # shorter than a row
+    assert ei.value.code == tsx.TSX_ERR_INVALID
+    assert tsx.query("f16", 64, 64, (8, 64), 2, "ldgsts", "copy", pitch=68)["copy_vec_bytes"] == 8
+    assert tsx.query("f16", 64, 64, (8, 64), 2, "sync", "copy", pitch=66)["copy_vec_bytes"] == 4
+    assert tsx.query("f32", 100, 128, (8, 32), 2, "tma", "copy")["pitch"] == 128
+
+
 def test_query_empty_tensor_is_legal(tsx):
     q = tsx.query("f32", 0, 128, (8, 32), 2, "tma", "copy")
     assert q["tiles"] == 0
