@@ -65,8 +65,16 @@ typedef enum { TSX_F16 = 0, TSX_BF16 = 1, TSX_F32 = 2 } tsx_dtype;
  *                threads with plain vector loads from global memory: one
  *                operand through the TMA circular buffer, the other through
  *                ordinary loads (nvFuser PR #2833, "Testing Setup",
- *                Pointwise).  Unary ops run as TSX_TMA. */
-typedef enum { TSX_TMA = 0, TSX_LDGSTS = 1, TSX_SYNC = 2, TSX_TMA_RANK3 = 3, TSX_TMA_MIXED = 4 } tsx_variant;
+ *                Pointwise).  Unary ops run as TSX_TMA.
+ *  TSX_TMA_PROMOTED  one box per <= 256-row chunk spans the whole tile row,
+ *                with no swizzle: the tensor map counts in elements widened
+ *                along 1 -> 2 -> 4 -> 8 bytes until the row holds at most
+ *                256 of them ("copy_async -> tma", table under "How inputs
+ *                change the algorithm": box > 256 triggers element-type
+ *                promotion).  Declines when even 8 bytes cannot. */
+typedef enum {
+    TSX_TMA = 0, TSX_LDGSTS = 1, TSX_SYNC = 2, TSX_TMA_RANK3 = 3, TSX_TMA_MIXED = 4, TSX_TMA_PROMOTED = 5
+} tsx_variant;
 
 /* Elementwise ops ("elementwise -> smem", table under "How inputs change
  * the algorithm").  copy moves bits unchanged; sqrt and add/mul/fma are
@@ -130,6 +138,9 @@ typedef struct tsx_plan_info {
     int32_t block_threads;
     /* elements between the starts of consecutive rows (cols for dense rows) */
     int64_t pitch;
+    /* element size the tensor map counts in: elem_size, or the wider one
+     * of TSX_TMA_PROMOTED */
+    int32_t tma_elem_bytes;
 } tsx_plan_info;
 
 /* Create a plan for [rows, cols] tensors of `dtype`, streamed in stage

@@ -127,6 +127,27 @@ def split(dtype: str, box_rows: int, box_cols: int, mode: str = "rank2", cols: i
     raise ValueError(mode)
 
 
+PROMOTION_CHAIN = (1, 2, 4, 8)   # element sizes a descriptor may be widened to
+
+
+def promote(es: int, row_bytes: int, cols_bytes: int):
+    """Element size for a box that spans a whole tile row without a swizzle.
+
+    TVM docs "copy_async -> tma", table under "How inputs change the
+    algorithm": a box of more than 256 elements triggers element-type
+    promotion along 1 -> 2 -> 4 -> 8 bytes.  The smallest size of the chain,
+    at least the element's own, that holds the row in at most 256 elements
+    and divides both the tile row and the tensor row; None when even 8
+    bytes cannot (the variant declines).
+    """
+    for pes in PROMOTION_CHAIN:
+        if pes < es or row_bytes % pes or cols_bytes % pes:
+            continue
+        if row_bytes // pes <= BOX_MAX:
+            return pes
+    return None
+
+
 def encode_args(dtype: str, rows: int, cols: int, sp: Split) -> tuple:
     """The tiled-encode argument list, in the TVM page's order.
 

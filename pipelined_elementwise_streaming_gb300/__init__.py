@@ -24,7 +24,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtsx.so")
 
 DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
-VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3, "tma_mixed": 4}
+VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3, "tma_mixed": 4, "tma_promoted": 5}
 OPS = {"copy": 0, "sqrt": 1, "exp": 2, "add": 3, "mul": 4, "fma": 5}
 TSX_ACCUMULATE = 0x100   # OR into an op: out += op(a, b, c) by TMA reduce-store
 ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
@@ -53,7 +53,7 @@ class tsx_plan_info(ctypes.Structure):
                                                "threads", "vec", "outer", "copy_vec_bytes",
                                                "slot_bytes", "stage_bytes", "smem_bytes",
                                                "ctas_per_sm", "grid", "sm_count", "block_threads")] + \
-               [("pitch", ctypes.c_int64)]
+               [("pitch", ctypes.c_int64), ("tma_elem_bytes", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {}

@@ -87,6 +87,16 @@ CUtensorMapDataType map_dtype(int dtype)
                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 }
 
+// A promoted map moves the same bytes in wider unsigned elements.
+CUtensorMapDataType map_type(const Geometry& g)
+{
+    if (g.tma_es == g.es)
+        return map_dtype(g.dtype);
+    return g.tma_es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+         : g.tma_es == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                         : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+}
+
 }  // namespace
 
 void set_last_error(const char* msg) { store_message(msg); }
@@ -199,7 +209,7 @@ int encode_tensor_map(const Geometry& g, const void* ptr, CUtensorMap* map)
     }
     for (int d = 0; d + 1 < m.rank; ++d)
         strides[d] = m.strides[d];
-    const CUresult r = fn(map, map_dtype(g.dtype), cuuint32_t(m.rank), const_cast<void*>(ptr), dims, strides, box,
+    const CUresult r = fn(map, map_type(g), cuuint32_t(m.rank), const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(m.swizzle),
                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -267,6 +277,7 @@ void fill_tma_args(const tsx_plan* p, const OpGeometry& og, TmaArgs* args)
     args->bytes_per_load = uint32_t(g.bytes_per_load);
     args->vec16_per_slot = og.vec16_per_slot;
     args->store_lag = g.store_lag;
+    args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
     args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
 }

@@ -67,10 +67,11 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
         } else {
             for (int a = 0; a < b.atoms; ++a) {
                 const uint32_t src = slot + (r * p.atoms + a) * p.load_smem_bytes;
+                const int x = (b.col0 + a * p.inner_elems) >> p.promote_shift;
                 if constexpr (ACC)
-                    tma_reduce_add_2d(&maps.m[3], src, b.col0 + a * p.inner_elems, y);
+                    tma_reduce_add_2d(&maps.m[3], src, x, y);
                 else
-                    tma_store_2d(&maps.m[3], src, b.col0 + a * p.inner_elems, y);
+                    tma_store_2d(&maps.m[3], src, x, y);
             }
         }
     }

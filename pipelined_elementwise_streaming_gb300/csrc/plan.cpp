@@ -77,7 +77,7 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
     *g = Geometry{};
     if (dtype < TSX_F16 || dtype > TSX_F32)
         return fail(why, "unknown dtype %lld", dtype), TSX_ERR_INVALID;
-    if (variant < TSX_TMA || variant > TSX_TMA_MIXED)
+    if (variant < TSX_TMA || variant > TSX_TMA_PROMOTED)
         return fail(why, "unknown variant %lld", variant), TSX_ERR_INVALID;
     if (rows < 0 || cols < 0)
         return fail(why, "negative shape %lld x %lld", rows, cols), TSX_ERR_INVALID;
@@ -119,7 +119,27 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
         // whole number of 16-byte units; a wider tile row is several atoms.
         if (row_bytes % 16)
             return fail(why, "a tile row of %lld bytes is not a multiple of 16", row_bytes), TSX_ERR_UNSUPPORTED;
-        const int inner_bytes = row_bytes < kSwizzleAtom ? int(row_bytes) : kSwizzleAtom;
+        // Element-type promotion: one box spans the whole tile row, with no
+        // swizzle, viewed in elements widened along 1 -> 2 -> 4 -> 8 bytes
+        // until the row holds at most 256 of them.
+        int tma_es = es;
+        if (variant == TSX_TMA_PROMOTED) {
+            tma_es = 0;
+            for (int pes : {1, 2, 4, 8}) {
+                if (pes < es || row_bytes % pes || (cols * es) % pes)
+                    continue;
+                if (row_bytes / pes <= kBoxMax) {
+                    tma_es = pes;
+                    break;
+                }
+            }
+            if (!tma_es)
+                return fail(why, "no element of 8 bytes or less holds a %lld-byte tile row in 256", row_bytes),
+                       TSX_ERR_UNSUPPORTED;
+        }
+        g->tma_es = tma_es;
+        const int inner_bytes = variant == TSX_TMA_PROMOTED ? int(row_bytes)
+                              : row_bytes < kSwizzleAtom ? int(row_bytes) : kSwizzleAtom;
         if (row_bytes % inner_bytes)
             return fail(why, "a tile row of %lld bytes is not a whole number of 128-byte atoms", row_bytes),
                    TSX_ERR_UNSUPPORTED;
@@ -134,7 +154,8 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
         g->atoms = int(row_bytes / inner_bytes);
         g->row_chunks = chunks;
         g->rows_per_load = box_rows / chunks;
-        g->swizzle_bytes = (inner_bytes == 32 || inner_bytes == 64 || inner_bytes == 128) ? inner_bytes : 0;
+        g->swizzle_bytes = variant != TSX_TMA_PROMOTED && (inner_bytes == 32 || inner_bytes == 64 || inner_bytes == 128)
+                               ? inner_bytes : 0;
         const uint32_t atom_bytes = uint32_t(g->rows_per_load) * inner_bytes;
         if (variant != TSX_TMA_RANK3) {
             g->loads_per_operand = g->atoms * g->row_chunks;
@@ -240,6 +261,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->tx_bytes = int32_t(og.tx_bytes);
     info->threads = og.threads;
     info->block_threads = og.block_threads;
+    info->tma_elem_bytes = g.tma_es;
     info->vec = og.vec;
     info->outer = og.outer;
     info->copy_vec_bytes = g.copy_vec_bytes;
@@ -282,11 +304,13 @@ void tensor_map_args(const Geometry& g, TensorMapArgs* m)
         m->box[1] = uint32_t(g.rows_per_load);
         m->box[2] = uint32_t(g.atoms);
     } else {
+        // rank 2; a promoted map counts the row in its wider elements
+        const uint64_t widen = uint64_t(g.tma_es) / uint64_t(g.es);
         m->rank = 2;
-        m->dims[0] = cols;
+        m->dims[0] = cols / widen;
         m->dims[1] = rows;
         m->strides[0] = uint64_t(g.pitch) * uint64_t(g.es);
-        m->box[0] = uint32_t(g.inner_elems);
+        m->box[0] = uint32_t(uint64_t(g.inner_elems) / widen);
         m->box[1] = uint32_t(g.rows_per_load);
     }
 }

@@ -20,6 +20,7 @@ struct Geometry {
     // TMA split
     int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
     int loads_per_operand = 0, bytes_per_load = 0, swizzle_bytes = 0;
+    int tma_es = 0;          // element size the tensor map uses (> es when promoted)
     uint32_t load_smem_bytes = 0;
     // one operand's tile in shared memory
     uint32_t slot_bytes = 0;

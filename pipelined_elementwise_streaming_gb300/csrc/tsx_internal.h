@@ -30,7 +30,10 @@ constexpr int kTmaBarrierBytes = 24;   // full, computed and empty mbarriers of 
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
 TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }
-TSX_HD constexpr bool is_tma_variant(int v) { return v == TSX_TMA || v == TSX_TMA_RANK3 || v == TSX_TMA_MIXED; }
+TSX_HD constexpr bool is_tma_variant(int v)
+{
+    return v == TSX_TMA || v == TSX_TMA_RANK3 || v == TSX_TMA_MIXED || v == TSX_TMA_PROMOTED;
+}
 // Operands that go through the TMA ring: all of them, except b for the mixed variant.
 TSX_HD constexpr int tma_operands(int variant, int op)
 {
@@ -47,6 +50,7 @@ struct TmaArgs {
     int* status;            // device status word (TSX_OK until a wait gives up)
     uint64_t timeout_ns;    // limit of every mbarrier wait
     int store_lag;          // tiles between a store's issue and its stage's release
+    int promote_shift;      // log2(tensor-map element / element): box x coordinates are in map elements
     int rows, cols;         // tensor extent (< 2^31)
     int box_rows, box_cols;
     int stages;

@@ -59,7 +59,7 @@ __device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p
             } else {
                 for (int a = 0; a < b.atoms; ++a)
                     tma_load_2d(slot + (r * p.atoms + a) * p.load_smem_bytes, &maps.m[j],
-                                b.col0 + a * p.inner_elems, y, bar);
+                                (b.col0 + a * p.inner_elems) >> p.promote_shift, y, bar);
             }
         }
     }

@@ -205,6 +205,29 @@ def test_query_pitched_rows(tsx):
     assert tsx.query("f32", 100, 128, (8, 32), 2, "tma", "copy")["pitch"] == 128
 
 
+def test_query_promoted_matches_oracle(tsx):
+    """One box spans the tile row, its element widened along 1 -> 2 -> 4 ->
+    8 bytes until the row holds at most 256 (oracle: structure.promote)."""
+    n = 0
+    for dtype, es in st.ELEM_SIZE.items():
+        for bc in (8, 64, 128, 200, 256, 384, 512, 768, 1024, 2048):
+            for cols in (4096, 4100, 1000):
+                row_bytes, cols_bytes = bc * es, cols * es
+                pes = st.promote(es, row_bytes, cols_bytes) if row_bytes % 16 == 0 else None
+                try:
+                    q = tsx.query(dtype, 64, cols, (8, bc), 2, "tma_promoted", "add")
+                except tsx.TsxError as e:
+                    assert pes is None or "shared memory" in str(e) or cols_bytes % 16, (dtype, bc, cols, str(e))
+                    continue
+                assert pes is not None, (dtype, bc, cols)
+                assert q["tma_elem_bytes"] == pes and q["swizzle"] == 0 and q["atoms"] == 1
+                assert q["box_dim"][:2] == [row_bytes // pes, 8]
+                assert q["global_dim"][:2] == [cols_bytes // pes, 64]
+                assert q["loads_per_operand"] == 1 and q["tx_bytes"] == 2 * 8 * row_bytes
+                n += 1
+    assert n > 20
+
+
 def test_query_empty_tensor_is_legal(tsx):
     q = tsx.query("f32", 0, 128, (8, 32), 2, "tma", "copy")
     assert q["tiles"] == 0

@@ -34,7 +34,7 @@ def _embedded(bits, dtype, pad):
     return buf, buf[pad:pad + bits.size].view(bits.shape)
 
 
-@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "tma_mixed", "ldgsts", "sync"])
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "tma_mixed", "tma_promoted", "ldgsts", "sync"])
 def test_canaries_and_inputs_untouched(tsx, variant):
     dtype, rows, cols, box = "f32", 77, 320, (16, 64)
     ins = [random_bits(dtype, (rows, cols), 40 + k) for k in range(3)]

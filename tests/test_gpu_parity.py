@@ -51,7 +51,7 @@ SHAPES = {
 }
 
 
-@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "tma_mixed", "ldgsts", "sync"])
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3", "tma_mixed", "tma_promoted", "ldgsts", "sync"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("op", OPS)
 def test_parity_small_shapes(tsx, variant, dtype, op):
@@ -89,6 +89,27 @@ def test_every_swizzle_mode(tsx, variant, dtype):
                               seed=zlib.crc32(f"swz/{variant}/{dtype}/{row_bytes}/{box_rows}/{op}".encode()))
                 n += 1
     assert n == 42
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_promoted_wide_tiles(tsx, dtype):
+    """Tile rows wider than 256 elements in one box: the tensor map counts
+    in 4- or 8-byte elements (element-type promotion), with ragged column
+    and row tails."""
+    es = 4 if dtype == "f32" else 2
+    n = 0
+    for box_cols in (256, 512, 768, 1024):
+        for rows, cols, box_rows in ((45, 2 * box_cols + 8 * (8 // es), 8), (30, box_cols, 8)):
+            try:
+                q = tsx.query(dtype, rows, cols, (box_rows, box_cols), 3, "tma_promoted", "fma")
+            except tsx.TsxError:
+                continue
+            assert q["tma_elem_bytes"] >= es
+            for op in ("fma", "exp"):
+                run_and_check(tsx, dtype, rows, cols, (box_rows, box_cols), 3, "tma_promoted", op,
+                              seed=zlib.crc32(f"promo/{dtype}/{box_cols}/{rows}/{op}".encode()))
+            n += 1
+    assert n >= 4
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3, 5, 8])

@@ -105,6 +105,27 @@ def test_split_declines():
     assert st.split("f16", 8, 256, "rank3", cols=100) is None   # row not a whole number of atoms
 
 
+def test_promotion_chain():
+    """TVM docs "copy_async -> tma": a box over 256 elements is widened along
+    1 -> 2 -> 4 -> 8 bytes."""
+    assert st.promote(2, 256 * 2, 4096) == 2          # 256 fp16: no promotion needed
+    assert st.promote(2, 512 * 2, 4096) == 4          # 512 fp16 -> 256 four-byte elements
+    assert st.promote(2, 1024 * 2, 4096) == 8         # 1024 fp16 -> 256 eight-byte elements
+    assert st.promote(2, 2048 * 2, 8192) is None      # 512 eight-byte elements: declines
+    assert st.promote(4, 512 * 4, 4096) == 8
+    assert st.promote(1, 300, 600) == 2               # 1 -> 2 bytes: 150 elements
+    assert st.promote(2, 520 * 2, 1040 * 2) == 8      # 1040 B rows: 4 B gives 260, 8 B gives 130
+    assert st.promote(2, 514 * 2, 4112) is None       # 1028 B rows: 4 B gives 257, 8 B does not divide
+    assert st.promote(2, 512 * 2, 2 * 1025) is None   # the tensor row (2050 B) is no whole number of 4 B
+    for es in (1, 2, 4):
+        for n in range(1, 3000):
+            pes = st.promote(es, n * es, 4 * n * es)
+            if pes is not None:
+                assert pes in st.PROMOTION_CHAIN and pes >= es and (n * es) // pes <= 256
+                smaller = [q for q in st.PROMOTION_CHAIN if es <= q < pes and (n * es) % q == 0]
+                assert all((n * es) // q > 256 for q in smaller)
+
+
 def test_encode_args_rank3_demo_tuple():
     """TVM "copy_async -> tma", Generated TIRx IR: the 8x256 float16 tile
     with the 128-B swizzle is one rank-3 load with exactly this encode."""
