@@ -211,7 +211,7 @@ int encode_tensor_map(const Geometry& g, const void* ptr, CUtensorMap* map)
         strides[d] = m.strides[d];
     const CUresult r = fn(map, map_type(g), cuuint32_t(m.rank), const_cast<void*>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(m.swizzle),
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          static_cast<CUtensorMapL2promotion>(m.l2_promotion), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char buf[96];
         std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));

@@ -56,6 +56,9 @@ template <bool ACC>
 __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, uint32_t slot, int64_t t)
 {
     const TileBoxes b = tile_boxes(p, t);
+    // box x coordinates in tensor-map elements (wider when promoted)
+    const int x0 = b.col0 >> p.promote_shift;
+    const int dx = p.inner_elems >> p.promote_shift;
     for (int r = 0; r < b.chunks; ++r) {
         const int y = b.row0 + r * p.rows_per_load;
         if (p.rank3) {
@@ -67,7 +70,7 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
         } else {
             for (int a = 0; a < b.atoms; ++a) {
                 const uint32_t src = slot + (r * p.atoms + a) * p.load_smem_bytes;
-                const int x = (b.col0 + a * p.inner_elems) >> p.promote_shift;
+                const int x = x0 + a * dx;
                 if constexpr (ACC)
                     tma_reduce_add_2d(&maps.m[3], src, x, y);
                 else

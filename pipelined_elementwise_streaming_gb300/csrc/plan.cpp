@@ -198,6 +198,9 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
         g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
     }
     g->store_lag = default_store_lag(stages);
+    // tuning knob: the tensor maps' L2 promotion (the TVM page passes 128 B)
+    const int l2 = env_int("TSX_L2_PROMOTION", 2);
+    g->l2_promotion = l2 < 0 || l2 > 3 ? 2 : l2;
     return TSX_OK;
 }
 
@@ -281,7 +284,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
             info->global_stride_bytes[d] = m.strides[d];
         info->interleave = 0;                       // CU_TENSOR_MAP_INTERLEAVE_NONE
         info->swizzle = m.swizzle;
-        info->l2_promotion = 2;                     // CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+        info->l2_promotion = m.l2_promotion;        // CUtensorMapL2promotion value
         info->oob_fill = 0;                         // CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE: zeros
     }
 }
@@ -289,6 +292,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
 void tensor_map_args(const Geometry& g, TensorMapArgs* m)
 {
     *m = TensorMapArgs{};
+    m->l2_promotion = g.l2_promotion;
     m->swizzle = g.swizzle_bytes == 128 ? 3 : g.swizzle_bytes == 64 ? 2 : g.swizzle_bytes == 32 ? 1 : 0;
     // dims[0] is the innermost (contiguous) dimension
     const uint64_t rows = uint64_t(g.rows), cols = uint64_t(g.cols);

@@ -21,6 +21,7 @@ struct Geometry {
     int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
     int loads_per_operand = 0, bytes_per_load = 0, swizzle_bytes = 0;
     int tma_es = 0;          // element size the tensor map uses (> es when promoted)
+    int l2_promotion = 2;    // CUtensorMapL2promotion: 0 none, 1 64 B, 2 128 B, 3 256 B
     uint32_t load_smem_bytes = 0;
     // one operand's tile in shared memory
     uint32_t slot_bytes = 0;
@@ -41,6 +42,7 @@ struct OpGeometry {
 
 struct TensorMapArgs {
     int rank = 0;
+    int l2_promotion = 2;
     uint64_t dims[5] = {};
     uint64_t strides[4] = {};
     uint32_t box[5] = {};

@@ -49,6 +49,9 @@ __device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(NIN * b.chunks * b.atoms) * p.bytes_per_load);
     if (t == p.fault_tile)
         return;   // test hook: the announced bytes never arrive
+    // box x coordinates in tensor-map elements (wider when promoted)
+    const int x0 = b.col0 >> p.promote_shift;
+    const int dx = p.inner_elems >> p.promote_shift;
 #pragma unroll
     for (int j = 0; j < NIN; ++j) {
         const uint32_t slot = stage + j * p.slot_bytes;
@@ -58,8 +61,7 @@ __device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p
                 tma_load_3d(slot + r * p.load_smem_bytes, &maps.m[j], 0, y, b.col0 / p.inner_elems, bar);
             } else {
                 for (int a = 0; a < b.atoms; ++a)
-                    tma_load_2d(slot + (r * p.atoms + a) * p.load_smem_bytes, &maps.m[j],
-                                (b.col0 + a * p.inner_elems) >> p.promote_shift, y, bar);
+                    tma_load_2d(slot + (r * p.atoms + a) * p.load_smem_bytes, &maps.m[j], x0 + a * dx, y, bar);
             }
         }
     }
