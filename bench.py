@@ -61,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--variant", default=None, help="default: the workload's variant")
     p.add_argument("--box", type=int, nargs=2, default=None, metavar=("ROWS", "COLS"),
                    help="stage tile other than the workload's (row sums run one CTA per band of ROWS rows)")
+    p.add_argument("--op", default=None, choices=["copy", "sqrt", "exp", "add", "mul", "fma"],
+                   help="op other than the workload's (same shape, dtype and value distribution)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--mode", default="ewise", choices=["ewise", "accumulate", "rowsum"],
                    help="ewise: out = op(...); accumulate: out += op(...) by TMA reduce-store; "
@@ -544,6 +546,10 @@ def main(argv=None):
         from dataclasses import replace
 
         w = replace(w, box_rows=args.box[0], box_cols=args.box[1])
+    if args.op is not None:
+        from dataclasses import replace
+
+        w = replace(w, op=args.op)
     stages = args.stages if args.stages is not None else w.default_stages
     variant = args.variant or w.variant
     if args.impl == "reference":

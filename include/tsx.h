@@ -187,15 +187,20 @@ int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const vo
  * [rows, cols]; each op result is rounded into the element type, then summed
  * in fp32 (the reduction schedules of nvFuser PR #2833, "Testing Setup":
  * Reduction, InnerPersistent).  row_sums: device fp32 [rows], 4-byte
- * aligned, overwritten.  A persistent CTA owns whole row bands of box_rows
- * rows and streams their tiles through the plan's TMA ring, so at most
- * ceil(rows / box_rows) CTAs run: choose box_rows for enough bands.  The
- * order of additions depends on the plan alone, so results repeat bit for
- * bit; against the exact sum their error is at most gamma(cols - 1) *
- * sum |x|, gamma(k) = k u / (1 - k u), u = 2^-24.  TSX_TMA / TSX_TMA_RANK3
- * plans only (else TSX_ERR_UNSUPPORTED); TSX_ACCUMULATE is rejected.  rows =
- * 0 does nothing; cols = 0 writes zeros.  Asynchronous on `stream`;
- * device-side timeouts are reported as for tsx_ewise. */
+ * aligned, overwritten.  The persistent grid splits the tiles, in row-major
+ * order, into one contiguous range per CTA, so a band of box_rows rows may
+ * be cut between CTAs; the shares of a cut band go through scratch that the
+ * plan allocates on its first row reduction of an op (TSX_ERR_NOMEM if that
+ * fails) and owns until it is destroyed.  Row reductions of one plan must
+ * therefore not run concurrently on different streams.  The order of
+ * additions depends on the plan alone, so results repeat bit for bit;
+ * against the exact sum their error is at most gamma(cols - 1) * sum |x|,
+ * gamma(k) = k u / (1 - k u), u = 2^-24.  TSX_TMA / TSX_TMA_RANK3 plans only
+ * (else TSX_ERR_UNSUPPORTED); TSX_ACCUMULATE is rejected.  rows = 0 does
+ * nothing; cols = 0 writes zeros.  Asynchronous on `stream`; device-side
+ * timeouts are reported as for tsx_ewise, and results of the plan's row
+ * reductions are undefined from a timeout until tsx_plan_status has been
+ * read. */
 int tsx_reduce_rows(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, float *row_sums,
                     tsx_stream_t stream);
 

@@ -121,6 +121,7 @@ struct tsx_plan {
         OpGeometry og;
         int ctas_per_sm = 0;
         int grid = 0;
+        RowsumScratch scratch{};   // row sums only: shares of the bands cut between CTAs
     } ops[12],   // op + 6 * accumulate
         rowsum_ops[6];
 
@@ -291,6 +292,8 @@ int alignment_of(const void* ptr)
     return 1;
 }
 
+size_t arrival_bytes(const Geometry& g) { return size_t(g.tiles_r) * size_t(g.box_rows) * sizeof(uint32_t); }
+
 int read_status(tsx_plan* p, bool clear)
 {
     int h = 0;
@@ -301,6 +304,14 @@ int read_status(tsx_plan* p, bool clear)
         e = cudaMemset(p->d_status, 0, sizeof(int));
         if (e != cudaSuccess)
             return cuda_error(e, "clearing the status word");
+        // a row reduction that gave up may have left arrivals counted
+        for (auto& L : p->rowsum_ops) {
+            if (!L.scratch.arrivals)
+                continue;
+            e = cudaMemset(L.scratch.arrivals, 0, arrival_bytes(p->g));
+            if (e != cudaSuccess)
+                return cuda_error(e, "clearing the row arrivals");
+        }
     }
     return h;
 }
@@ -349,9 +360,28 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         if (p->ctas_per_sm_cap > 0 && blocks > p->ctas_per_sm_cap)
             blocks = p->ctas_per_sm_cap;
         L.ctas_per_sm = blocks;
-        // one CTA per row band at most: a band is never split between CTAs
+        // contiguous tile ranges, one per CTA; a band is cut between at most
+        // 1 + ceil((tiles_c - 1) / floor(T / G)) consecutive CTAs
         const int64_t slots = int64_t(p->sm_count) * blocks;
-        L.grid = int(p->g.tiles_r < slots ? p->g.tiles_r : slots);
+        const Geometry& g = p->g;
+        L.grid = int(g.tiles < slots ? g.tiles : slots);
+        const int64_t shortest = g.tiles / L.grid;
+        const int64_t pieces = 1 + (g.tiles_c - 1 + shortest - 1) / shortest;
+        if (pieces > 1) {
+            L.scratch.pieces = pieces;
+            cudaError_t e1 = cudaMalloc(&L.scratch.piece, size_t(g.tiles_r) * size_t(pieces) * g.box_rows * sizeof(float));
+            cudaError_t e2 = e1 == cudaSuccess ? cudaMalloc(&L.scratch.arrivals, arrival_bytes(g)) : e1;
+            cudaError_t e3 = e2 == cudaSuccess ? cudaMemset(L.scratch.arrivals, 0, arrival_bytes(g)) : e2;
+            if (e3 != cudaSuccess) {
+                cudaFree(L.scratch.piece);
+                cudaFree(L.scratch.arrivals);
+                L.scratch = RowsumScratch{};
+                (void)cudaGetLastError();
+                return set_error(e1 == cudaErrorMemoryAllocation || e2 == cudaErrorMemoryAllocation ? TSX_ERR_NOMEM
+                                                                                                      : TSX_ERR_CUDA,
+                                 "allocating the row reduction's scratch");
+            }
+        }
         L.ready = true;
     }
     *out = &L;
@@ -417,6 +447,10 @@ void tsx_plan_destroy(tsx_plan_t p)
         return;
     if (p->d_status)
         cudaFree(p->d_status);
+    for (auto& L : p->rowsum_ops) {
+        cudaFree(L.scratch.piece);
+        cudaFree(L.scratch.arrivals);
+    }
     delete p;
 }
 
@@ -598,7 +632,7 @@ int tsx_reduce_rows(tsx_plan_t p, tsx_op op, const void* a, const void* b, const
     TmaArgs args{};
     fill_tma_args(p, L->og, &args);
     cudaError_t e = launch_rowsum(g.dtype, op, L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args,
-                                  row_sums);
+                                  L->scratch, row_sums);
     if (e != cudaSuccess)
         return cuda_error(e, "kernel launch");
     if (p->checked) {

@@ -1,14 +1,15 @@
 // The row-reduction kernel: row_sums[r] = sum over c of op(a, b, c)[r, c].
 //
 // The schedule is the inner-persistent reduction of the nvFuser page
-// ("Testing Setup", Reduction and InnerPersistent): a persistent CTA owns
-// whole row bands (box_rows rows), and streams each band's tiles, left to
-// right, through the same S-stage TMA ring as the elementwise kernel, so a
-// row never needs a reduction across CTAs.
+// ("Testing Setup", Reduction and InnerPersistent): every tile of a row band
+// streams through the same S-stage TMA ring as the elementwise kernel and is
+// folded into per-row partials in shared memory.  The persistent grid splits
+// the tiles, taken in row-major order (band after band, left to right), into
+// G contiguous ranges of floor(T / G) or ceil(T / G) tiles: CTA c streams
+// tiles [c T / G, (c + 1) T / G), so the work is even however few the bands.
 //
-//   warp 0      the producer (as in the elementwise kernel): the CTA's k-th
-//               tile is tile (band(k), k mod tiles_c) of its k / tiles_c-th
-//               band; stage reuse waits on `empty`.
+//   warp 0      the producer (as in the elementwise kernel: one box per
+//               lane); stage reuse waits on `empty`.
 //   warps 1..   the compute warps.  Every tile of a plan lands in shared
 //               memory with the same layout, so the 16-byte unit u of a
 //               staged slot holds the same (row, column within the tile) in
@@ -16,17 +17,26 @@
 //               + threads, ...: it applies the op to the unit's vectors,
 //               rounds into the element type, adds the elements in order and
 //               adds that to the unit's fp32 partial in shared memory (set,
-//               on the band's first tile).  Only a band's last, ragged tile
-//               needs each unit's column, to leave out the columns past the
-//               tensor's end.  Every warp then releases the stage (`empty`,
-//               one arrival per warp).  After the band's last tile one
-//               thread per row adds the partials of the row's units, box by
-//               box in a fixed order, into the row's result.
+//               on the first tile of the CTA's share of a band).  Only a
+//               band's last, ragged tile needs each unit's column, to leave
+//               out the columns past the tensor's end.  Every warp then
+//               releases the stage (`empty`, one arrival per warp).  When
+//               the CTA's share of a band ends, one thread per row adds the
+//               partials of the row's units, box by box in a fixed order.
 //
-// The order of additions is fixed by the shapes alone, so results repeat
-// bit for bit from run to run.  Columns past the end of the tensor (zero
-// filled, or stale when a whole box lies outside) are skipped: the column
-// of a staged vector is found through the swizzle inverse.
+// A band the CTA streamed whole gets its row sums written directly.  A band
+// cut between CTAs c0 < ... < c1 (consecutive, since the ranges are) has
+// each share's row totals stored in the plan's scratch; the thread that
+// stores a row's share then counts an arrival on the row, and the one that
+// counts the last arrival adds the shares in CTA order into the result
+// (the fence-then-count pattern of the CUDA programming guide's memory
+// fence example).  No CTA waits on another.
+//
+// The order of additions is fixed by the shapes and the grid size, both
+// fixed per plan, so results repeat bit for bit from run to run.  Columns
+// past the end of the tensor (zero filled, or stale when a whole box lies
+// outside) are skipped: the column of a staged vector is found through the
+// swizzle inverse.
 
 #include "tsx_tma_common.cuh"
 
@@ -56,17 +66,15 @@ __device__ __forceinline__ void add_vec(float& part, const uint4& r)
     }
 }
 
-// The op on the staged vectors of unit u, its elements added in order.
+// The op on the staged vectors of unit u, its elements added in order to `part`.
 template <int DT, int OP>
-__device__ __forceinline__ float unit_sum(const TmaArgs& p, const uint4* S, uint32_t u)
+__device__ __forceinline__ void add_unit(float& part, const TmaArgs& p, const uint4* S, uint32_t u)
 {
     constexpr int NIN = op_arity(OP);
     const uint4 va = S[u];
     const uint4 vb = NIN > 1 ? S[p.slot_bytes / 16 + u] : va;
     const uint4 vc = NIN > 2 ? S[2 * (p.slot_bytes / 16) + u] : va;
-    float part = 0.f;
     add_vec<DT>(part, op_vec16<DT, OP>(va, vb, vc));
-    return part;
 }
 
 // Whether unit u of a staged slot holds columns inside the tensor (a ragged
@@ -112,11 +120,40 @@ __device__ __forceinline__ float row_total(const TmaArgs& p, const float* partia
     return v;
 }
 
+// Units of a staged slot whose partials a compute thread keeps in registers
+// (units tid, tid + threads, ...); any further units keep theirs in shared
+// memory.
+constexpr int kRegUnits = 8;
+
+// The CTA whose tile range holds tile x: the largest c with c T / G <= x.
+__device__ __forceinline__ int64_t range_owner(int64_t x, int64_t T, int64_t G)
+{
+    return ((x + 1) * G + T - 1) / T - 1;
+}
+
+// One row of a band cut between CTAs c0 .. c0 + shares - 1: store this
+// CTA's share v as share j (shares are box_rows floats apart), count it, and
+// if it is the row's last arrival add the shares in CTA order into *result.
+__device__ __forceinline__ void finish_cut_row(float* share_col, uint32_t* arrivals, int64_t box_rows, int64_t j,
+                                               uint32_t shares, float v, float* result)
+{
+    share_col[j * box_rows] = v;
+    __threadfence();
+    if (atomicInc(arrivals, shares - 1) == shares - 1) {
+        __threadfence();
+        float t = 0.f;
+        for (uint32_t k = 0; k < shares; ++k)
+            t += __ldcg(share_col + k * box_rows);
+        *result = t;
+    }
+}
+
 template <int DT, int OP>
 __global__ void __launch_bounds__(kMaxThreads)
-    tma_rowsum(const __grid_constant__ TmaMaps maps, const TmaArgs p, float* row_sums)
+    tma_rowsum(const __grid_constant__ TmaMaps maps, const TmaArgs p, const RowsumScratch sc, float* row_sums)
 {
     constexpr int NIN = op_arity(OP);
+    constexpr bool kAllLanes = true;   // how the producer warp waits (no exp exception here: measured)
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
@@ -134,10 +171,9 @@ __global__ void __launch_bounds__(kMaxThreads)
     const int compute_warps = blockDim.x / 32 - 1;
     const int64_t G = gridDim.x;
     const int64_t cta = blockIdx.x;
-    const int64_t bands = cta < p.tiles_r ? (p.tiles_r - 1 - cta) / G + 1 : 0;
-    const int64_t N = bands * p.tiles_c;
-    // the CTA's k-th tile: column tile k mod tiles_c of its (k / tiles_c)-th band
-    auto tile_of = [&](int64_t k) { return (cta + (k / p.tiles_c) * G) * p.tiles_c + k % p.tiles_c; };
+    // the CTA's tiles: lo, lo + 1, ..., lo + N - 1
+    const int64_t lo = cta * p.tiles / G;
+    const int64_t N = (cta + 1) * p.tiles / G - lo;
     const bool elected = warp == 0 && elect_one();
 
     // Pre-prologue.
@@ -157,33 +193,44 @@ __global__ void __launch_bounds__(kMaxThreads)
 
     if (warp == 0) {
         // ---------------------------------------------------- producer
-        if (elected) {
-            int64_t issued = 0;
-            const int64_t pro = N < S - 1 ? N : S - 1;
-            for (; issued < pro; ++issued)
-                issue_tile<NIN>(maps, p, base + (issued % S) * p.stage_bytes, full + 8u * (issued % S),
-                                tile_of(issued));
-            for (; issued < N; ++issued) {
-                const int64_t k = issued;
-                const uint32_t s = static_cast<uint32_t>(k % S);
-                if (k >= S && !wait_or_abort(empty + 8u * s, static_cast<uint32_t>((k / S - 1) & 1), p, abort_flag))
-                    break;
-                issue_tile<NIN>(maps, p, base + s * p.stage_bytes, full + 8u * s, tile_of(k));
-            }
-            if (*abort_flag) {
-                const int64_t first = issued > S ? issued - S : 0;
-                for (int64_t k = first; k < issued; ++k)
-                    (void)mbar_wait(full + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
-            }
+        const int lane = static_cast<int>(threadIdx.x & 31);
+        const int n_loads = NIN * (p.rank3 ? p.row_chunks : p.row_chunks * p.atoms);
+        const BoxRef mine = box_ref(maps, p, lane < n_loads ? lane : 0, 0);
+        TileCursor tc(p, lo, 1);
+        StageCursor st;
+        int64_t issued = 0;
+        const int64_t pro = N < S - 1 ? N : S - 1;
+        for (; issued < pro; ++issued) {
+            issue_tile_lanes<NIN>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+            tc.next(p);
+            st.next(S);
+        }
+        for (; issued < N; ++issued) {
+            if (issued >= S && !role_wait<kAllLanes>(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag))
+                break;
+            issue_tile_lanes<NIN>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+            tc.next(p);
+            st.next(S);
+        }
+        if (*abort_flag && lane == 0) {
+            const int64_t first = issued > S ? issued - S : 0;
+            for (int64_t k = first; k < issued; ++k)
+                (void)mbar_wait(full + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
         }
     } else {
         // ---------------------------------------------- compute warps
         const uint32_t tid = threadIdx.x - 32;
         const uint32_t threads = blockDim.x - 32;
         // stage, phase, band and column tile advance with the tile counter
-        // (no divisions in the loop)
+        // (no divisions in the loop); first_ct opens the CTA's share of the band
         uint32_t s = 0, phase = 0, band_parity = 0;
-        int64_t band = cta, ct = 0;
+        // the thread's first kRegUnits units: partials in registers
+        float acc[kRegUnits];
+#pragma unroll
+        for (int k = 0; k < kRegUnits; ++k)
+            acc[k] = 0.f;
+        int64_t band = lo / p.tiles_c;
+        int64_t ct = lo - band * p.tiles_c, first_ct = ct;
         for (int64_t i = 0; i < N; ++i) {
             if (!wait_or_abort(full + 8u * s, phase, p, abort_flag))
                 break;
@@ -194,28 +241,70 @@ __global__ void __launch_bounds__(kMaxThreads)
             tb.atoms = p.atoms;
             const bool ragged = tb.col0 + p.box_cols > p.cols;
             const uint4* stage = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
-            if (ct == 0) {
-                for (uint32_t u = tid; u < p.vec16_per_slot; u += threads)
-                    partial[u] = ragged && !unit_in_columns<DT>(p, tb, u) ? 0.f : unit_sum<DT, OP>(p, stage, u);
+            if (!ragged) {
+#pragma unroll
+                for (int k = 0; k < kRegUnits; ++k) {
+                    const uint32_t u = tid + k * threads;
+                    if (u >= p.vec16_per_slot)
+                        break;
+                    add_unit<DT, OP>(acc[k], p, stage, u);
+                }
             } else {
-                for (uint32_t u = tid; u < p.vec16_per_slot; u += threads)
-                    partial[u] += ragged && !unit_in_columns<DT>(p, tb, u) ? 0.f : unit_sum<DT, OP>(p, stage, u);
+#pragma unroll
+                for (int k = 0; k < kRegUnits; ++k) {
+                    const uint32_t u = tid + k * threads;
+                    if (u >= p.vec16_per_slot)
+                        break;
+                    if (unit_in_columns<DT>(p, tb, u))
+                        add_unit<DT, OP>(acc[k], p, stage, u);
+                }
+            }
+            // units past the register partials keep theirs in shared memory
+            for (uint32_t u = tid + kRegUnits * threads; u < p.vec16_per_slot; u += threads) {
+                float part = ct == first_ct ? 0.f : partial[u];
+                if (!ragged || unit_in_columns<DT>(p, tb, u))
+                    add_unit<DT, OP>(part, p, stage, u);
+                partial[u] = part;
             }
             __syncwarp();
             if ((threadIdx.x & 31) == 0)
                 mbar_arrive(empty + 8u * s);
-            if (ct == p.tiles_c - 1) {
-                // the band is complete once every compute warp has added its
-                // last partials; then each row's partials, box by box
+            if (ct == p.tiles_c - 1 || i == N - 1) {
+                // the CTA's share of the band is complete once every compute
+                // warp has added its last partials; then each row's partials,
+                // box by box
+#pragma unroll
+                for (int k = 0; k < kRegUnits; ++k) {
+                    const uint32_t u = tid + k * threads;
+                    if (u >= p.vec16_per_slot)
+                        break;
+                    partial[u] = acc[k];
+                    acc[k] = 0.f;
+                }
+                __syncwarp();
                 if ((threadIdx.x & 31) == 0)
                     mbar_arrive(band_done);
                 if (!wait_or_abort(band_done, band_parity, p, abort_flag))
                     break;
-                for (uint32_t r = tid; r < static_cast<uint32_t>(p.box_rows); r += threads) {
-                    const int64_t row = tb.row0 + r;
-                    if (row >= p.rows)
-                        break;
-                    row_sums[row] = row_total<DT>(p, partial, static_cast<int>(r));
+                if (first_ct == 0 && ct == p.tiles_c - 1) {
+                    for (uint32_t r = tid; r < static_cast<uint32_t>(p.box_rows); r += threads) {
+                        const int64_t row = tb.row0 + r;
+                        if (row >= p.rows)
+                            break;
+                        row_sums[row] = row_total<DT>(p, partial, static_cast<int>(r));
+                    }
+                } else {
+                    const int64_t x0 = band * p.tiles_c;
+                    const int64_t c0 = range_owner(x0, p.tiles, G);
+                    const uint32_t shares = static_cast<uint32_t>(range_owner(x0 + p.tiles_c - 1, p.tiles, G) - c0 + 1);
+                    for (uint32_t r = tid; r < static_cast<uint32_t>(p.box_rows); r += threads) {
+                        const int64_t row = tb.row0 + r;
+                        if (row >= p.rows)
+                            break;
+                        finish_cut_row(sc.piece + band * sc.pieces * p.box_rows + r, sc.arrivals + row,
+                                       p.box_rows, cta - c0, shares, row_total<DT>(p, partial, static_cast<int>(r)),
+                                       row_sums + row);
+                    }
                 }
                 // before the next band overwrites the partials
                 __syncwarp();
@@ -224,8 +313,9 @@ __global__ void __launch_bounds__(kMaxThreads)
                 if (!wait_or_abort(band_free, band_parity, p, abort_flag))
                     break;
                 band_parity ^= 1;
-                band += G;
+                ++band;
                 ct = 0;
+                first_ct = 0;
             } else {
                 ++ct;
             }
@@ -259,13 +349,15 @@ const void* const kKernels[3][6] = {TSX_ROW(TSX_F16), TSX_ROW(TSX_BF16), TSX_ROW
 const void* rowsum_kernel(int dtype, int op) { return kKernels[dtype][op]; }
 
 cudaError_t launch_rowsum(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
-                          const CUtensorMap* maps, const TmaArgs& args, float* row_sums)
+                          const CUtensorMap* maps, const TmaArgs& args, const RowsumScratch& scratch,
+                          float* row_sums)
 {
     TmaMaps m;
     for (int j = 0; j < 4; ++j)
         m.m[j] = maps[j];
     TmaArgs a = args;
-    void* params[] = {&m, &a, &row_sums};
+    RowsumScratch sc = scratch;
+    void* params[] = {&m, &a, &sc, &row_sums};
     return cudaLaunchKernel(kKernels[dtype][op], dim3(grid), dim3(threads), params, smem, stream);
 }
 

@@ -4,17 +4,18 @@
 // order) and streams them through S stage buffers in shared memory.  The
 // warps of a CTA have three roles:
 //
-//   warp 0      the producer: its elected lane arrives once on the stage's
-//               `full` mbarrier with expect_tx = the bytes of the stage's
-//               loads, then issues the cp.async.bulk.tensor loads; the TMA
-//               unit completes the phase when the bytes have landed (TVM docs
-//               "copy_async -> tma", "Demonstration program"; nvFuser PR
-//               #2833 "Add TMA support for circular buffering pass",
-//               "Lowering Details").
-//   warp 1      the store warp: its elected lane waits until the tile is
-//               computed, issues the TMA store from the stage, and hands the
-//               stage back to the producer (`empty`) once the store has
-//               finished reading shared memory.
+//   warp 0      the producer: lane 0 arrives once on the stage's `full`
+//               mbarrier with expect_tx = the bytes of the stage's loads,
+//               then every lane issues its share of the cp.async.bulk.tensor
+//               loads (one box per lane; the pages issue them from one
+//               thread); the TMA unit completes the phase when the bytes
+//               have landed (TVM docs "copy_async -> tma", "Demonstration
+//               program"; nvFuser PR #2833 "Add TMA support for circular
+//               buffering pass", "Lowering Details").
+//   warp 1      the store warp: waits until the tile is computed, each lane
+//               issues its share of the TMA stores from the stage, and lane
+//               0 hands the stage back to the producer (`empty`) once every
+//               lane's stores have finished reading shared memory.
 //   warps 2..   the compute warps: wait on `full` (parity (i / S) mod 2 for
 //               their i-th tile), apply the op to 16-byte vectors (f *
 //               threads + tid) of each operand's slot, write the result over
@@ -50,32 +51,35 @@ namespace {
 
 using namespace dev;
 
-// TMA store of tile t from the slot at shared address `slot`; with ACC a
-// reduce-store that adds the tile into global memory.
+// The store warp's TMA stores of one tile from the slot at shared address
+// `slot`: each lane stores the boxes numbered lane, lane + 32, ... (`mine`
+// is the lane's first, n_boxes those of a full tile) and commits them as one
+// bulk group of its own; with ACC a reduce-store that adds the tile into
+// global memory.
 template <bool ACC>
-__device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, uint32_t slot, int64_t t)
+__device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc,
+                                           const BoxRef& mine, int n_boxes, uint32_t slot)
 {
-    const TileBoxes b = tile_boxes(p, t);
-    // box x coordinates in tensor-map elements (wider when promoted)
-    const int x0 = b.col0 >> p.promote_shift;
-    const int dx = p.inner_elems >> p.promote_shift;
-    for (int r = 0; r < b.chunks; ++r) {
-        const int y = b.row0 + r * p.rows_per_load;
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const TileBoxes b = boxes_at(p, tc.band, tc.ct);
+    for (int L = lane; L < n_boxes; L += 32) {
+        const BoxRef x = L == lane ? mine : box_ref(maps, p, L, 3);
+        if (!box_in(x, b))
+            continue;
+        const uint32_t src = slot + x.off;
+        const int y = b.row0 + x.dy;
         if (p.rank3) {
-            const uint32_t src = slot + r * p.load_smem_bytes;
+            const int z = static_cast<int>(tc.ct * p.atoms);
             if constexpr (ACC)
-                tma_reduce_add_3d(&maps.m[3], src, 0, y, b.col0 / p.inner_elems);
+                tma_reduce_add_3d(x.map, src, 0, y, z);
             else
-                tma_store_3d(&maps.m[3], src, 0, y, b.col0 / p.inner_elems);
+                tma_store_3d(x.map, src, 0, y, z);
         } else {
-            for (int a = 0; a < b.atoms; ++a) {
-                const uint32_t src = slot + (r * p.atoms + a) * p.load_smem_bytes;
-                const int x = x0 + a * dx;
-                if constexpr (ACC)
-                    tma_reduce_add_2d(&maps.m[3], src, x, y);
-                else
-                    tma_store_2d(&maps.m[3], src, x, y);
-            }
+            const int xc = (b.col0 >> p.promote_shift) + x.dx;
+            if constexpr (ACC)
+                tma_reduce_add_2d(x.map, src, xc, y);
+            else
+                tma_store_2d(x.map, src, xc, y);
         }
     }
     bulk_commit();
@@ -115,6 +119,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     constexpr int NIN = op_arity(OP);
     // operands in the stage: all of them, or all but b in the mixed variant
     constexpr int NT = MIXED ? tma_operands(TSX_TMA_MIXED, OP) : NIN;
+    constexpr bool kAllLanes = OP != TSX_EXP;   // how the producer and store warps wait
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
@@ -148,59 +153,71 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         prefetch_tensormap(&maps.m[3]);
     __syncthreads();
 
+    const int lane = static_cast<int>(threadIdx.x & 31);
     if (warp == 0) {
         // ---------------------------------------------------- producer
-        if (elected) {
-            int64_t issued = 0;
-            const int64_t pro = N < S - 1 ? N : S - 1;
-            // Prologue: the first S - 1 tiles, into stages that start empty.
-            for (; issued < pro; ++issued)
-                issue_tile<NT>(maps, p, base + (issued % S) * p.stage_bytes, full + 8u * (issued % S),
-                                cta + issued * G);
-            // Main loop: tile k = i + S - 1 into stage k mod S, once the
-            // store warp has released that stage's previous tile (k - S).
-            for (; issued < N; ++issued) {
-                const int64_t k = issued;
-                const uint32_t s = static_cast<uint32_t>(k % S);
-                if (k >= S && !wait_or_abort(empty + 8u * s, static_cast<uint32_t>((k / S - 1) & 1), p, abort_flag))
-                    break;
-                issue_tile<NT>(maps, p, base + s * p.stage_bytes, full + 8u * s, cta + k * G);
-            }
-            if (*abort_flag) {
-                // let the loads still in flight land before shared memory goes away
-                const int64_t first = issued > S ? issued - S : 0;
-                for (int64_t k = first; k < issued; ++k)
-                    (void)mbar_wait(full + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
-            }
+        const int n_loads = NT * (p.rank3 ? p.row_chunks : p.row_chunks * p.atoms);
+        const BoxRef mine = box_ref(maps, p, lane < n_loads ? lane : 0, 0);
+        TileCursor tc(p, cta, G);
+        StageCursor st;
+        int64_t issued = 0;
+        const int64_t pro = N < S - 1 ? N : S - 1;
+        // Prologue: the first S - 1 tiles, into stages that start empty.
+        for (; issued < pro; ++issued) {
+            issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+            tc.next(p);
+            st.next(S);
+        }
+        // Main loop: tile k = i + S - 1 into stage k mod S, once the store
+        // warp has released that stage's previous tile (k - S).
+        for (; issued < N; ++issued) {
+            if (issued >= S && !role_wait<kAllLanes>(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag))
+                break;
+            issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+            tc.next(p);
+            st.next(S);
+        }
+        if (*abort_flag && lane == 0) {
+            // let the loads still in flight land before shared memory goes away
+            const int64_t first = issued > S ? issued - S : 0;
+            for (int64_t k = first; k < issued; ++k)
+                (void)mbar_wait(full + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------- store warp
-        if (elected) {
-            const int lag = p.store_lag < S - 1 ? p.store_lag : S - 1;
-            for (int64_t i = 0; i < N; ++i) {
-                const uint32_t s = static_cast<uint32_t>(i % S);
-                const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
-                // copy has no compute step: the loaded tile goes straight back
-                const uint32_t ready = OP == TSX_COPY ? full : computed;
-                if (!wait_or_abort(ready + 8u * s, parity, p, abort_flag))
-                    break;
-                store_tile<ACC>(maps, p, base + s * p.stage_bytes, cta + i * G);
-                // release tile i - lag once its store has read shared memory
-                bulk_wait_read(lag);
-                if (i >= lag)
-                    mbar_arrive(empty + 8u * static_cast<uint32_t>((i - lag) % S));
+        const int n_boxes = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
+        const BoxRef mine = box_ref(maps, p, lane < n_boxes ? lane : 0, 3);
+        const int lag = p.store_lag < S - 1 ? p.store_lag : S - 1;
+        TileCursor tc(p, cta, G);
+        StageCursor st, released;   // tile i and tile i - lag
+        for (int64_t i = 0; i < N; ++i) {
+            // copy has no compute step: the loaded tile goes straight back
+            const uint32_t ready = OP == TSX_COPY ? full : computed;
+            if (!role_wait<kAllLanes>(ready + 8u * st.s, st.phase, p, abort_flag))
+                break;
+            store_tile<ACC>(maps, p, tc, mine, n_boxes, base + st.s * p.stage_bytes);
+            // release tile i - lag once every lane's stores of it have read
+            // shared memory
+            bulk_wait_read(lag);
+            __syncwarp();
+            if (i >= lag) {
+                if (lane == 0)
+                    mbar_arrive(empty + 8u * released.s);
+                released.next(S);
             }
-            bulk_wait_all();
+            tc.next(p);
+            st.next(S);
         }
+        bulk_wait_all();
     } else if (OP != TSX_COPY) {
         // ---------------------------------------------- compute warps
         const uint32_t tid = threadIdx.x - 64;
         const uint32_t threads = blockDim.x - 64;
+        StageCursor st;
         for (int64_t i = 0; i < N; ++i) {
-            const uint32_t s = static_cast<uint32_t>(i % S);
-            if (!wait_or_abort(full + 8u * s, static_cast<uint32_t>((i / S) & 1), p, abort_flag))
+            if (!wait_or_abort(full + 8u * st.s, st.phase, p, abort_flag))
                 break;
-            uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes);
+            uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(st.s) * p.stage_bytes);
             if constexpr (MIXED && NIN >= 2) {
                 compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, cta + i * G, tid, threads);
             } else {
@@ -217,7 +234,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             fence_proxy_async_smem();
             __syncwarp();
             if ((threadIdx.x & 31) == 0)
-                mbar_arrive(computed + 8u * s);
+                mbar_arrive(computed + 8u * st.s);
+            st.next(S);
         }
     }
 

@@ -235,7 +235,9 @@ __device__ __forceinline__ uint32_t f32_as_u32(float x) { return __float_as_uint
 // element type the result is within 1 ulp of exp(x).
 __device__ __forceinline__ float exp_for_16bit(float x) { return __expf(x); }
 
-// Two 16-bit elements packed in 32 bits (low half first).
+// Two 16-bit elements packed in 32 bits (low half first).  fma and sqrt use
+// the native 16-bit instructions (one rounding of the exact result); the
+// other ops evaluate in fp32 and round once into the element type.
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
 {
@@ -245,6 +247,8 @@ __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
         if constexpr (OP == TSX_FMA) {
             // one rounding of the exact a * b + c into fp16
             r = __hfma2(ha, *reinterpret_cast<const __half2*>(&b), *reinterpret_cast<const __half2*>(&c));
+        } else if constexpr (OP == TSX_SQRT) {
+            r = h2sqrt(ha);   // documented round-to-nearest-even
         } else {
             const float2 fa = __half22float2(ha);
             float2 fb = make_float2(0.f, 0.f);
@@ -262,6 +266,8 @@ __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
         if constexpr (OP == TSX_FMA) {
             r = __hfma2(ha, *reinterpret_cast<const __nv_bfloat162*>(&b),
                         *reinterpret_cast<const __nv_bfloat162*>(&c));
+        } else if constexpr (OP == TSX_SQRT) {
+            r = h2sqrt(ha);   // documented round-to-nearest-even
         } else {
             const float2 fa = __bfloat1622float2(ha);
             float2 fb = make_float2(0.f, 0.f);

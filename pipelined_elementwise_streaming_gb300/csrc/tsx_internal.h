@@ -104,9 +104,19 @@ inline bool split_op(int op_arg, int* op, bool* accumulate)
     return *op >= TSX_COPY && *op <= TSX_FMA;
 }
 // The row-reduction kernel (k_rowsum.cu): TMA ring, rows summed in fp32.
+// CTA c of G streams tiles [c T / G, (c + 1) T / G) in row-major order, so a
+// row band may be cut between consecutive CTAs.  Each CTA's share of a cut
+// band is written to `piece` and the last CTA to count a row in `arrivals`
+// adds the row's shares in CTA order.
+struct RowsumScratch {
+    float* piece;           // [tiles_r][pieces][box_rows] row totals of each CTA's share of a band
+    uint32_t* arrivals;     // [tiles_r * box_rows] arrivals per row; zero between launches
+    int64_t pieces;         // most CTAs that one band can be cut between
+};
 const void* rowsum_kernel(int dtype, int op);
 cudaError_t launch_rowsum(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
-                          const CUtensorMap* maps, const TmaArgs& args, float* row_sums);
+                          const CUtensorMap* maps, const TmaArgs& args, const RowsumScratch& scratch,
+                          float* row_sums);
 const void* ldgsts_kernel(int dtype, int op);
 cudaError_t launch_ldgsts(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
                           const void* a, const void* b, const void* c, void* out, const CopyArgs& args);

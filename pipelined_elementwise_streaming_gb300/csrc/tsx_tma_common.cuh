@@ -1,7 +1,8 @@
 // Pieces of the TMA circular-buffer kernels shared by the elementwise
 // kernel (k_tma.cu) and the row-reduction kernel (k_rowsum.cu): the tensor
-// maps, which boxes of a tile touch the tensor, the producer's issue of a
-// tile, the swizzle inverse and the bounded mbarrier wait.
+// maps, which boxes of a tile touch the tensor, cursors over tiles and
+// stages, the producer warp's issue of a tile, the swizzle inverse and the
+// bounded mbarrier wait.
 #pragma once
 
 #include "tsx_device.cuh"
@@ -23,49 +24,133 @@ struct TileBoxes {
     int atoms;    // innermost boxes with at least one column inside (1 for rank 3)
 };
 
-__device__ __forceinline__ TileBoxes tile_boxes(const TmaArgs& p, int64_t t)
+// The boxes of the tile in row band `band`, column tile `ct`.  Only an edge
+// tile needs the divisions.
+__device__ __forceinline__ TileBoxes boxes_at(const TmaArgs& p, int64_t band, int64_t ct)
 {
     TileBoxes b;
-    b.row0 = static_cast<int>((t / p.tiles_c) * p.box_rows);
-    b.col0 = static_cast<int>((t % p.tiles_c) * p.box_cols);
-    const int chunks_in = (p.rows - b.row0 + p.rows_per_load - 1) / p.rows_per_load;
-    b.chunks = chunks_in < p.row_chunks ? chunks_in : p.row_chunks;
-    if (p.rank3) {
-        b.atoms = 1;
-    } else {
+    b.row0 = static_cast<int>(band * p.box_rows);
+    b.col0 = static_cast<int>(ct * p.box_cols);
+    b.chunks = p.row_chunks;
+    b.atoms = p.rank3 ? 1 : p.atoms;
+    if (b.row0 + p.box_rows > p.rows) {
+        const int chunks_in = (p.rows - b.row0 + p.rows_per_load - 1) / p.rows_per_load;
+        b.chunks = chunks_in < b.chunks ? chunks_in : b.chunks;
+    }
+    if (!p.rank3 && b.col0 + p.box_cols > p.cols) {
         const int atoms_in = (p.cols - b.col0 + p.inner_elems - 1) / p.inner_elems;
-        b.atoms = atoms_in < p.atoms ? atoms_in : p.atoms;
+        b.atoms = atoms_in < b.atoms ? atoms_in : b.atoms;
     }
     return b;
 }
 
-// expect_tx (the bytes of every load this tile issues), then the loads of
-// tile t into the stage at shared address `stage`.
-template <int NIN>
-__device__ __forceinline__ void issue_tile(const TmaMaps& maps, const TmaArgs& p, uint32_t stage, uint32_t bar,
-                                           int64_t t)
+__device__ __forceinline__ TileBoxes tile_boxes(const TmaArgs& p, int64_t t)
 {
-    const TileBoxes b = tile_boxes(p, t);
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(NIN * b.chunks * b.atoms) * p.bytes_per_load);
-    if (t == p.fault_tile)
-        return;   // test hook: the announced bytes never arrive
-    // box x coordinates in tensor-map elements (wider when promoted)
-    const int x0 = b.col0 >> p.promote_shift;
-    const int dx = p.inner_elems >> p.promote_shift;
-#pragma unroll
-    for (int j = 0; j < NIN; ++j) {
-        const uint32_t slot = stage + j * p.slot_bytes;
-        for (int r = 0; r < b.chunks; ++r) {
-            const int y = b.row0 + r * p.rows_per_load;
-            if (p.rank3) {
-                tma_load_3d(slot + r * p.load_smem_bytes, &maps.m[j], 0, y, b.col0 / p.inner_elems, bar);
-            } else {
-                for (int a = 0; a < b.atoms; ++a)
-                    tma_load_2d(slot + (r * p.atoms + a) * p.load_smem_bytes, &maps.m[j], x0 + a * dx, y, bar);
-            }
+    const int64_t band = t / p.tiles_c;
+    return boxes_at(p, band, t - band * p.tiles_c);
+}
+
+// Walks the tiles t0, t0 + step, t0 + 2 step, ... in (row band, column tile)
+// form without a division per step.
+struct TileCursor {
+    int64_t band, ct, step_r, step_c;
+    __device__ __forceinline__ TileCursor(const TmaArgs& p, int64_t t0, int64_t step)
+    {
+        band = t0 / p.tiles_c;
+        ct = t0 - band * p.tiles_c;
+        step_r = step / p.tiles_c;
+        step_c = step - step_r * p.tiles_c;
+    }
+    __device__ __forceinline__ void next(const TmaArgs& p)
+    {
+        ct += step_c;
+        band += step_r;
+        if (ct >= p.tiles_c) {
+            ct -= p.tiles_c;
+            ++band;
         }
     }
+    __device__ __forceinline__ int64_t tile(const TmaArgs& p) const { return band * p.tiles_c + ct; }
+};
+
+// Stage s = k mod S and parity (k / S) mod 2 of a tile counter k.
+struct StageCursor {
+    uint32_t s = 0, phase = 0;
+    __device__ __forceinline__ void next(int S)
+    {
+        if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+// One box of a full tile's TMA loads (operand slot j) or stores: where it
+// sits in the stage, its tensor map and its coordinate offsets from the
+// tile's origin.  Boxes are numbered operand by operand, row chunk by row
+// chunk, atom by atom, as they sit in the stage.
+struct BoxRef {
+    const CUtensorMap* map;
+    uint32_t off;   // bytes from the start of the stage
+    int r, a;       // row chunk, atom (0 for rank 3)
+    int dx, dy;     // coordinate offsets (x in tensor-map elements)
+};
+
+__device__ __forceinline__ BoxRef box_ref(const TmaMaps& maps, const TmaArgs& p, int L, int first_map)
+{
+    const int per_op = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
+    const int j = L / per_op;
+    const int rem = L - j * per_op;
+    BoxRef x;
+    x.map = &maps.m[first_map + j];
+    x.off = static_cast<uint32_t>(j) * p.slot_bytes + static_cast<uint32_t>(rem) * p.load_smem_bytes;
+    x.r = p.rank3 ? rem : rem / p.atoms;
+    x.a = p.rank3 ? 0 : rem - x.r * p.atoms;
+    x.dx = x.a * (p.inner_elems >> p.promote_shift);
+    x.dy = x.r * p.rows_per_load;
+    return x;
 }
+
+// Whether box x of a full tile touches the tensor in a tile with boxes b.
+__device__ __forceinline__ bool box_in(const BoxRef& x, const TileBoxes& b) { return x.r < b.chunks && x.a < b.atoms; }
+
+// Load box x of the tile at origin b (column tile ct) into the stage at
+// shared address `stage`, completing on `bar`.
+__device__ __forceinline__ void load_box(const TmaArgs& p, const BoxRef& x, const TileBoxes& b, int64_t ct,
+                                         uint32_t stage, uint32_t bar)
+{
+    const int y = b.row0 + x.dy;
+    if (p.rank3)
+        tma_load_3d(stage + x.off, x.map, 0, y, static_cast<int>(ct * p.atoms), bar);
+    else
+        tma_load_2d(stage + x.off, x.map, (b.col0 >> p.promote_shift) + x.dx, y, bar);
+}
+
+// The producer warp's issue of one tile: lane 0 arrives on `bar` with
+// expect_tx = the bytes of every load the tile issues, then each lane issues
+// the loads numbered lane, lane + 32, ... (`mine` is the lane's first one,
+// precomputed; n_loads those of a full tile).  The loads of one tile go out
+// from one warp instruction rather than one thread's loop.
+template <int NIN>
+__device__ __forceinline__ void issue_tile_lanes(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc,
+                                                 const BoxRef& mine, int n_loads, uint32_t stage, uint32_t bar)
+{
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const TileBoxes b = boxes_at(p, tc.band, tc.ct);
+    if (lane == 0)
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(NIN * b.chunks * b.atoms) * p.bytes_per_load);
+    __syncwarp();
+    if (tc.tile(p) == p.fault_tile)
+        return;   // test hook: the announced bytes never arrive
+    if (lane < n_loads && box_in(mine, b))
+        load_box(p, mine, b, tc.ct, stage, bar);
+    for (int L = lane + 32; L < n_loads; L += 32) {
+        const BoxRef x = box_ref(maps, p, L, 0);
+        if (box_in(x, b))
+            load_box(p, x, b, tc.ct, stage, bar);
+    }
+}
+
 
 // Offset inside one TMA box in shared memory -> offset in the box's
 // row-major image.  The 128-, 64- and 32-byte swizzles exchange the 16-byte
@@ -85,7 +170,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 16; ++k)
+            if (mbar_try_wait(bar, parity))
+                return true;
         if (*abort_flag)
             return false;
         if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -94,7 +183,25 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
             return false;
         }
     }
-    return true;
+}
+
+// A wait of the producer or store warp, with one answer for the whole warp.
+// ALL_LANES: every lane waits on the barrier itself; otherwise lane 0 waits
+// and the others take its answer.  Which is faster depends on the compute
+// stage beside it: every op streams faster with all lanes waiting except
+// exp, whose fp32 evaluation streams faster with lane 0 alone waiting
+// (measured on GB300 for both 16-bit and fp32 tensors).
+template <bool ALL_LANES>
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, const TmaArgs& p, volatile int* abort_flag)
+{
+    if constexpr (ALL_LANES) {
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
+    } else {
+        bool ok = true;
+        if ((threadIdx.x & 31) == 0)
+            ok = wait_or_abort(bar, parity, p, abort_flag);
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
 }
 
 }  // namespace dev

@@ -1,8 +1,8 @@
 """Row sums over staged tiles (tsx_reduce_rows) against the oracle: within
 the summation bound gamma(cols - 1) * sum |x| of the exact sum (plus the exp
-bound where the terms themselves carry it), exact for integer-valued rows,
-repeatable bit for bit, and blind to the zero-filled columns of ragged
-tiles."""
+bound where the terms themselves carry it), exact for integer-valued rows
+(also when bands are cut between CTAs), repeatable bit for bit, and blind to
+the zero-filled columns of ragged tiles."""
 
 import zlib
 
@@ -91,6 +91,39 @@ def test_rowsum_integer_rows_are_exact(tsx):
     for box, stages in (((8, 128), 3), ((16, 64), 2), ((1, 256), 4)):
         got = _rowsum(tsx, "f32", rows, cols, box, stages, "tma", "copy", [a.view(np.uint32)])
         assert np.array_equal(got, a.astype(np.float64).sum(axis=1)), box
+
+
+@pytest.mark.parametrize("rows,cols,box,ctas_per_sm", [
+    (3, 65536, (1, 256), 0),       # 768 tiles: each band cut between about 256 CTAs
+    (300, 4096, (1, 256), 0),      # 4800 tiles: ranges of several tiles end mid-band
+    (300, 4096, (1, 256), 1),      # the same with one CTA per SM: other cut points
+    (37, 5000, (8, 64), 2),        # ragged rows and columns, 8-row bands cut
+    (1, 1 << 20, (1, 512), 0),     # one row over every CTA
+])
+def test_rowsum_bands_cut_between_ctas_are_exact(tsx, monkeypatch, rows, cols, box, ctas_per_sm):
+    """Integer-valued rows, so any lost or doubled share shows: the tile
+    ranges of consecutive CTAs cut bands at many points, and the shares of a
+    cut band are combined by its last arriving CTA."""
+    if ctas_per_sm:
+        monkeypatch.setenv("TSX_CTAS_PER_SM", str(ctas_per_sm))
+    rng = np.random.default_rng(rows * 7 + cols)
+    a = rng.integers(-64, 64, (rows, cols)).astype(np.float32)
+    want = a.astype(np.float64).sum(axis=1)
+    for stages in (2, 4):
+        got = _rowsum(tsx, "f32", rows, cols, box, stages, "tma", "copy", [a.view(np.uint32)])
+        assert np.array_equal(got, want), (box, stages, np.nonzero(got != want)[0][:5])
+
+
+def test_rowsum_cut_bands_repeat_bit_for_bit(tsx):
+    rows, cols = 5, 300000
+    a = _values("f16", (rows, cols), 8)
+    with tsx.Plan("f16", rows, cols, box=(1, 256), stages=3) as plan:
+        da = to_dev(a, "f16")
+        runs = [plan.reduce_rows("exp", da).cpu().numpy().view(np.uint32) for _ in range(4)]
+        assert plan.status() == tsx.TSX_OK
+    for r in runs[1:]:
+        assert np.array_equal(runs[0], r)
+    _check(runs[0].view(np.float32).astype(np.float64), "exp", "f16", [a], cols, "cut bands")
 
 
 def test_rowsum_ignores_the_padding_of_ragged_tiles(tsx):
