@@ -171,7 +171,11 @@ tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, 
  * otherwise; c is required by fma and must be NULL otherwise (else
  * TSX_ERR_INVALID).  out may be exactly a, b or c; any other overlap is
  * undefined.  For an empty tensor (rows or cols 0) the call does nothing
- * and the pointers are not examined.  Base pointers must be 16-byte aligned
+ * and the pointers are not examined.  Buffers are device memory; TSX_LDGSTS
+ * and TSX_SYNC plans also take page-locked host memory that the device
+ * addresses directly (cudaHostAlloc, or a pinned torch tensor), in any mix
+ * with device buffers: the kernel then reads and writes it over the host
+ * link, with no staging copy.  Base pointers must be 16-byte aligned
  * for the TMA variants;
  * TSX_LDGSTS / TSX_SYNC narrow their copy width to the pointers' alignment
  * (16, 8 or 4 bytes) and return TSX_ERR_ALIGN below 4.

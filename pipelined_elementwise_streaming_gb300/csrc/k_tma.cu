@@ -52,17 +52,17 @@ namespace {
 using namespace dev;
 
 // The store warp's TMA stores of one tile from the slot at shared address
-// `slot`: each lane stores the boxes numbered lane, lane + 32, ... (`mine`
-// is the lane's first, n_boxes those of a full tile) and commits them as one
-// bulk group of its own; with ACC a reduce-store that adds the tile into
-// global memory.
+// `slot`: each of the first `lanes` lanes stores the boxes numbered lane,
+// lane + lanes, ... of the n_boxes of a full tile (`mine` is its first) and
+// commits them as one bulk group of its own; with ACC a reduce-store that
+// adds the tile into global memory.
 template <bool ACC>
 __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc,
-                                           const BoxRef& mine, int n_boxes, uint32_t slot)
+                                           const BoxRef& mine, int n_boxes, int lanes, uint32_t slot)
 {
     const int lane = static_cast<int>(threadIdx.x & 31);
     const TileBoxes b = boxes_at(p, tc.band, tc.ct);
-    for (int L = lane; L < n_boxes; L += 32) {
+    for (int L = lane; L < n_boxes; L += lanes) {
         const BoxRef x = L == lane ? mine : box_ref(maps, p, L, 3);
         if (!box_in(x, b))
             continue;
@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------- store warp
         const int n_boxes = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
+        // lanes issuing stores: one per box, except that reduce-stores go out
+        // from lane 0 alone (measured faster on GB300)
+        const int lanes = ACC ? 1 : n_boxes < 32 ? n_boxes : 32;
         const BoxRef mine = box_ref(maps, p, lane < n_boxes ? lane : 0, 3);
         const int lag = p.store_lag < S - 1 ? p.store_lag : S - 1;
         TileCursor tc(p, cta, G);
@@ -195,10 +198,12 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             const uint32_t ready = OP == TSX_COPY ? full : computed;
             if (!role_wait<kAllLanes>(ready + 8u * st.s, st.phase, p, abort_flag))
                 break;
-            store_tile<ACC>(maps, p, tc, mine, n_boxes, base + st.s * p.stage_bytes);
             // release tile i - lag once every lane's stores of it have read
-            // shared memory
-            bulk_wait_read(lag);
+            // shared memory (lanes without boxes keep out of the bulk groups)
+            if (lane < lanes) {
+                store_tile<ACC>(maps, p, tc, mine, n_boxes, lanes, base + st.s * p.stage_bytes);
+                bulk_wait_read(lag);
+            }
             __syncwarp();
             if (i >= lag) {
                 if (lane == 0)
@@ -208,7 +213,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             tc.next(p);
             st.next(S);
         }
-        bulk_wait_all();
+        if (lane < lanes)
+            bulk_wait_all();
     } else if (OP != TSX_COPY) {
         // ---------------------------------------------- compute warps
         const uint32_t tid = threadIdx.x - 64;
