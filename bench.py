@@ -548,17 +548,18 @@ def run_reference(args, w, stages, variant):
     if rank != 0:
         return None
     K, W = args.steps, args.warmup
-    # size each step so the whole run stays within about a minute
-    per_step_budget = max(1e-3, 60.0 / max(1, K + W))
+    # size each step so the whole run, input generation included, stays
+    # within about a minute (at most 2 s a step)
+    per_step_budget = min(2.0, max(1e-3, 60.0 / max(1, K + W)))
     import oracle
 
     oracle.build()
     probe = np.arange(0, min(w.elems, 1 << 16), dtype=np.uint64)
-    ins = w.inputs_at(probe)
     t0 = time.perf_counter()
+    ins = w.inputs_at(probe)
     oracle.ewise(w.op, w.dtype, *ins)
     per_elem = (time.perf_counter() - t0) / probe.size
-    n = int(max(1024, min(w.elems, per_step_budget / max(per_elem, 1e-10))))
+    n = int(max(1024, min(w.elems, 1 << 24, per_step_budget / max(per_elem, 1e-10))))
     rng = np.random.default_rng(0)
     total_bytes, total_s = 0, 0.0
     for k in range(W + K):
