@@ -23,9 +23,9 @@
 //               "elementwise -> smem", "Algorithm").  In the mixed variant
 //               operand b is not staged: the compute warps read it from
 //               global memory with plain vector loads at the positions of
-//               the staged vectors (nvFuser PR #2833, "Testing Setup",
-//               Pointwise: one tensor by TMA circular buffering, the other
-//               by ordinary loads).
+//               the staged vectors, one tile ahead into registers (nvFuser
+//               PR #2833, "Testing Setup", Pointwise: one tensor by TMA
+//               circular buffering, the other by Set circular buffering).
 //
 // The producer follows the loop structure of the nvFuser page ("Loop
 // Structure", "Detailed Pseudo-Code"): a pre-prologue that initialises the
@@ -85,28 +85,66 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
     bulk_commit();
 }
 
-// The op on one staged tile of the mixed variant: a (and c) from the slots,
-// b from global memory at the element the staged vector holds.
-template <int DT, int OP>
-__device__ __forceinline__ void compute_tile_mixed(const TmaArgs& p, uint4* A, const uint4* C, int64_t t,
-                                                   uint32_t tid, uint32_t threads)
+// Operand b of the mixed variant is not staged by TMA.  The compute threads
+// load it from global memory with plain 16-byte loads at the elements their
+// staged vectors hold: the "Set" circular buffering of the nvFuser page's
+// Pointwise test, kept in registers.  A thread's first kSetUnits units of a
+// tile (tid, tid + threads, ...) are loaded one tile ahead, before the wait
+// on the tile's stage, so the loads are in flight while the thread waits and
+// computes; any further units load on use.  The planner gives the mixed
+// variant enough threads that every unit is among the first kSetUnits.
+
+// b at staged unit u of the tile with boxes tb (zero outside the tensor and
+// in the padding after a box).  Loaded through L2 only: b may be the output,
+// whose other tiles TMA stores overwrite meanwhile.
+template <int DT>
+__device__ __forceinline__ uint4 load_b_unit(const TmaArgs& p, const TileBoxes& tb, uint32_t u)
 {
     constexpr int ES = DT == TSX_F32 ? 4 : 2;
-    const TileBoxes tb = tile_boxes(p, t);
-    const char* Bg = static_cast<const char*>(p.set_operand);
     const uint32_t inner_bytes = static_cast<uint32_t>(p.inner_elems) * ES;
-    for (uint32_t u = tid; u < p.vec16_per_slot; u += threads) {
-        const uint32_t off = u * 16;
-        const uint32_t load = off / p.load_smem_bytes;
-        const uint32_t within = off - load * p.load_smem_bytes;
-        uint4 vb = make_uint4(0, 0, 0, 0);
-        if (within < p.box_bytes) {
-            const uint32_t lo = unswizzle(within, p.swizzle_mask);
-            const int64_t row = tb.row0 + static_cast<int64_t>(load / p.atoms) * p.rows_per_load + lo / inner_bytes;
-            const int64_t col = tb.col0 + static_cast<int64_t>(load % p.atoms) * p.inner_elems + (lo % inner_bytes) / ES;
-            if (row < p.rows && col < p.cols)
-                vb = *reinterpret_cast<const uint4*>(Bg + (row * p.pitch + col) * ES);
+    const uint32_t off = u * 16;
+    const uint32_t load = off / p.load_smem_bytes;
+    const uint32_t within = off - load * p.load_smem_bytes;
+    uint4 vb = make_uint4(0, 0, 0, 0);
+    if (within < p.box_bytes) {
+        const uint32_t lo = unswizzle(within, p.swizzle_mask);
+        const int64_t row = tb.row0 + static_cast<int64_t>(load / p.atoms) * p.rows_per_load + lo / inner_bytes;
+        const int64_t col = tb.col0 + static_cast<int64_t>(load % p.atoms) * p.inner_elems + (lo % inner_bytes) / ES;
+        if (row < p.rows && col < p.cols)
+            vb = __ldcg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.set_operand) +
+                                                       (row * p.pitch + col) * ES));
+    }
+    return vb;
+}
+
+template <int DT>
+__device__ __forceinline__ void load_b_ahead(const TmaArgs& p, const TileBoxes& tb, uint32_t tid, uint32_t threads,
+                                             uint4 (&v)[kSetUnits])
+{
+#pragma unroll
+    for (int k = 0; k < kSetUnits; ++k) {
+        const uint32_t u = tid + k * threads;
+        v[k] = u < p.vec16_per_slot ? load_b_unit<DT>(p, tb, u) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// The op on one staged tile of the mixed variant: a (and c) from the slots,
+// b from the registers loaded ahead (bv) or, past those, from global memory.
+template <int DT, int OP>
+__device__ __forceinline__ void compute_tile_mixed(const TmaArgs& p, uint4* A, const uint4* C, const TileBoxes& tb,
+                                                   uint32_t tid, uint32_t threads, const uint4 (&bv)[kSetUnits])
+{
+#pragma unroll
+    for (int k = 0; k < kSetUnits; ++k) {
+        const uint32_t u = tid + k * threads;
+        if (u < p.vec16_per_slot) {
+            const uint4 va = A[u];
+            const uint4 vc = op_arity(OP) > 2 ? C[u] : va;
+            A[u] = op_vec16<DT, OP>(va, bv[k], vc);
         }
+    }
+    for (uint32_t u = tid + kSetUnits * threads; u < p.vec16_per_slot; u += threads) {
+        const uint4 vb = load_b_unit<DT>(p, tb, u);
         const uint4 va = A[u];
         const uint4 vc = op_arity(OP) > 2 ? C[u] : va;
         A[u] = op_vec16<DT, OP>(va, vb, vc);
@@ -220,12 +258,31 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         const uint32_t tid = threadIdx.x - 64;
         const uint32_t threads = blockDim.x - 64;
         StageCursor st;
+        // mixed variant: b of the next tile, loaded ahead into registers
+        constexpr bool kSet = MIXED && NIN >= 2;
+        uint4 b_next[kSetUnits];
+        TileCursor tc(p, cta, G);
+        if constexpr (kSet) {
+            if (N > 0)
+                load_b_ahead<DT>(p, boxes_at(p, tc.band, tc.ct), tid, threads, b_next);
+        }
         for (int64_t i = 0; i < N; ++i) {
+            uint4 b_cur[kSetUnits];
+            TileBoxes tb;
+            if constexpr (kSet) {
+#pragma unroll
+                for (int k = 0; k < kSetUnits; ++k)
+                    b_cur[k] = b_next[k];
+                tb = boxes_at(p, tc.band, tc.ct);
+                tc.next(p);
+                if (i + 1 < N)
+                    load_b_ahead<DT>(p, boxes_at(p, tc.band, tc.ct), tid, threads, b_next);
+            }
             if (!wait_or_abort(full + 8u * st.s, st.phase, p, abort_flag))
                 break;
             uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(st.s) * p.stage_bytes);
-            if constexpr (MIXED && NIN >= 2) {
-                compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, cta + i * G, tid, threads);
+            if constexpr (kSet) {
+                compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, tb, tid, threads, b_cur);
             } else {
                 const uint4* B = A + p.slot_bytes / 16;
                 const uint4* C = A + 2 * (p.slot_bytes / 16);

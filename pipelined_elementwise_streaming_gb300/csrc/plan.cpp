@@ -36,13 +36,15 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-int default_threads(int variant, size_t smem_bytes)
+int default_threads(int variant, size_t smem_bytes, uint32_t units)
 {
     // Threads of the elementwise stage.  TMA paths: about 256 compute
     // threads per SM in all, shared by the CTAs that fit in its shared
     // memory, between 2 and 8 compute warps per CTA (beside the producer
-    // and store warps); the mixed variant, whose compute threads also wait
-    // on global loads of b, aims at 1024 per SM and up to 16 warps per CTA.
+    // and store warps); the mixed variant, whose compute threads also load
+    // b one tile ahead for at most kSetUnits of the slot's `units` 16-byte
+    // vectors each, aims at about 512 per SM, rounded to the nearest warp,
+    // and at least enough threads to cover the slot that way.
     // The cp.async / synchronous ablations use 128, the thread count of the
     // TVM ldgsts demonstration program.  TSX_THREADS overrides (a multiple
     // of 32).
@@ -52,9 +54,15 @@ int default_threads(int variant, size_t smem_bytes)
         const bool mixed = variant == TSX_TMA_MIXED;
         const size_t per_cta = smem_bytes + kSmemPerCtaReserved;
         const int ctas = per_cta ? int(kSmemPerSm / per_cta) : 1;
-        const int share = (mixed ? 1024 : 256) / (ctas < 1 ? 1 : ctas);
+        const int share = (mixed ? 512 : 256) / (ctas < 1 ? 1 : ctas);
         const int cap = mixed ? 512 : 256;
-        fallback = share < 64 ? 64 : share > cap ? cap : share / 32 * 32;
+        const int warps = mixed ? (share + 16) / 32 : share / 32;
+        fallback = share < 64 ? 64 : share > cap ? cap : warps * 32;
+        if (mixed) {
+            const int cover = int((units + kSetUnits - 1) / kSetUnits + 31) / 32 * 32;
+            const int most = kMaxThreads - 32 * kTmaRoleWarps;
+            fallback = fallback > cover ? fallback : cover < most ? cover : most;
+        }
     }
     const int limit = tma ? kMaxThreads - 32 * kTmaRoleWarps : kMaxThreads;
     int t = env_int("TSX_THREADS", fallback);
@@ -227,7 +235,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     if (og->smem_bytes > size_t(max_smem))
         return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
                TSX_ERR_UNSUPPORTED;
-    og->threads = default_threads(g.variant, og->smem_bytes);
+    og->threads = default_threads(g.variant, og->smem_bytes, g.slot_bytes / 16);
     og->block_threads = og->threads + (tma ? 32 * kTmaRoleWarps : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;

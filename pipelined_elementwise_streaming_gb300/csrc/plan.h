@@ -49,7 +49,7 @@ struct TensorMapArgs {
     int swizzle = 0;   // CUtensorMapSwizzle value
 };
 
-int default_threads(int variant, size_t smem_bytes);
+int default_threads(int variant, size_t smem_bytes, uint32_t units);
 int default_store_lag(int stages);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,
                   int variant, Geometry* g, std::string* why);

@@ -40,6 +40,10 @@ TSX_HD constexpr int tma_operands(int variant, int op)
     return variant == TSX_TMA_MIXED && op_arity(op) >= 2 ? op_arity(op) - 1 : op_arity(op);
 }
 
+// Units (16-byte vectors of a staged slot) per compute thread whose operand
+// b the mixed variant loads one tile ahead into registers.
+constexpr int kSetUnits = 4;
+
 // Kernel arguments of the TMA circular-buffer kernel.
 struct TmaArgs {
     int64_t tiles;          // T: tiles in the tensor
