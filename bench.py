@@ -276,7 +276,7 @@ def run_ours(args, w, stages, variant):
     mode = args.mode
     nbytes = step_bytes(w, mode)
     plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant)
-    info = plan.info(w.op)
+    info = plan.info(w.op, row_sums=mode == "rowsum")
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))

@@ -85,10 +85,14 @@ typedef enum {
  * ("copy_async -> tma", table under "How inputs change the algorithm":
  * s2g with a reduce op): out = out + op(a, b, c), the sum rounded to nearest
  * even into the element type and added by the TMA unit in global memory.
- * Offered by TSX_TMA and TSX_TMA_RANK3 (else TSX_ERR_UNSUPPORTED). */
+ * Offered by TSX_TMA and TSX_TMA_RANK3 (else TSX_ERR_UNSUPPORTED).
+ *
+ * TSX_ROW_SUMS, OR-ed into an op, is understood by tsx_plan_get_info only:
+ * it asks for the launch tsx_reduce_rows makes for that op. */
 typedef enum {
     TSX_COPY = 0, TSX_SQRT = 1, TSX_EXP = 2, TSX_ADD = 3, TSX_MUL = 4, TSX_FMA = 5,
-    TSX_ACCUMULATE = 0x100
+    TSX_ACCUMULATE = 0x100,
+    TSX_ROW_SUMS = 0x200
 } tsx_op;
 
 typedef enum {
@@ -194,8 +198,9 @@ int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const vo
  * aligned, overwritten.  The persistent grid splits the tiles, in row-major
  * order, into one contiguous range per CTA, so a band of box_rows rows may
  * be cut between CTAs; the shares of a cut band go through scratch that the
- * plan allocates on its first row reduction of an op (TSX_ERR_NOMEM if that
- * fails) and owns until it is destroyed.  Row reductions of one plan must
+ * plan allocates on its first row reduction of an op, or the first
+ * tsx_plan_get_info with TSX_ROW_SUMS (TSX_ERR_NOMEM if that fails), and
+ * owns until it is destroyed.  Row reductions of one plan must
  * therefore not run concurrently on different streams.  The order of
  * additions depends on the plan alone, so results repeat bit for bit;
  * against the exact sum their error is at most gamma(cols - 1) * sum |x|,
@@ -237,7 +242,9 @@ int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t 
 
 /* tsx_plan_query for an existing plan, including the launch it makes on its
  * device (occupancy-derived CTAs per SM and grid).  Both accept an op with
- * TSX_ACCUMULATE. */
+ * TSX_ACCUMULATE; this one also an op with TSX_ROW_SUMS, for the launch of
+ * tsx_reduce_rows (threads, shared memory, grid), with the errors that call
+ * would return.  Elsewhere TSX_ROW_SUMS is TSX_ERR_INVALID. */
 int tsx_plan_get_info(tsx_plan_t plan, tsx_op op, tsx_plan_info *info);
 
 /* tsx_ewise for callers that may not allocate device memory.  The paper has

@@ -27,6 +27,7 @@ DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
 VARIANTS = {"tma": 0, "ldgsts": 1, "sync": 2, "tma_rank3": 3, "tma_mixed": 4, "tma_promoted": 5}
 OPS = {"copy": 0, "sqrt": 1, "exp": 2, "add": 3, "mul": 4, "fma": 5}
 TSX_ACCUMULATE = 0x100   # OR into an op: out += op(a, b, c) by TMA reduce-store
+TSX_ROW_SUMS = 0x200     # OR into an op for tsx_plan_get_info: the launch of tsx_reduce_rows
 ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
 STATUS = {0: "TSX_OK", -1: "TSX_ERR_INVALID", -2: "TSX_ERR_UNSUPPORTED", -3: "TSX_ERR_ALIGN",
           -4: "TSX_ERR_CUDA", -5: "TSX_ERR_TIMEOUT", -6: "TSX_ERR_NOMEM"}
@@ -211,9 +212,11 @@ class Plan:
         """Device-side status since the last call (reads and clears it)."""
         return tsx_plan_status(self.handle)
 
-    def info(self, op: str = "copy") -> dict:
+    def info(self, op: str = "copy", row_sums: bool = False) -> dict:
+        """The plan and its launch for `op` (of reduce_rows with row_sums)."""
         info = tsx_plan_info()
-        rc = tsx_plan_get_info(self.handle, _code(OPS, op), ctypes.byref(info))
+        code = _code(OPS, op) | (TSX_ROW_SUMS if row_sums else 0)
+        rc = tsx_plan_get_info(self.handle, code, ctypes.byref(info))
         if rc != TSX_OK:
             raise TsxError(rc, tsx_last_error())
         return info.as_dict()

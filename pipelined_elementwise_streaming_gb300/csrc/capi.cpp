@@ -467,14 +467,19 @@ int tsx_plan_get_info(tsx_plan_t p, tsx_op op_arg, tsx_plan_info* info)
 {
     if (!p || !info)
         return set_error(TSX_ERR_INVALID, "NULL plan or info");
+    const bool row_sums = (op_arg & TSX_ROW_SUMS) != 0;
     int op;
     bool accumulate;
-    if (!split_op(op_arg, &op, &accumulate))
+    if (!split_op(op_arg & ~TSX_ROW_SUMS, &op, &accumulate))
         return set_error(TSX_ERR_INVALID, "unknown op");
-    if (accumulate && !accumulate_offered(p->g.variant))
-        return set_error(TSX_ERR_UNSUPPORTED, "TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
+    if (accumulate && (row_sums || !accumulate_offered(p->g.variant)))
+        return set_error(row_sums ? TSX_ERR_INVALID : TSX_ERR_UNSUPPORTED,
+                         row_sums ? "TSX_ACCUMULATE does not apply to row sums"
+                                  : "TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
+    if (row_sums && p->g.variant != TSX_TMA && p->g.variant != TSX_TMA_RANK3)
+        return set_error(TSX_ERR_UNSUPPORTED, "row sums need a TSX_TMA or TSX_TMA_RANK3 plan");
     tsx_plan::OpLaunch* L = nullptr;
-    const int rc = prepare_op(p, op, accumulate, &L);
+    const int rc = row_sums ? prepare_rowsum(p, op, &L) : prepare_op(p, op, accumulate, &L);
     if (rc != TSX_OK)
         return rc;
     fill_info(p->g, L->og, info);

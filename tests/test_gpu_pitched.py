@@ -94,3 +94,27 @@ def test_pitched_view_must_match_the_plan(tsx):
             plan.ewise("copy", torch.zeros(rows, cols, device="cuda"), out=buf[:, :cols])   # dense input
         out = plan.ewise("copy", buf[:, :cols])          # out allocated with the plan's pitch
         assert out.stride(0) == pitch
+
+
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_pitched_row_sums(tsx, variant, dtype):
+    """Row sums over a pitched view: the padding (NaN sentinels) must not
+    leak into any sum; integer-valued rows make the sums exact."""
+    rows, cols, pitch, box = {"f32": (45, 96, 128, (8, 32)), "bf16": (70, 128, 192, (32, 64))}[dtype]
+    rng = np.random.default_rng(rows + cols)
+    vals = rng.integers(-8, 8, (rows, cols)).astype(np.float32)
+    if dtype == "f32":
+        bits = vals.view(np.uint32)
+    else:
+        bits = (vals.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    buf, view = _pitched(bits, dtype, pitch)
+    try:
+        plan = tsx.Plan(dtype, rows, cols, box=box, stages=3, variant=variant, pitch=pitch)
+    except tsx.TsxError:
+        pytest.skip("declined on the host")
+    with plan:
+        got = plan.reduce_rows("copy", view).cpu().numpy().astype(np.float64)
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+    assert np.array_equal(got, vals.astype(np.float64).sum(axis=1))

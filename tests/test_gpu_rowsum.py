@@ -164,6 +164,28 @@ def test_rowsum_edges_and_declines(tsx):
         assert rc == tsx.TSX_ERR_INVALID
 
 
+def test_rowsum_launch_info(tsx):
+    """TSX_ROW_SUMS asks tsx_plan_get_info for the row reduction's launch;
+    the other entry points reject the flag."""
+    with tsx.Plan("bf16", 300, 4096, box=(8, 128), stages=3) as plan:
+        ew, rs = plan.info("exp"), plan.info("exp", row_sums=True)
+        assert rs["block_threads"] == rs["threads"] + 32   # compute warps + the producer
+        assert ew["block_threads"] == ew["threads"] + 64   # + producer and store warps
+        assert 0 < rs["grid"] <= rs["tiles"] and rs["grid"] <= rs["ctas_per_sm"] * rs["sm_count"]
+        a = torch.zeros(300, 4096, dtype=torch.bfloat16, device="cuda")
+        out = torch.empty_like(a)
+        s = torch.cuda.current_stream().cuda_stream
+        assert tsx.tsx_ewise(plan.handle, tsx.OPS["exp"] | tsx.TSX_ROW_SUMS, a.data_ptr(), None, None,
+                             out.data_ptr(), s) == tsx.TSX_ERR_INVALID
+        sums = torch.empty(300, device="cuda")
+        assert tsx.tsx_reduce_rows(plan.handle, tsx.OPS["exp"] | tsx.TSX_ROW_SUMS, a.data_ptr(), None, None,
+                                   sums.data_ptr(), s) == tsx.TSX_ERR_INVALID
+    with tsx.Plan("f32", 16, 64, box=(8, 32), stages=2, variant="sync") as plan:
+        with pytest.raises(tsx.TsxError) as ei:
+            plan.info("copy", row_sums=True)
+        assert ei.value.code == tsx.TSX_ERR_UNSUPPORTED
+
+
 def test_rowsum_wait_timeout_is_reported(tsx, monkeypatch):
     """The producer is told to skip one tile's loads: the compute warps'
     bounded wait gives up, TSX_ERR_TIMEOUT is recorded, and the GPU stays
