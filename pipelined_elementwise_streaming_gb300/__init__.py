@@ -98,6 +98,9 @@ def _load():
     L.tsx_ewise_noalloc.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5 + \
                                    [ctypes.POINTER(ctypes.c_int)]
+    L.tsx_debug_trace.restype = ctypes.c_int
+    L.tsx_debug_trace.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     return L
 
 
@@ -116,6 +119,8 @@ tsx_reduce_rows = lib.tsx_reduce_rows
 # The plan-free, allocation-free form of tsx_ewise (device status word in a
 # static device array; see include/tsx.h for who needs it and its limits).
 tsx_ewise_noalloc = lib.tsx_ewise_noalloc
+# Test hook (include/tsx_debug.h): the schedule trace of a traced launch.
+tsx_debug_trace = lib.tsx_debug_trace
 
 
 def tsx_last_error() -> str:
@@ -211,6 +216,21 @@ class Plan:
     def status(self) -> int:
         """Device-side status since the last call (reads and clears it)."""
         return tsx_plan_status(self.handle)
+
+    def trace(self):
+        """The schedule trace of the plan's last traced launch (plans created
+        with env TSX_TRACE): uint32 [grid, events per CTA, 4]."""
+        import numpy as np
+
+        grid, per = ctypes.c_int32(), ctypes.c_int32()
+        rc = tsx_debug_trace(self.handle, None, 0, ctypes.byref(grid), ctypes.byref(per))
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+        buf = np.zeros((grid.value, per.value, 4), dtype=np.uint32)
+        rc = tsx_debug_trace(self.handle, buf.ctypes.data, buf.size, None, None)
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+        return buf
 
     def info(self, op: str = "copy", row_sums: bool = False) -> dict:
         """The plan and its launch for `op` (of reduce_rows with row_sums)."""

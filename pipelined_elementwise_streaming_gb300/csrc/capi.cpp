@@ -13,6 +13,7 @@
 #include <string>
 
 #include "plan.h"
+#include "tsx_debug.h"
 
 namespace tsx {
 
@@ -113,6 +114,11 @@ struct tsx_plan {
     int* d_status = nullptr;
     uint64_t timeout_ns = 1000000000ull;
     int64_t fault_tile = -1;
+    // test hook (env TSX_TRACE = events per CTA): traced kernels record their
+    // schedule into trace_buf, [trace_grid][trace_cap] events of 16 bytes
+    int trace_cap = 0;
+    uint32_t* trace_buf = nullptr;
+    int trace_grid = 0;
     bool checked = false;
     int ctas_per_sm_cap = 0;
 
@@ -139,21 +145,44 @@ namespace {
 // The mixed variant runs its own instantiation only for ops with a b operand.
 bool mixed_launch(int variant, int op) { return variant == TSX_TMA_MIXED && op_arity(op) >= 2; }
 
-int tma_kind(int variant, int op, bool accumulate)
+int tma_kind(int variant, int op, bool accumulate, bool traced)
 {
-    return accumulate ? kTmaAccumulate : mixed_launch(variant, op) ? kTmaMixed : kTmaPlain;
+    if (accumulate)
+        return kTmaAccumulate;
+    if (mixed_launch(variant, op))
+        return kTmaMixed;
+    return traced ? kTmaTraced : kTmaPlain;
 }
 
 // The reduce-store is offered by the two all-TMA variants.
 bool accumulate_offered(int variant) { return variant == TSX_TMA || variant == TSX_TMA_RANK3; }
 
-const void* kernel_of(int variant, int dtype, int op, bool accumulate)
+const void* kernel_of(int variant, int dtype, int op, bool accumulate, bool traced)
 {
     if (variant == TSX_LDGSTS)
         return ldgsts_kernel(dtype, op);
     if (variant == TSX_SYNC)
         return sync_kernel(dtype, op);
-    return tma_kernel(dtype, op, tma_kind(variant, op, accumulate));
+    return tma_kernel(dtype, op, tma_kind(variant, op, accumulate, traced));
+}
+
+// The trace ring of the traced kernel (test hook): large enough for `grid`
+// CTAs, cleared on `st` before every launch.
+int prepare_trace(tsx_plan* p, int grid, cudaStream_t st)
+{
+    const size_t per_cta = size_t(p->trace_cap) * 16;
+    if (p->trace_grid < grid) {
+        cudaFree(p->trace_buf);
+        p->trace_buf = nullptr;
+        p->trace_grid = 0;
+        if (cudaMalloc(&p->trace_buf, per_cta * size_t(grid)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return set_error(TSX_ERR_NOMEM, "allocating the trace ring");
+        }
+        p->trace_grid = grid;
+    }
+    const cudaError_t e = cudaMemsetAsync(p->trace_buf, 0, per_cta * size_t(grid), st);
+    return e == cudaSuccess ? TSX_OK : cuda_error(e, "clearing the trace ring");
 }
 
 // Geometry, kernel attributes, occupancy and grid for one op (cached).
@@ -165,7 +194,9 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
         const int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
         if (rc != TSX_OK)
             return set_error(rc, why);
-        const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate);
+        const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate, p->trace_cap > 0);
+        if (!fn)
+            return set_error(TSX_ERR_UNSUPPORTED, "TSX_TRACE: only fp32 copy and add have a traced kernel");
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.og.smem_bytes));
         if (e != cudaSuccess)
             return cuda_error(e, "cudaFuncSetAttribute");
@@ -434,6 +465,10 @@ tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, 
     const int64_t ms = env_i64("TSX_TIMEOUT_MS", 1000);
     p->timeout_ns = uint64_t(ms > 0 ? ms : 1000) * 1000000ull;
     p->fault_tile = env_i64("TSX_FAULT_SKIP_TILE", -1);
+    {
+        const int64_t cap = env_i64("TSX_TRACE", 0);
+        p->trace_cap = cap > 0 && cap <= (1 << 20) ? int(cap) : 0;
+    }
     p->checked = env_i64("TSX_CHECKED", 0) != 0;
     p->ctas_per_sm_cap = int(env_i64("TSX_CTAS_PER_SM", 0));
 
@@ -447,6 +482,7 @@ void tsx_plan_destroy(tsx_plan_t p)
         return;
     if (p->d_status)
         cudaFree(p->d_status);
+    cudaFree(p->trace_buf);
     for (auto& L : p->rowsum_ops) {
         cudaFree(L.scratch.piece);
         cudaFree(L.scratch.arrivals);
@@ -462,6 +498,27 @@ int tsx_plan_status(tsx_plan_t p)
 }
 
 const char* tsx_last_error(void) { return g_last_error; }
+
+int tsx_debug_trace(tsx_plan_t p, uint32_t* events, int64_t capacity, int32_t* grid, int32_t* per_cta)
+{
+    if (!p || (!events && capacity > 0) || capacity < 0)
+        return set_error(TSX_ERR_INVALID, "NULL plan or events");
+    if (p->trace_cap <= 0 || !p->trace_buf)
+        return set_error(TSX_ERR_INVALID, "the plan has no trace (TSX_TRACE unset, or no traced launch yet)");
+    const int64_t words = int64_t(p->trace_grid) * p->trace_cap * 4;
+    const int64_t n = capacity < words ? capacity : words;
+    if (n > 0) {
+        const cudaError_t e = cudaMemcpy(events, p->trace_buf, size_t(n) * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess)
+            return cuda_error(e, "reading the trace");
+    }
+    if (grid)
+        *grid = p->trace_grid;
+    if (per_cta)
+        *per_cta = p->trace_cap;
+    set_last_error("");
+    return TSX_OK;
+}
 
 int tsx_plan_get_info(tsx_plan_t p, tsx_op op_arg, tsx_plan_info* info)
 {
@@ -546,7 +603,14 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
         TmaArgs args{};
         fill_tma_args(p, L->og, &args);
         args.set_operand = mixed ? b : nullptr;
-        e = launch_tma(g.dtype, op, tma_kind(g.variant, op, accumulate), L->grid, L->og.block_threads,
+        if (p->trace_cap > 0) {
+            rc = prepare_trace(p, L->grid, st);
+            if (rc != TSX_OK)
+                return rc;
+            args.trace = p->trace_buf;
+            args.trace_cap = p->trace_cap;
+        }
+        e = launch_tma(g.dtype, op, tma_kind(g.variant, op, accumulate, p->trace_cap > 0), L->grid, L->og.block_threads,
                        L->og.smem_bytes, st, maps, args);
     } else {
         int vb = g.copy_vec_bytes < align ? g.copy_vec_bytes : align;

@@ -3,7 +3,7 @@
 // The schedule is the inner-persistent reduction of the nvFuser page
 // ("Testing Setup", Reduction and InnerPersistent): every tile of a row band
 // streams through the same S-stage TMA ring as the elementwise kernel and is
-// folded into per-row partials in shared memory.  The persistent grid splits
+// folded into fp32 partials.  The persistent grid splits
 // the tiles, taken in row-major order (band after band, left to right), into
 // G contiguous ranges of floor(T / G) or ceil(T / G) tiles: CTA c streams
 // tiles [c T / G, (c + 1) T / G), so the work is even however few the bands.
@@ -15,14 +15,16 @@
 //               staged slot holds the same (row, column within the tile) in
 //               every tile.  Compute thread tid always takes units tid, tid
 //               + threads, ...: it applies the op to the unit's vectors,
-//               rounds into the element type, adds the elements in order and
-//               adds that to the unit's fp32 partial in shared memory (set,
-//               on the first tile of the CTA's share of a band).  Only a
-//               band's last, ragged tile needs each unit's column, to leave
-//               out the columns past the tensor's end.  Every warp then
-//               releases the stage (`empty`, one arrival per warp).  When
-//               the CTA's share of a band ends, one thread per row adds the
-//               partials of the row's units, box by box in a fixed order.
+//               rounds into the element type and adds the elements in order
+//               to the unit's fp32 partial, kept in a register for the
+//               thread's first kRegUnits units and in shared memory for any
+//               further ones.  Only a band's last, ragged tile needs each
+//               unit's column, to leave out the columns past the tensor's
+//               end.  Every warp then releases the stage (`empty`, one
+//               arrival per warp).  When the CTA's share of a band ends, the
+//               register partials go to shared memory and one thread per row
+//               adds the partials of the row's units, box by box in a fixed
+//               order.
 //
 // A band the CTA streamed whole gets its row sums written directly.  A band
 // cut between CTAs c0 < ... < c1 (consecutive, since the ranges are) has

@@ -151,7 +151,23 @@ __device__ __forceinline__ void compute_tile_mixed(const TmaArgs& p, uint4* A, c
     }
 }
 
-template <int DT, int OP, bool MIXED, bool ACC>
+// Test hook of the traced instantiations: record one event in the CTA's
+// ring, numbered by a shared-memory counter.  A thread records an event
+// before the barrier arrival that lets other roles act on it, so the
+// numbering respects the order the barriers impose.
+template <bool TRACE>
+__device__ __forceinline__ void trace_event(const TmaArgs& p, uint32_t* counter, int kind, int64_t k, uint32_t a,
+                                            uint32_t b)
+{
+    if constexpr (TRACE) {
+        const uint32_t i = atomicAdd(counter, 1u);
+        if (i < static_cast<uint32_t>(p.trace_cap))
+            reinterpret_cast<uint4*>(p.trace)[static_cast<size_t>(blockIdx.x) * p.trace_cap + i] =
+                make_uint4(i, static_cast<uint32_t>(kind), static_cast<uint32_t>(k), a | (b << 16));
+    }
+}
+
+template <int DT, int OP, bool MIXED, bool ACC, bool TRACE = false>
 __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__ TmaMaps maps, const TmaArgs p)
 {
     constexpr int NIN = op_arity(OP);
@@ -167,6 +183,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     const uint32_t computed = full + 8u * S;
     const uint32_t empty = computed + 8u * S;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 8u * S - base));
+    uint32_t* trace_counter = reinterpret_cast<uint32_t*>(smem + (empty + 8u * S - base) + 4);
 
     const int warp = threadIdx.x / 32;
     const int compute_warps = blockDim.x / 32 - 2;
@@ -185,6 +202,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             mbar_init(empty + 8u * s, 1);
         }
         *abort_flag = 0;
+        *trace_counter = 0;
         fence_proxy_async_smem();
     }
     if (warp == 1 && elected)
@@ -202,6 +220,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         const int64_t pro = N < S - 1 ? N : S - 1;
         // Prologue: the first S - 1 tiles, into stages that start empty.
         for (; issued < pro; ++issued) {
+            if (lane == 0)
+                trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 0);
             issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
             tc.next(p);
             st.next(S);
@@ -211,6 +231,11 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         for (; issued < N; ++issued) {
             if (issued >= S && !role_wait<kAllLanes>(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag))
                 break;
+            if (lane == 0) {
+                if (issued >= S)
+                    trace_event<TRACE>(p, trace_counter, kTraceReuse, issued, st.s, st.phase ^ 1u);
+                trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 1);
+            }
             issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
             tc.next(p);
             st.next(S);
@@ -236,6 +261,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             const uint32_t ready = OP == TSX_COPY ? full : computed;
             if (!role_wait<kAllLanes>(ready + 8u * st.s, st.phase, p, abort_flag))
                 break;
+            if (lane == 0)
+                trace_event<TRACE>(p, trace_counter, kTraceStore, i, st.s, st.phase);
             // release tile i - lag once every lane's stores of it have read
             // shared memory (lanes without boxes keep out of the bulk groups)
             if (lane < lanes) {
@@ -244,8 +271,10 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             }
             __syncwarp();
             if (i >= lag) {
-                if (lane == 0)
+                if (lane == 0) {
+                    trace_event<TRACE>(p, trace_counter, kTraceRelease, i - lag, released.s, 0);
                     mbar_arrive(empty + 8u * released.s);
+                }
                 released.next(S);
             }
             tc.next(p);
@@ -280,6 +309,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             }
             if (!wait_or_abort(full + 8u * st.s, st.phase, p, abort_flag))
                 break;
+            if (tid == 0)
+                trace_event<TRACE>(p, trace_counter, kTraceWait, i, st.s, st.phase);
             uint4* A = reinterpret_cast<uint4*>(smem + static_cast<size_t>(st.s) * p.stage_bytes);
             if constexpr (kSet) {
                 compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, tb, tid, threads, b_cur);
@@ -295,6 +326,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             }
             // this thread's generic-proxy writes become visible to the TMA store
             fence_proxy_async_smem();
+            if (tid == 0)
+                trace_event<TRACE>(p, trace_counter, kTraceBody, i, st.s, 0);
             __syncwarp();
             if ((threadIdx.x & 31) == 0)
                 mbar_arrive(computed + 8u * st.s);
@@ -324,7 +357,22 @@ const void* const kKernels[3][3][6] = {TSX_KIND(false, false), TSX_KIND(true, fa
 
 }  // namespace
 
-const void* tma_kernel(int dtype, int op, int kind) { return kKernels[kind][dtype][op]; }
+// the traced instantiations (test hook)
+const void* traced_kernel(int dtype, int op)
+{
+    if (dtype != TSX_F32)
+        return nullptr;
+    if (op == TSX_COPY)
+        return (const void*)tma_ewise<TSX_F32, TSX_COPY, false, false, true>;
+    if (op == TSX_ADD)
+        return (const void*)tma_ewise<TSX_F32, TSX_ADD, false, false, true>;
+    return nullptr;
+}
+
+const void* tma_kernel(int dtype, int op, int kind)
+{
+    return kind == kTmaTraced ? traced_kernel(dtype, op) : kKernels[kind][dtype][op];
+}
 
 cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args)
@@ -334,7 +382,7 @@ cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_
         m.m[j] = maps[j];
     TmaArgs a = args;
     void* params[] = {&m, &a};
-    return cudaLaunchKernel(kKernels[kind][dtype][op], dim3(grid), dim3(threads), params, smem, stream);
+    return cudaLaunchKernel(tma_kernel(dtype, op, kind), dim3(grid), dim3(threads), params, smem, stream);
 }
 
 }  // namespace tsx

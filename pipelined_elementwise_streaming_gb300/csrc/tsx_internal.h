@@ -72,6 +72,21 @@ struct TmaArgs {
     const void* set_operand;
     uint32_t box_bytes;        // rows_per_load * inner bytes: the data part of one load
     int swizzle_mask;          // 7, 3, 1 for the 128/64/32-byte swizzle, 0 for none
+    // test hook (traced kernels only): per CTA a ring of trace_cap events of
+    // four 32-bit words each
+    uint32_t* trace;
+    int trace_cap;
+};
+
+// Event kinds of the traced kernel (test hook): what happened to tile k of
+// the CTA, recorded in the order the CTA's threads counted them.
+enum TraceKind {
+    kTraceLoad = 1,      // producer: about to issue tile k into stage a; b = 0 prologue, 1 main loop
+    kTraceReuse = 2,     // producer: stage a of tile k released (empty phase b completed)
+    kTraceWait = 3,      // compute: tile k's stage a full (phase b completed)
+    kTraceBody = 4,      // compute: tile k computed (thread 0's share)
+    kTraceStore = 5,     // store: tile k's stores about to be issued from stage a
+    kTraceRelease = 6,   // store: tile k's stage a handed back to the producer
 };
 
 // Kernel arguments of the cp.async and synchronous ablation kernels.
@@ -91,10 +106,11 @@ struct CopyArgs {
 
 // Kernel lookup and launch, one set per variant (k_tma.cu, k_ldgsts.cu,
 // k_sync.cu).  `maps` holds the tensor maps of a, b, c and out.
-// Instantiations of the TMA kernel: plain, mixed (b by plain loads), and
-// accumulate (the result reduce-added into out).  maps[0..2] are the
-// TMA-loaded operands in slot order, maps[3] the output.
-enum TmaKind { kTmaPlain = 0, kTmaMixed = 1, kTmaAccumulate = 2 };
+// Instantiations of the TMA kernel: plain, mixed (b by plain loads),
+// accumulate (the result reduce-added into out), and traced (a plain kernel
+// that also records its schedule; fp32 copy and add only, else NULL).
+// maps[0..2] are the TMA-loaded operands in slot order, maps[3] the output.
+enum TmaKind { kTmaPlain = 0, kTmaMixed = 1, kTmaAccumulate = 2, kTmaTraced = 3 };
 const void* tma_kernel(int dtype, int op, int kind = kTmaPlain);
 cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args);

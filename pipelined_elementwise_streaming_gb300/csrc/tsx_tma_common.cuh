@@ -44,12 +44,6 @@ __device__ __forceinline__ TileBoxes boxes_at(const TmaArgs& p, int64_t band, in
     return b;
 }
 
-__device__ __forceinline__ TileBoxes tile_boxes(const TmaArgs& p, int64_t t)
-{
-    const int64_t band = t / p.tiles_c;
-    return boxes_at(p, band, t - band * p.tiles_c);
-}
-
 // Walks the tiles t0, t0 + step, t0 + 2 step, ... in (row band, column tile)
 // form without a division per step.
 struct TileCursor {

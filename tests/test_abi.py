@@ -2,6 +2,7 @@
 and its planner agrees with the oracle's structure models (no GPU needed)."""
 
 import ctypes
+import glob
 import itertools
 import os
 import re
@@ -11,7 +12,7 @@ import pytest
 from oracle import structure as st
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "tsx.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -25,14 +26,18 @@ def tsx():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tsx_[a-z_]+)\s*\(", text)))
+    """Every function any header under include/ declares."""
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(tsx_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for required in ("tsx_plan_create", "tsx_ewise", "tsx_plan_destroy", "tsx_plan_status", "tsx_last_error"):
+    for required in ("tsx_plan_create", "tsx_ewise", "tsx_plan_destroy", "tsx_plan_status", "tsx_last_error",
+                     "tsx_reduce_rows", "tsx_ewise_noalloc", "tsx_debug_trace"):
         assert required in names
 
 
