@@ -120,6 +120,18 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def git_revision():
+    """The checkout's commit, or None where the tree is not a git checkout."""
+    import subprocess
+
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "--short=12", "HEAD"], capture_output=True, text=True,
+                           timeout=10)
+    except (OSError, subprocess.SubprocessError):
+        return None
+    return r.stdout.strip() or None if r.returncode == 0 else None
+
+
 def source_digest() -> str:
     import hashlib
 
@@ -359,6 +371,12 @@ def run_ours(args, w, stages, variant):
     else:
         e2e = {"value": None, "unit": "GB/s", "note": f"the end-to-end leg runs in ewise mode only, not {mode}"}
     plan.close()
+    # the first rows of the device result, for the oracle's check in the
+    # CPU-baseline leg (ewise mode: out holds op(inputs) exactly once)
+    head = None
+    if mode == "ewise":
+        band = oracle_band_rows(w)
+        head = out[:band].contiguous().view(torch.int16 if ti.ELEM_SIZE[w.dtype] == 2 else torch.int32).cpu().numpy()
 
     result = {
         "metric": METRIC,
@@ -382,6 +400,8 @@ def run_ours(args, w, stages, variant):
                   else f"inputs larger than L2 ({nbytes >> 20} MiB moved per step vs 129 MiB L2), "
                        "steps back to back",
             "parallelism": "replicas" if world > 1 else "single GPU",
+            "kernel_sources_sha256_16": source_digest(),
+            "git": git_revision(),
         },
         "memcpy_ceiling_gbs": round(ceiling, 1),
         "frac_of_memcpy_ceiling": round(value / world / ceiling, 4),
@@ -397,6 +417,7 @@ def run_ours(args, w, stages, variant):
             "median_launch_ms": round(statistics.median(launch_s) * 1e3, 5),
         },
     }
+    result["_device_head"] = head
     return result, td, rank
 
 
@@ -513,14 +534,20 @@ def run_e2e(torch, tsx, w, stages, variant, host, dev_in, out, steps, td, band_b
 
 # ------------------------------------------------------------ the oracle
 
-def cpu_time_oracle(w, seconds_budget, start_row=0, max_rows=None):
+def oracle_band_rows(w) -> int:
+    """Rows per band of the CPU-baseline leg (about 4 Mi elements)."""
+    return max(1, min(w.rows, (1 << 22) // w.cols or 1))
+
+
+def cpu_time_oracle(w, seconds_budget, start_row=0, max_rows=None, first=None):
     """Run the oracle over row bands of the workload until the budget is
-    spent or the rows run out.  Returns (bytes, seconds, rows, cores)."""
+    spent or the rows run out.  Returns (bytes, seconds, rows, cores); the
+    first band's result goes to first[0] when a list is given."""
     import oracle
 
     oracle.build()
     rows_done, spent, nbytes = 0, 0.0, 0
-    band = max(1, min(w.rows, (1 << 22) // w.cols or 1))
+    band = oracle_band_rows(w)
     r = start_row
     limit = w.rows if max_rows is None else min(w.rows, start_row + max_rows)
     while r < limit and spent < seconds_budget:
@@ -528,19 +555,44 @@ def cpu_time_oracle(w, seconds_budget, start_row=0, max_rows=None):
         idx = np.arange(r * w.cols, r1 * w.cols, dtype=np.uint64)
         ins = w.inputs_at(idx)
         t0 = time.perf_counter()
-        oracle.ewise(w.op, w.dtype, *ins)
+        res = oracle.ewise(w.op, w.dtype, *ins)
         spent += time.perf_counter() - t0
+        if first is not None and not first:
+            first.append(res)
         nbytes += (w.n_in + 1) * idx.size * ti.ELEM_SIZE[w.dtype]
         rows_done += r1 - r
         r = r1
     return nbytes, spent, rows_done, 1
 
 
-def cpu_baseline(w, seconds):
-    nbytes, spent, rows, cores = cpu_time_oracle(w, seconds)
-    return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+def cpu_baseline(w, seconds, device_head=None):
+    """The oracle's throughput on the host; with the device result's first
+    rows, also the element-by-element check of those rows against the
+    oracle's (bit-exact, or the exp ulp bound)."""
+    import oracle
+
+    first = []
+    nbytes, spent, rows, cores = cpu_time_oracle(w, seconds, first=first)
+    base = {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of {w.name} ({rows * w.cols} elements), single-threaded C oracle, "
                       f"{spent:.1f} s of CPU time"}
+    parity = None
+    if device_head is not None and first:
+        bits = np.dtype(np.uint16 if ti.ELEM_SIZE[w.dtype] == 2 else np.uint32)
+        got = device_head.reshape(-1).view(bits)
+        want = np.asarray(first[0]).reshape(-1).view(bits)[: got.size]
+        if w.op == "exp":
+            bad = int(np.count_nonzero(oracle.ulp_distance(got, want, w.dtype) > oracle.EXP_ULP_BOUND[w.dtype]))
+            rule = f"within {oracle.EXP_ULP_BOUND[w.dtype]} ulp"
+        elif w.op == "copy":
+            bad = int(np.count_nonzero(got != want))
+            rule = "bitwise"
+        else:
+            bad = int(np.count_nonzero(~oracle.same_value(got, want, w.dtype)))
+            rule = "bit-exact"
+        parity = {"elements": int(got.size), "mismatches": bad, "rule": rule, "against": "oracle",
+                  "rows": f"0..{device_head.shape[0] - 1} of the timed steps' output"}
+    return base, parity
 
 
 def run_reference(args, w, stages, variant):
@@ -607,9 +659,12 @@ def main(argv=None):
             print(json.dumps(res), flush=True)
         return 0
     res, td, rank = run_ours(args, w, stages, variant)
+    head = res.pop("_device_head", None)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+            res["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, head)
+            if parity is not None:
+                res["parity"] = parity
         print(json.dumps(res), flush=True)
     barrier(td)
     if td is not None:
