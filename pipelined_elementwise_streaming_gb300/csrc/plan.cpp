@@ -45,11 +45,13 @@ int default_threads(int variant, size_t smem_bytes, uint32_t units)
     // b one tile ahead for at most kSetUnits of the slot's `units` 16-byte
     // vectors each, aims at about 512 per SM, rounded to the nearest warp,
     // and at least enough threads to cover the slot that way.
-    // The cp.async / synchronous ablations use 128, the thread count of the
-    // TVM ldgsts demonstration program.  TSX_THREADS overrides (a multiple
-    // of 32).
+    // The cp.async / synchronous ablations give each thread about four
+    // 16-byte units of the slot, between 128 threads (the TVM ldgsts
+    // demonstration program's count, which its 128x32 fp16 tile gets) and
+    // 512.  TSX_THREADS overrides (a multiple of 32).
     const bool tma = is_tma_variant(variant);
-    int fallback = 128;
+    int fallback = int((units / 4 + 31) / 32 * 32);
+    fallback = fallback < 128 ? 128 : fallback > 512 ? 512 : fallback;
     if (tma) {
         const bool mixed = variant == TSX_TMA_MIXED;
         const size_t per_cta = smem_bytes + kSmemPerCtaReserved;
