@@ -67,6 +67,10 @@ def parse_args(argv=None):
     p.add_argument("--mode", default="ewise", choices=["ewise", "accumulate", "rowsum"],
                    help="ewise: out = op(...); accumulate: out += op(...) by TMA reduce-store; "
                         "rowsum: fp32 row sums of op(...)")
+    p.add_argument("--sweep", action="store_true",
+                   help="tuning sweep instead of the benchmark: time the workload's op over candidate boxes, stage "
+                        "counts and thread counts (the plans the host accepts), check each result against the "
+                        "workload's own plan bit for bit, and print one JSON line per candidate, fastest first")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -595,6 +599,76 @@ def cpu_baseline(w, seconds, device_head=None):
     return base, parity
 
 
+SWEEP_BOXES = [(8, 128), (16, 128), (32, 128), (64, 128), (128, 128), (8, 256), (32, 256), (64, 64), (128, 64),
+               (256, 64), (16, 512), (64, 512)]
+
+
+def run_sweep(args, w, stages, variant):
+    """Time every accepted (box, stages, threads) candidate of the workload's
+    op and variant; each candidate's output must equal the workload's own
+    plan's output bit for bit.  Returns the result lines, fastest first."""
+    import os as _os
+
+    import torch
+
+    import pipelined_elementwise_streaming_gb300 as tsx
+
+    torch.cuda.set_device(0)
+    dev_in = [h.to("cuda") for h in to_host_tensors(w, torch)]
+    ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))
+    ref = torch.zeros_like(dev_in[0])
+    out = torch.zeros_like(dev_in[0])
+    s = torch.cuda.current_stream().cuda_stream
+    with tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant) as p:
+        p.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], ref.data_ptr(), s)
+    torch.cuda.synchronize()
+    nbytes = step_bytes(w, "ewise")
+    K = max(20, min(args.steps, 200))
+    lines = []
+    seen = set()
+    saved = _os.environ.get("TSX_THREADS")
+    try:
+        for box in SWEEP_BOXES:
+            for st in (2, 3, 4, 6):
+                for threads in (None, 128, 256):
+                    if threads is None:
+                        _os.environ.pop("TSX_THREADS", None)
+                    else:
+                        _os.environ["TSX_THREADS"] = str(threads)
+                    try:
+                        plan = tsx.Plan(w.dtype, w.rows, w.cols, box=box, stages=st, variant=variant)
+                        info = plan.info(w.op)
+                    except tsx.TsxError:
+                        continue
+                    key = (box, st, info["threads"])
+                    if (threads is not None and info["threads"] != threads) or key in seen:
+                        plan.close()
+                        continue
+                    seen.add(key)
+                    out.zero_()
+                    for _ in range(3):
+                        plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(K):
+                        plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ok = plan.status() == tsx.TSX_OK and torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+                    plan.close()
+                    sec = e0.elapsed_time(e1) / 1e3 / K
+                    lines.append({"sweep": w.name, "op": w.op, "variant": variant, "box": list(box), "stages": st,
+                                  "threads": info["threads"], "grid": info["grid"], "gbs": round(nbytes / sec / 1e9, 1),
+                                  "same_as_workload_plan": bool(ok)})
+    finally:
+        if saved is None:
+            _os.environ.pop("TSX_THREADS", None)
+        else:
+            _os.environ["TSX_THREADS"] = saved
+    lines.sort(key=lambda d: -d["gbs"])
+    return lines
+
+
 def run_reference(args, w, stages, variant):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -653,6 +727,10 @@ def main(argv=None):
         w = replace(w, op=args.op)
     stages = args.stages if args.stages is not None else w.default_stages
     variant = args.variant or w.variant
+    if args.sweep:
+        for line in run_sweep(args, w, stages, variant):
+            print(json.dumps(line), flush=True)
+        return 0
     if args.impl == "reference":
         res = run_reference(args, w, stages, variant)
         if res is not None:
