@@ -1,0 +1,89 @@
+"""The tuning knobs (environment, read at plan creation) change launch
+shapes and timing only, never results: every setting is checked against the
+oracle on ragged shapes, and the store lag also against the schedule model
+through the traced kernel."""
+
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import structure as st
+from tests import _gpu
+from tests._gpu import bits_of, compare, random_bits, to_dev, torch
+from tests.test_gpu_schedule_trace import _check_cta
+
+pytestmark = pytest.mark.gpu
+
+ARITY = {"copy": 1, "sqrt": 1, "exp": 1, "add": 2, "mul": 2, "fma": 3}
+CASES = [("f32", "fma", 77, 1000, (8, 128)), ("bf16", "exp", 130, 2056, (32, 64)), ("f16", "add", 33, 520, (16, 256))]
+
+
+@pytest.fixture(scope="module")
+def tsx():
+    _gpu.need_gpu()
+    import pipelined_elementwise_streaming_gb300 as m
+
+    return m
+
+
+def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", accumulate=False):
+    seed = zlib.crc32(f"knob/{dtype}/{op}/{rows}/{cols}/{box}/{stages}/{variant}".encode())
+    ins = [random_bits(dtype, (rows, cols), seed + k) for k in range(ARITY[op])]
+    want = oracle.ewise(op, dtype, *ins)
+    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant=variant) as plan:
+        out = plan.ewise(op, *[to_dev(x, dtype) for x in ins])
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+        info = plan.info(op)
+    compare(op, dtype, bits_of(out, dtype), want, f"{variant} {dtype} {op} box {box} S={stages}")
+    return info
+
+
+@pytest.mark.parametrize("knob,values", [
+    ("TSX_STORE_LAG", ["0", "1", "2", "3"]),
+    ("TSX_L2_PROMOTION", ["0", "1", "2", "3"]),
+    ("TSX_THREADS", ["32", "96", "256", "960"]),
+    ("TSX_CTAS_PER_SM", ["1", "2", "3"]),
+])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_knobs_leave_results_unchanged(tsx, monkeypatch, knob, values, case):
+    dtype, op, rows, cols, box = CASES[case]
+    for v in values:
+        monkeypatch.setenv(knob, v)
+        for variant in ("tma", "tma_rank3"):
+            for stages in (2, 4):
+                try:
+                    tsx.query(dtype, rows, cols, box, stages, variant, op)
+                except tsx.TsxError:
+                    continue
+                info = _run(tsx, dtype, op, rows, cols, box, stages, variant)
+                if knob == "TSX_THREADS":
+                    assert info["threads"] == int(v)
+                if knob == "TSX_CTAS_PER_SM":
+                    assert info["ctas_per_sm"] <= int(v)
+        monkeypatch.delenv(knob)
+
+
+@pytest.mark.parametrize("lag", [0, 2, 3])
+@pytest.mark.parametrize("stages", [2, 4])
+def test_store_lag_follows_the_schedule_model(tsx, monkeypatch, lag, stages):
+    """With TSX_STORE_LAG the store warp releases tile i - lag (lag capped at
+    S - 1) after tile i's stores; the trace must still satisfy the model."""
+    monkeypatch.setenv("TSX_STORE_LAG", str(lag))
+    monkeypatch.setenv("TSX_TRACE", "256")
+    monkeypatch.setenv("TSX_CTAS_PER_SM", "1")
+    tiles = 1000
+    rows, cols = 8 * tiles, 32
+    a, b = random_bits("f32", (rows, cols), lag), random_bits("f32", (rows, cols), lag + 1)
+    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages) as plan:
+        out = plan.ewise("add", to_dev(a, "f32"), to_dev(b, "f32"))
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+        trace = plan.trace()
+    compare("add", "f32", bits_of(out, "f32"), oracle.ewise("add", "f32", a, b), "traced add")
+    eff = min(lag, stages - 1)
+    G = trace.shape[0]
+    for c in range(G):
+        _check_cta(trace[c], len(st.cta_tiles(tiles, G, c)), stages, eff, "add")
