@@ -1,6 +1,7 @@
-"""Host-side logic of bench.py: the reference (CPU oracle) arm's JSON line,
-the timing aggregation over ranks (world size 2, gloo, on CPU) and the
-clock-sample parser."""
+"""Host-side logic of bench.py: the reference (CPU oracle) arm's JSON line
+and its rank handling, the oracle check of the device output, the timing
+aggregation over ranks (world size 2, gloo, on CPU) and the clock-sample
+parser."""
 
 import json
 import multiprocessing as mp
@@ -22,6 +23,32 @@ def test_reference_arm_json_line(capsys):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "sqrt_500x4096_f32"
+
+
+def test_reference_arm_other_ranks_print_nothing(capsys, monkeypatch):
+    """Under torchrun only rank 0 runs and prints the reference arm; the
+    other ranks exit 0 without work."""
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    rc = bench.main(["--impl", "reference", "--steps", "3", "--warmup", "1", "--workload", "sqrt_500x4096_f32"])
+    assert rc == 0
+    assert capsys.readouterr().out.strip() == ""
+
+
+def test_parity_leg_flags_a_differing_element():
+    """The CPU-baseline leg's check of the device output: an output equal to
+    the oracle's has no mismatch, one flipped bit is one mismatch."""
+    import numpy as np
+
+    import oracle
+
+    w = bench.ti.WORKLOADS["fma_128x1048576_f32"].with_rows(1)
+    band = bench.oracle_band_rows(w)
+    idx = np.arange(0, band * w.cols, dtype=np.uint64)
+    head = np.asarray(oracle.ewise(w.op, w.dtype, *w.inputs_at(idx))).view(np.int32).reshape(band, w.cols)
+    assert bench.cpu_baseline(w, 0.2, head)[1]["mismatches"] == 0
+    head[0, 7] ^= 1
+    assert bench.cpu_baseline(w, 0.2, head)[1]["mismatches"] == 1
 
 
 def test_cpu_baseline_is_bounded():
