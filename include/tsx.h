@@ -23,10 +23,12 @@
  *
  * Conventions for every entry point:
  *  - Device pointers are CUDA device (or managed) addresses on the device
- *    that was current when the plan was created.  The caller owns every
+ *    that was current when the plan was created (TSX_LDGSTS and TSX_SYNC
+ *    also take pinned host memory; see tsx_ewise).  The caller owns every
  *    buffer and keeps it alive until the work queued on the stream is done.
- *  - Tensors are dense and row-major: element (r, c) sits at byte offset
- *    (r * cols + c) * element_size from the base pointer.
+ *  - Tensors are row-major: element (r, c) sits at byte offset
+ *    (r * pitch + c) * element_size from the base pointer, pitch = cols
+ *    unless the plan was created with tsx_plan_create_pitched.
  *  - Functions returning int return a tsx_status (0 = TSX_OK, negative =
  *    error).  On an error nothing was queued on the stream, and
  *    tsx_last_error() describes it.
@@ -44,15 +46,17 @@ extern "C" {
 #endif
 
 /* Element types.  Arithmetic on 16-bit types is carried out in fp32 and
- * rounded once to nearest-even into the element type (fma: one rounding of
- * the exact a * b + c). */
+ * rounded once to nearest-even into the element type; fma and sqrt use the
+ * native 16-bit instructions, one rounding of the exact result. */
 typedef enum { TSX_F16 = 0, TSX_BF16 = 1, TSX_F32 = 2 } tsx_dtype;
 
 /* How stages are filled.
- *  TSX_TMA       one elected thread issues cp.async.bulk.tensor loads (one
- *                rank-2 box per 128-byte atom of a tile row and per <= 256-row
- *                chunk) completing on the stage's mbarrier; the result goes
- *                back with cp.async.bulk.tensor stores.  The primary path.
+ *  TSX_TMA       the producer warp issues the cp.async.bulk.tensor loads of
+ *                a tile, one box per lane (one rank-2 box per 128-byte atom
+ *                of a tile row and per <= 256-row chunk), completing on the
+ *                stage's mbarrier, whose expect_tx lane 0 announces (the
+ *                pages issue from one elected thread); the result goes back
+ *                with cp.async.bulk.tensor stores.  The primary path.
  *  TSX_LDGSTS    every thread issues cp.async (LDGSTS) copies of 16, 8 or 4
  *                bytes; commit_group / wait_group per stage; the result is
  *                written with vector stores.  Ablation.
@@ -62,10 +66,11 @@ typedef enum { TSX_F16 = 0, TSX_BF16 = 1, TSX_F32 = 2 } tsx_dtype;
  *                a row chunk ("copy_async -> tma", "Generated TIRx IR");
  *                needs cols to be a whole number of atoms.
  *  TSX_TMA_MIXED as TSX_TMA for a (and c), while b is read by the compute
- *                threads with plain vector loads from global memory: one
- *                operand through the TMA circular buffer, the other through
- *                ordinary loads (nvFuser PR #2833, "Testing Setup",
- *                Pointwise).  Unary ops run as TSX_TMA.
+ *                threads with plain vector loads from global memory, one
+ *                tile ahead into registers: one operand through the TMA
+ *                circular buffer, the other through Set circular buffering
+ *                (nvFuser PR #2833, "Testing Setup", Pointwise).  Unary ops
+ *                run as TSX_TMA.
  *  TSX_TMA_PROMOTED  one box per <= 256-row chunk spans the whole tile row,
  *                with no swizzle: the tensor map counts in elements widened
  *                along 1 -> 2 -> 4 -> 8 bytes until the row holds at most
