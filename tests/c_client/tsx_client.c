@@ -6,7 +6,9 @@
  *   2. tsx_plan_query plans without a GPU;
  *   3. on a GPU, an fp32 fma over a ragged [rows, cols] tensor equals the C
  *      library's fmaf element by element (fmaf rounds a * b + c once, as
- *      the operation is defined), and the plan's status stays TSX_OK.
+ *      the operation is defined), and the plan's status stays TSX_OK;
+ *   4. tsx_ewise_noalloc gives the same bits;
+ *   5. row sums of small integers are exact.
  *
  * Usage: tsx_client [--no-gpu].  Prints one line per check and exits 0 when
  * every check passed. */
@@ -91,6 +93,37 @@ static void gpu_checks(void)
             bad++;
     }
     check(bad == 0, "fma equals fmaf bit for bit");
+
+    /* the allocation-free entry point gives the same bits */
+    float* h_na = (float*)malloc(bytes);
+    int status = -100;
+    check(tsx_ewise_noalloc(TSX_F32, rows, cols, 8, 128, 4, TSX_TMA, TSX_FMA, d[0], d[1], d[2], d[3], NULL,
+                            &status) == TSX_OK && status == TSX_OK,
+          "tsx_ewise_noalloc");
+    cudaMemcpy(h_na, d[3], bytes, cudaMemcpyDeviceToHost);
+    check(memcmp(h_na, h[3], bytes) == 0, "noalloc equals tsx_ewise bit for bit");
+    free(h_na);
+
+    /* row sums of small integers are exact in fp32 whatever the order */
+    for (size_t i = 0; i < n; ++i)
+        h[0][i] = (float)((int)(mix(7 * i) % 129) - 64);
+    cudaMemcpy(d[0], h[0], bytes, cudaMemcpyHostToDevice);
+    float* d_sums = NULL;
+    float h_sums[37];
+    cudaMalloc((void**)&d_sums, sizeof h_sums);
+    check(tsx_reduce_rows(plan, TSX_COPY, d[0], NULL, NULL, d_sums, NULL) == TSX_OK, "tsx_reduce_rows");
+    cudaDeviceSynchronize();
+    check(tsx_plan_status(plan) == TSX_OK, "device status after row sums");
+    cudaMemcpy(h_sums, d_sums, sizeof h_sums, cudaMemcpyDeviceToHost);
+    int exact = 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double want = 0;
+        for (int64_t c = 0; c < cols; ++c)
+            want += h[0][r * cols + c];
+        exact &= (double)h_sums[r] == want;
+    }
+    check(exact, "integer row sums exact");
+    cudaFree(d_sums);
     tsx_plan_destroy(plan);
     tsx_plan_destroy(NULL);
     for (int k = 0; k < 4; ++k) {
