@@ -192,7 +192,9 @@ tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, 
  * wait that exceeds its time limit (default 1 s, env TSX_TIMEOUT_MS) makes
  * the kernel record TSX_ERR_TIMEOUT in the plan's status word and return;
  * read it with tsx_plan_status.  With env TSX_CHECKED=1 the call
- * synchronizes the stream and returns the device status instead. */
+ * synchronizes the stream and returns the device status instead.  After a
+ * plan's first call of an op (which sets up its launch) later calls of that
+ * op only launch on `stream`, so they can be captured into a CUDA graph. */
 int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, void *out,
               tsx_stream_t stream);
 
