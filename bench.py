@@ -73,7 +73,11 @@ def parse_args(argv=None):
                         "workload's own plan bit for bit, and print one JSON line per candidate, fastest first")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-second", action="store_true",
+                   help="skip the second stated bar (bf16 exp over [16384, 16384] at stages 2, 3 and 4), which the "
+                        "default run times after the headline workload")
+    p.add_argument("--cpu-seconds", type=float, default=5.0,
+                   help="budget of the single-thread oracle timing")
     return p.parse_args(argv)
 
 
@@ -170,74 +174,112 @@ def recorded_traffic(workload: str, variant: str, stages: int):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """SM clock and clock-event reasons of this process's GPU while timed
+    regions run, read on a background thread about every half millisecond
+    through NVML's read-only queries (nvmlDeviceGetClockInfo,
+    nvmlDeviceGetCurrentClocksEventReasons).  Nothing is set.  Samples keep
+    their host time, so each timed region takes its own (``region``)."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits that matter for a timing
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.0005
 
-    def __init__(self, gpu_index: int):
-        self.gpu_index = gpu_index
-        self.proc = None
-        self.lines = []
-        self.reader = None
+    def __init__(self, device_index: int, uuid: str | None = None):
+        self.device_index = device_index
+        self.uuid = uuid
+        self.samples = []          # (host time, sm MHz, reason bits)
+        self.sm_max = None
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+
+    def _open(self):
+        import ctypes
+
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError as e:
+            self.error = f"NVML unavailable: {e}"
+            return False
+        if nv.nvmlInit_v2() != 0:
+            self.error = "nvmlInit failed"
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            u = self.uuid if self.uuid.startswith("GPU-") else "GPU-" + self.uuid
+            ok = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.device_index), ctypes.byref(h)) == 0
+        if not ok:
+            self.error = "no NVML handle for the device"
+            return False
+        self._nvml, self._handle = nv, h
+        mhz = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mhz)) == 0:   # NVML_CLOCK_SM
+            self.sm_max = float(mhz.value)
+        self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        return True
+
+    def _read_one(self):
+        import ctypes
+
+        mhz = ctypes.c_uint()
+        bits = ctypes.c_ulonglong()
+        if self._nvml.nvmlDeviceGetClockInfo(self._handle, ctypes.c_int(1), ctypes.byref(mhz)) != 0:
+            return None
+        if self._reasons_fn is None or self._reasons_fn(self._handle, ctypes.byref(bits)) != 0:
+            bits.value = 0
+        return float(mhz.value), int(bits.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self._read_one()
+            if r is not None:
+                self.samples.append((time.monotonic(), r[0], r[1]))
+            time.sleep(self.PERIOD_S)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-            return
-        self.reader = threading.Thread(target=self._read, daemon=True)
-        self.reader.start()
-        time.sleep(0.6)
+        if self._open():
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.monotonic(), line.strip()))
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        if self._nvml is not None:
+            self._nvml.nvmlShutdown()
+            self._nvml = None
 
-    def mark(self):
-        return time.monotonic()
+    def region(self, t0: float, t1: float) -> dict:
+        """Summary of the samples taken between host times t0 and t1."""
+        if self.error:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.error], "samples": 0, "source": "nvml"}
+        return summarise_clocks([(f, b) for t, f, b in list(self.samples) if t0 <= t <= t1], self.sm_max)
 
-    def stop(self, t0, t1):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, smax, reasons, n = [], None, set(), 0
-        for ts, line in self.lines:
-            if ts < t0 or ts > t1:
-                continue
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-            except ValueError:
-                continue
-            n += 1
-            for name, flag in zip(names, parts[5:9]):
-                if flag.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": n}
+
+def summarise_clocks(samples, sm_max) -> dict:
+    """Median SM MHz and the union of the throttle reasons over (MHz, reason
+    bits) samples."""
+    reasons = sorted({name for _, bits in samples for bit, name in ClockSampler.REASONS.items() if bits & bit})
+    mhz = [f for f, _ in samples]
+    return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": sm_max, "reasons": reasons,
+            "samples": len(mhz), "source": "nvml"}
 
 
 # --------------------------------------------------------------- our path
 
-def to_host_tensors(w, torch):
-    """The workload's inputs as pinned host tensors of the element type."""
+def to_host_tensors(w, torch, ins=None):
+    """The workload's inputs (element bits; generated unless given) as pinned
+    host tensors of the element type."""
     out = []
-    for bits in w.inputs():
+    for bits in (w.inputs() if ins is None else ins):
         if w.dtype == "f32":
             t = torch.from_numpy(bits.view(np.float32))
         else:
@@ -277,31 +319,18 @@ def step_bytes(w, mode: str) -> int:
     return w.algorithmic_bytes
 
 
-def run_ours(args, w, stages, variant):
-    import torch
-
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    td = init_dist(world, "nccl")
-    import pipelined_elementwise_streaming_gb300 as tsx
-
-    host = to_host_tensors(w, torch)
-    dev_in = [h.to("cuda", non_blocking=False) for h in host]
-    out = torch.zeros_like(dev_in[0])
-    row_sums = torch.empty(w.rows, dtype=torch.float32, device="cuda")
-    mode = args.mode
+def time_steps(torch, tsx, w, plan, mode, dev_in, out, row_sums, K, W, sampler):
+    """W untimed then K timed steps of one plan on the current stream, each
+    bracketed by CUDA events on that stream.  Inputs larger than L2 run back
+    to back; smaller ones get an L2 flush before every step and only the
+    kernels are counted.  Returns the timing record."""
     nbytes = step_bytes(w, mode)
-    plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant)
-    info = plan.info(w.op, row_sums=mode == "rowsum")
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))
     po = out.data_ptr()
     small = nbytes < 4 * L2_BYTES
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
-
-    ceiling = memcpy_ceiling(torch)
-
     op_code = tsx.OPS[w.op] | (tsx.TSX_ACCUMULATE if mode == "accumulate" else 0)
 
     def step():
@@ -312,23 +341,17 @@ def run_ours(args, w, stages, variant):
         else:
             plan.ewise_ptr(op_code, ptrs[0], ptrs[1], ptrs[2], po, sh)
 
-    for _ in range(args.warmup):
+    for _ in range(W):
         if flush is not None:
             flush.zero_()
         step()
     torch.cuda.synchronize()
     if plan.status() != tsx.TSX_OK:
         raise RuntimeError("device-side wait gave up during warm-up")
-
-    sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    barrier(td)
+    region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_wall0 = time.monotonic()
-    region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     region0.record(stream)
     for k in range(K):
         if flush is not None:
@@ -338,21 +361,106 @@ def run_ours(args, w, stages, variant):
         ev[k][1].record(stream)
     region1.record(stream)
     torch.cuda.synchronize()
-    barrier(td)
     t_wall1 = time.monotonic()
-    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
     if plan.status() != tsx.TSX_OK:
         raise RuntimeError("device-side wait gave up in the timed region")
-
     launch_s = [a.elapsed_time(b) / 1e3 for a, b in ev]
     kernel_total = sum(launch_s)
     region_s = region0.elapsed_time(region1) / 1e3
-    step_s = kernel_total if small else region_s   # with flushes, only the kernels are counted
-    max_s, total_bytes = aggregate(td, step_s, float(nbytes) * K)
-    value = total_bytes / max_s / 1e9
-    avg_launch = kernel_total / K
-    achieved = nbytes / avg_launch / 1e9
+    return {"nbytes": nbytes, "small": small, "launch_s": launch_s, "kernel_total": kernel_total,
+            "step_s": kernel_total if small else region_s, "K": K,
+            "clocks": sampler.region(t_wall0, t_wall1) if sampler else None}
+
+
+def roofline_of(t, peak, peak_kind, traffic, kernel):
+    avg_launch = t["kernel_total"] / t["K"]
+    achieved = t["nbytes"] / avg_launch / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+            "traffic": traffic, "kernel": kernel, "median_launch_ms": round(statistics.median(t["launch_s"]) * 1e3, 5)}
+
+
+def device_bits(torch, t):
+    """A CUDA tensor's element bits as a host numpy array."""
+    if t.element_size() == 2:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+# The second stated bar: bf16 exp over [16384, 16384] (box 128x128 as two
+# 128x64 loads), timed at each of its stated stage counts after the headline.
+SECOND_WORKLOAD = "exp_16384x16384_bf16"
+
+
+def run_second(args, torch, tsx, sampler, peak, peak_kind):
+    """The second bar workload at every stated stage count: its own timing,
+    roofline and memcpy ceiling, and its output kept for the oracle check."""
+    w = ti.WORKLOADS[SECOND_WORKLOAD]
+    ins = w.inputs()
+    dev_in = [h.to("cuda") for h in to_host_tensors(w, torch, ins)]
+    out = torch.zeros_like(dev_in[0])
+    ceiling = memcpy_ceiling(torch)
+    per_stage = {}
+    outputs = {}
+    for S in w.stages:
+        plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=S, variant=w.variant)
+        info = plan.info(w.op)
+        out.zero_()
+        t = time_steps(torch, tsx, w, plan, "ewise", dev_in, out, None, args.steps, args.warmup, sampler)
+        plan.close()
+        value = t["nbytes"] * t["K"] / t["step_s"] / 1e9
+        outputs[S] = device_bits(torch, out)
+        per_stage[str(S)] = {
+            "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(t["step_s"] / t["K"] * 1e3, 5),
+            "steps": t["K"], "gpu_launches": t["K"], "frac_of_memcpy_ceiling": round(value / ceiling, 4),
+            "threads": info["threads"], "grid": info["grid"], "ctas_per_sm": info["ctas_per_sm"],
+            "roofline": roofline_of(t, peak, peak_kind, recorded_traffic(w.name, w.variant, S),
+                                    f"tma_ewise<{w.dtype},{w.op}>"),
+            "clocks": t["clocks"],
+        }
+    del dev_in, out
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "op": w.op, "dtype": w.dtype, "rows": w.rows, "cols": w.cols,
+            "box": [w.box_rows, w.box_cols], "loads_per_operand": 2, "variant": w.variant,
+            "algorithmic_bytes_per_step": w.algorithmic_bytes, "memcpy_ceiling_gbs": round(ceiling, 1),
+            "l2": f"inputs larger than L2 ({w.algorithmic_bytes >> 20} MiB moved per step vs 129 MiB L2), "
+                  "steps back to back",
+            "stages": per_stage}, (ins, outputs)
+
+
+def run_ours(args, w, stages, variant):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    td = init_dist(world, "nccl")
+    import pipelined_elementwise_streaming_gb300 as tsx
+
+    ins = w.inputs()
+    host = to_host_tensors(w, torch, ins)
+    dev_in = [h.to("cuda", non_blocking=False) for h in host]
+    out = torch.zeros_like(dev_in[0])
+    row_sums = torch.empty(w.rows, dtype=torch.float32, device="cuda")
+    mode = args.mode
+    plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant)
+    info = plan.info(w.op, row_sums=mode == "rowsum")
     peak, peak_kind = measured_peak()
+    sampler = None
+    if rank == 0:
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(local).uuid)
+        except Exception:
+            pass
+        sampler = ClockSampler(local, uuid).start()
+
+    ceiling = memcpy_ceiling(torch)
+    barrier(td)
+    t = time_steps(torch, tsx, w, plan, mode, dev_in, out, row_sums, args.steps, args.warmup, sampler)
+    barrier(td)
+    nbytes, K = t["nbytes"], t["K"]
+    max_s, total_bytes = aggregate(td, t["step_s"], float(nbytes) * K)
+    value = total_bytes / max_s / 1e9
 
     # end to end: pinned host inputs in, host result out, every step
     E = max(1, args.e2e_steps)
@@ -375,12 +483,18 @@ def run_ours(args, w, stages, variant):
     else:
         e2e = {"value": None, "unit": "GB/s", "note": f"the end-to-end leg runs in ewise mode only, not {mode}"}
     plan.close()
-    # the first rows of the device result, for the oracle's check in the
+    # the whole device result of the timed steps, for the oracle check in the
     # CPU-baseline leg (ewise mode: out holds op(inputs) exactly once)
-    head = None
-    if mode == "ewise":
-        band = oracle_band_rows(w)
-        head = out[:band].contiguous().view(torch.int16 if ti.ELEM_SIZE[w.dtype] == 2 else torch.int32).cpu().numpy()
+    result_bits = device_bits(torch, out) if mode == "ewise" else None
+    del dev_in, out, host
+    torch.cuda.empty_cache()
+
+    second, second_out = None, None
+    if (rank == 0 and not args.no_second and mode == "ewise" and w.name == DEFAULT_WORKLOAD and args.rows is None
+            and args.box is None and args.op is None):
+        second, second_out = run_second(args, torch, tsx, sampler, peak, peak_kind)
+    if sampler:
+        sampler.stop()
 
     result = {
         "metric": METRIC,
@@ -389,18 +503,19 @@ def run_ours(args, w, stages, variant):
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": round(step_s / K * 1e3, 5),
+        "ms_per_step": round(t["step_s"] / K * 1e3, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": DTYPE_NAME[w.dtype],
         "data": "synthetic (seeded SplitMix64 inputs, the workload's stated distribution)",
         "config": {
-            "workload": w.name + ("" if args.rows is None else f" (first {w.rows} rows)"), "op": w.op, "rows": w.rows, "cols": w.cols, "box": [w.box_rows, w.box_cols],
+            "workload": w.name + ("" if args.rows is None else f" (first {w.rows} rows)"), "op": w.op, "rows": w.rows,
+            "cols": w.cols, "box": [w.box_rows, w.box_cols],
             "stages": stages, "variant": variant, "threads": info["threads"], "grid": info["grid"],
             "ctas_per_sm": info["ctas_per_sm"], "loads_per_operand": info["loads_per_operand"],
             "mode": mode, "algorithmic_bytes_per_step": nbytes,
-            "l2": "L2 flushed between timed steps (kernel time only)" if small
+            "l2": "L2 flushed between timed steps (kernel time only)" if t["small"]
                   else f"inputs larger than L2 ({nbytes >> 20} MiB moved per step vs 129 MiB L2), "
                        "steps back to back",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -409,19 +524,18 @@ def run_ours(args, w, stages, variant):
         },
         "memcpy_ceiling_gbs": round(ceiling, 1),
         "frac_of_memcpy_ceiling": round(value / world / ceiling, 4),
-        "clocks": clocks,
+        "clocks": t["clocks"],
         "e2e": e2e,
         "gpu_launches": K,
-        "roofline": {
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-            "traffic": recorded_traffic(w.name, variant, stages) if mode == "ewise" else None,
-            "kernel": (f"tma_rowsum<{w.dtype},{w.op}>" if mode == "rowsum" else
-                       f"tma_ewise<{w.dtype},{w.op}>" if variant.startswith("tma") else f"{variant}_ewise"),
-            "median_launch_ms": round(statistics.median(launch_s) * 1e3, 5),
-        },
+        "roofline": roofline_of(t, peak, peak_kind,
+                                recorded_traffic(w.name, variant, stages) if mode == "ewise" else None,
+                                f"tma_rowsum<{w.dtype},{w.op}>" if mode == "rowsum" else
+                                f"tma_ewise<{w.dtype},{w.op}>" if variant.startswith("tma") else f"{variant}_ewise"),
     }
-    result["_device_head"] = head
+    if second is not None:
+        result["workloads"] = {second["workload"]: second}
+    result["_check"] = (ins, result_bits) if result_bits is not None else None
+    result["_second_out"] = second_out
     return result, td, rank
 
 
@@ -538,65 +652,80 @@ def run_e2e(torch, tsx, w, stages, variant, host, dev_in, out, steps, td, band_b
 
 # ------------------------------------------------------------ the oracle
 
-def oracle_band_rows(w) -> int:
-    """Rows per band of the CPU-baseline leg (about 4 Mi elements)."""
-    return max(1, min(w.rows, (1 << 22) // w.cols or 1))
-
-
-def cpu_time_oracle(w, seconds_budget, start_row=0, max_rows=None, first=None):
-    """Run the oracle over row bands of the workload until the budget is
-    spent or the rows run out.  Returns (bytes, seconds, rows, cores); the
-    first band's result goes to first[0] when a list is given."""
+def oracle_single_core(w, ins, seconds_budget, band_elems=1 << 22):
+    """The oracle on one host thread over leading bands of the workload's
+    inputs until the budget is spent.  Returns (bytes, seconds, elements)."""
     import oracle
 
-    oracle.build()
-    rows_done, spent, nbytes = 0, 0.0, 0
-    band = oracle_band_rows(w)
-    r = start_row
-    limit = w.rows if max_rows is None else min(w.rows, start_row + max_rows)
-    while r < limit and spent < seconds_budget:
-        r1 = min(limit, r + band)
-        idx = np.arange(r * w.cols, r1 * w.cols, dtype=np.uint64)
-        ins = w.inputs_at(idx)
+    flat = [x.reshape(-1) for x in ins]
+    n, spent, done = flat[0].size, 0.0, 0
+    while done < n and spent < seconds_budget:
+        e = min(n, done + band_elems)
         t0 = time.perf_counter()
-        res = oracle.ewise(w.op, w.dtype, *ins)
+        oracle.ewise(w.op, w.dtype, *[x[done:e] for x in flat])
         spent += time.perf_counter() - t0
-        if first is not None and not first:
-            first.append(res)
-        nbytes += (w.n_in + 1) * idx.size * ti.ELEM_SIZE[w.dtype]
-        rows_done += r1 - r
-        r = r1
-    return nbytes, spent, rows_done, 1
+        done = e
+    return (w.n_in + 1) * done * ti.ELEM_SIZE[w.dtype], spent, done
 
 
-def cpu_baseline(w, seconds, device_head=None):
-    """The oracle's throughput on the host; with the device result's first
-    rows, also the element-by-element check of those rows against the
-    oracle's (bit-exact, or the exp ulp bound)."""
+def oracle_check(w, ins, device_out, cores):
+    """The oracle over the whole workload on every host core, timed, and the
+    device output compared with it element by element under the parity rule
+    (bit-exact; exp within its ulp bound).  Returns (oracle seconds, oracle
+    bits, parity record)."""
     import oracle
 
-    first = []
-    nbytes, spent, rows, cores = cpu_time_oracle(w, seconds, first=first)
-    base = {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of {w.name} ({rows * w.cols} elements), single-threaded C oracle, "
-                      f"{spent:.1f} s of CPU time"}
+    t0 = time.perf_counter()
+    want = oracle.ewise_parallel(w.op, w.dtype, *ins, threads=cores)
+    seconds = time.perf_counter() - t0
     parity = None
-    if device_head is not None and first:
-        bits = np.dtype(np.uint16 if ti.ELEM_SIZE[w.dtype] == 2 else np.uint32)
-        got = device_head.reshape(-1).view(bits)
-        want = np.asarray(first[0]).reshape(-1).view(bits)[: got.size]
-        if w.op == "exp":
-            bad = int(np.count_nonzero(oracle.ulp_distance(got, want, w.dtype) > oracle.EXP_ULP_BOUND[w.dtype]))
-            rule = f"within {oracle.EXP_ULP_BOUND[w.dtype]} ulp"
-        elif w.op == "copy":
-            bad = int(np.count_nonzero(got != want))
-            rule = "bitwise"
-        else:
-            bad = int(np.count_nonzero(~oracle.same_value(got, want, w.dtype)))
-            rule = "bit-exact"
-        parity = {"elements": int(got.size), "mismatches": bad, "rule": rule, "against": "oracle",
-                  "rows": f"0..{device_head.shape[0] - 1} of the timed steps' output"}
+    if device_out is not None:
+        parity = parity_record(w, device_out, want, cores)
+    return seconds, want, parity
+
+
+def parity_record(w, device_out, want, cores):
+    import oracle
+
+    bad, first = oracle.count_mismatches(w.op, w.dtype, device_out, want, cores)
+    rule = (f"within {oracle.EXP_ULP_BOUND[w.dtype]} ulp" if w.op == "exp" else
+            "bitwise" if w.op == "copy" else "bit-exact")
+    rec = {"elements": int(np.asarray(device_out).size), "mismatches": bad, "rule": rule, "against": "oracle",
+           "rows": f"all {w.rows} rows of the timed steps' output"}
+    if bad:
+        rec["first_mismatch_flat_index"] = first
+    return rec
+
+
+def cpu_baseline(w, ins, device_out, seconds, cores=None):
+    """The oracle's throughput on the host (all cores over the whole workload,
+    and one core over a bounded sample) and, with the device output, the
+    element-by-element check of all of it against the oracle's."""
+    import oracle
+
+    cores = cores or oracle.host_cores()
+    oracle.build()
+    all_s, _, parity = oracle_check(w, ins, device_out, cores)
+    nbytes = w.algorithmic_bytes
+    one_bytes, one_s, one_elems = oracle_single_core(w, ins, seconds)
+    base = {"value": round(nbytes / all_s / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"all {w.elems} elements of {w.name}, C oracle cut into element ranges over {cores} host "
+                      f"threads, {all_s:.2f} s wall",
+            "single_core": {"value": round(one_bytes / one_s / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"the first {one_elems} elements of {w.name}, one thread, {one_s:.1f} s"}}
     return base, parity
+
+
+def second_checks(args, second, second_data, cores):
+    """Oracle timing and full parity of the second bar workload's outputs."""
+    w = ti.WORKLOADS[second["workload"]]
+    ins, outputs = second_data
+    all_s, want, _ = oracle_check(w, ins, None, cores)
+    second["cpu_baseline"] = {"value": round(w.algorithmic_bytes / all_s / 1e9, 4), "unit": "GB/s", "cores": cores,
+                              "kind": "oracle",
+                              "sample": f"all {w.elems} elements, C oracle over {cores} host threads, {all_s:.2f} s"}
+    for S, bits in outputs.items():
+        second["stages"][str(S)]["parity"] = parity_record(w, bits, want, cores)
 
 
 SWEEP_BOXES = [(8, 128), (16, 128), (32, 128), (64, 128), (128, 128), (8, 256), (32, 256), (64, 64), (128, 64),
@@ -607,8 +736,6 @@ def run_sweep(args, w, stages, variant):
     """Time every accepted (box, stages, threads) candidate of the workload's
     op and variant; each candidate's output must equal the workload's own
     plan's output bit for bit.  Returns the result lines, fastest first."""
-    import os as _os
-
     import torch
 
     import pipelined_elementwise_streaming_gb300 as tsx
@@ -626,80 +753,77 @@ def run_sweep(args, w, stages, variant):
     K = max(20, min(args.steps, 200))
     lines = []
     seen = set()
-    saved = _os.environ.get("TSX_THREADS")
-    try:
-        for box in SWEEP_BOXES:
-            for st in (2, 3, 4, 6):
-                for threads in (None, 128, 256):
-                    if threads is None:
-                        _os.environ.pop("TSX_THREADS", None)
-                    else:
-                        _os.environ["TSX_THREADS"] = str(threads)
-                    try:
-                        plan = tsx.Plan(w.dtype, w.rows, w.cols, box=box, stages=st, variant=variant)
-                        info = plan.info(w.op)
-                    except tsx.TsxError:
-                        continue
-                    key = (box, st, info["threads"])
-                    if (threads is not None and info["threads"] != threads) or key in seen:
-                        plan.close()
-                        continue
-                    seen.add(key)
-                    out.zero_()
-                    for _ in range(3):
-                        plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record()
-                    for _ in range(K):
-                        plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
-                    e1.record()
-                    torch.cuda.synchronize()
-                    ok = plan.status() == tsx.TSX_OK and torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+    for box in SWEEP_BOXES:
+        for st in (2, 3, 4, 6):
+            for threads in (None, 128, 256):
+                tuning = None if threads is None else {"threads": threads}
+                try:
+                    plan = tsx.Plan(w.dtype, w.rows, w.cols, box=box, stages=st, variant=variant, tuning=tuning)
+                    info = plan.info(w.op)
+                except tsx.TsxError:
+                    continue
+                key = (box, st, info["threads"])
+                if key in seen:
                     plan.close()
-                    sec = e0.elapsed_time(e1) / 1e3 / K
-                    lines.append({"sweep": w.name, "op": w.op, "variant": variant, "box": list(box), "stages": st,
-                                  "threads": info["threads"], "grid": info["grid"], "gbs": round(nbytes / sec / 1e9, 1),
-                                  "same_as_workload_plan": bool(ok)})
-    finally:
-        if saved is None:
-            _os.environ.pop("TSX_THREADS", None)
-        else:
-            _os.environ["TSX_THREADS"] = saved
+                    continue
+                seen.add(key)
+                out.zero_()
+                for _ in range(3):
+                    plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(K):
+                    plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
+                e1.record()
+                torch.cuda.synchronize()
+                ok = plan.status() == tsx.TSX_OK and torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+                plan.close()
+                sec = e0.elapsed_time(e1) / 1e3 / K
+                lines.append({"sweep": w.name, "op": w.op, "variant": variant, "box": list(box), "stages": st,
+                              "threads": info["threads"], "grid": info["grid"], "gbs": round(nbytes / sec / 1e9, 1),
+                              "same_as_workload_plan": bool(ok)})
     lines.sort(key=lambda d: -d["gbs"])
     return lines
 
 
 def run_reference(args, w, stages, variant):
+    """The reference arm: the oracle, as it stands, on the host's cores.  Each
+    step is one bounded contiguous sample of the workload at a random offset,
+    cut into element ranges over every host core; one more sample is timed on
+    a single thread for scale."""
     world, rank, _ = dist_env()
     if rank != 0:
         return None
-    K, W = args.steps, args.warmup
-    # size each step so the whole run, input generation included, stays
-    # within about a minute (at most 2 s a step)
-    per_step_budget = min(2.0, max(1e-3, 60.0 / max(1, K + W)))
     import oracle
 
+    K, W = args.steps, args.warmup
+    cores = oracle.host_cores()
     oracle.build()
     probe = np.arange(0, min(w.elems, 1 << 16), dtype=np.uint64)
-    t0 = time.perf_counter()
     ins = w.inputs_at(probe)
+    t0 = time.perf_counter()
     oracle.ewise(w.op, w.dtype, *ins)
     per_elem = (time.perf_counter() - t0) / probe.size
-    n = int(max(1024, min(w.elems, 1 << 24, per_step_budget / max(per_elem, 1e-10))))
+    # about 1 s of single-thread oracle work per step (input generation comes
+    # on top), at most 2^24 elements: the whole run stays within a few minutes
+    n = int(max(1024, min(w.elems, 1 << 24, 1.0 / max(per_elem, 1e-10))))
     rng = np.random.default_rng(0)
     total_bytes, total_s = 0, 0.0
     for k in range(W + K):
         start = int(rng.integers(0, max(1, w.elems - n)))
-        idx = np.arange(start, start + n, dtype=np.uint64)
-        x = w.inputs_at(idx)
+        x = w.inputs_range(start, n)
         t0 = time.perf_counter()
-        oracle.ewise(w.op, w.dtype, *x)
+        oracle.ewise_parallel(w.op, w.dtype, *x, threads=cores)
         dt = time.perf_counter() - t0
         if k >= W:
             total_s += dt
             total_bytes += (w.n_in + 1) * n * ti.ELEM_SIZE[w.dtype]
     value = total_bytes / total_s / 1e9
-    sample = f"{n} contiguous elements of {w.name} per step (random offset), single-threaded C oracle"
+    t0 = time.perf_counter()
+    oracle.ewise(w.op, w.dtype, *x)
+    one = (w.n_in + 1) * n * ti.ELEM_SIZE[w.dtype] / (time.perf_counter() - t0) / 1e9
+    sample = (f"{n} contiguous elements of {w.name} per step (random offset), C oracle cut into element ranges "
+              f"over {cores} host threads")
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(total_s / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
@@ -707,7 +831,9 @@ def run_reference(args, w, stages, variant):
         "config": {"workload": w.name, "op": w.op, "rows": w.rows, "cols": w.cols,
                    "box": [w.box_rows, w.box_cols], "stages": stages, "variant": variant},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "single_core": {"value": round(one, 4), "unit": "GB/s", "cores": 1,
+                                         "sample": f"one more sample of {n} elements on one thread"}},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -737,12 +863,22 @@ def main(argv=None):
             print(json.dumps(res), flush=True)
         return 0
     res, td, rank = run_ours(args, w, stages, variant)
-    head = res.pop("_device_head", None)
+    check = res.pop("_check", None)
+    second_data = res.pop("_second_out", None)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, head)
+            import oracle
+
+            cores = oracle.host_cores()
+            if check is not None:
+                ins, device_out = check
+            else:
+                ins, device_out = w.inputs(), None
+            res["cpu_baseline"], parity = cpu_baseline(w, ins, device_out, args.cpu_seconds, cores)
             if parity is not None:
                 res["parity"] = parity
+            if second_data is not None:
+                second_checks(args, res["workloads"][SECOND_WORKLOAD], second_data, cores)
         print(json.dumps(res), flush=True)
     barrier(td)
     if td is not None:

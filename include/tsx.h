@@ -150,10 +150,48 @@ typedef struct tsx_plan_info {
     /* element size the tensor map counts in: elem_size, or the wider one
      * of TSX_TMA_PROMOTED */
     int32_t tma_elem_bytes;
+    /* TMA variants: tiles between a store's issue and the release of its
+     * stage (the store warp checks cp.async.bulk.wait_group.read that many
+     * tiles later) */
+    int32_t store_lag;
+    /* limit of every device-side wait, in milliseconds */
+    int32_t timeout_ms;
 } tsx_plan_info;
+
+/* Launch knobs of a plan.  Every field has a "planner's choice" value; start
+ * from tsx_tuning_defaults() and set only what you want to force.  None of
+ * them changes a result: the tests hold every setting to the oracle.
+ *  threads       compute threads of a CTA ([outer, threads, vec]: the
+ *                partition the TVM docs "elementwise -> smem" page
+ *                synthesizes from the thread count, "Algorithm" step 2); a
+ *                multiple of 32; <= 0: the planner's choice
+ *  ctas_per_sm   at most this many resident CTAs per SM in the persistent
+ *                grid; <= 0: as many as occupancy allows
+ *  store_lag     TMA variants: 0..3 tiles between a store's issue and the
+ *                release of its stage; < 0: the planner's (1, or 2 from six
+ *                stages on)
+ *  l2_promotion  CUtensorMapL2promotion of the tensor maps, 0..3 (none, 64,
+ *                128, 256 B); < 0: 128 B, the value of TVM docs
+ *                "copy_async -> tma" ("Generated TIRx IR")
+ *  timeout_ms    limit of every device-side wait; <= 0: 1000
+ *  checked       non-zero: tsx_ewise / tsx_reduce_rows synchronize the
+ *                stream and return the device status (debugging) */
+typedef struct tsx_tuning {
+    int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked;
+} tsx_tuning;
+
+/* Fill *t with the planner's-choice value of every field.  No source on the
+ * pages: the knobs are this library's (the measurement side of its spec
+ * chooses stage count and box shape from counters; these are the rest). */
+void tsx_tuning_defaults(tsx_tuning *t);
 
 /* Create a plan for [rows, cols] tensors of `dtype`, streamed in stage
  * tiles of box_rows x box_cols through `stages` stages by `variant`.
+ * Source: the library's specified call list (the pages describe a DSL, not a
+ * library); what the plan fixes is the host side of TVM docs
+ * "copy_async -> tma", "Algorithm" steps 2-3 (encode the descriptor once on
+ * the host) and nvFuser PR #2833 "Lowering Details" (box <= 256, loads per
+ * stage, expect_tx bytes).
  * Binds the plan to the current CUDA device and allocates one 4-byte device
  * status word.  rows or cols may be 0 (every call is then a no-op).
  * Limits: rows, cols < 2^31; 1 <= stages <= 16; box dims >= 1; TMA variants
@@ -174,8 +212,19 @@ tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_
 tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
                                    int box_cols, int stages, tsx_variant variant);
 
+/* tsx_plan_create_pitched with launch knobs (see tsx_tuning; NULL: every
+ * field the planner's choice).  Out-of-range knobs give NULL with
+ * TSX_ERR_INVALID in tsx_last_error(). */
+tsx_plan_t tsx_plan_create_tuned(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                 int box_cols, int stages, tsx_variant variant, const tsx_tuning *tuning);
+
 /* out = op(a, b, c) element by element over the plan's [rows, cols]
- * (out += op(a, b, c) with TSX_ACCUMULATE).
+ * (out += op(a, b, c) with TSX_ACCUMULATE).  Source: the library's specified
+ * call list; the operation is TVM docs "copy_async -> tma" ("Algorithm"
+ * steps 2-4: load a tile to shared memory, signal an mbarrier) with the op
+ * applied in shared memory as in TVM docs "elementwise -> smem"
+ * ("Algorithm", "Generated CUDA"), pipelined over tiles as in nvFuser PR
+ * #2833 ("Loop Structure", "Detailed Pseudo-Code").
  * a is required; b is required by add / mul / fma and must be NULL
  * otherwise; c is required by fma and must be NULL otherwise (else
  * TSX_ERR_INVALID).  out may be exactly a, b or c; any other overlap is
@@ -189,10 +238,11 @@ tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, 
  * TSX_LDGSTS / TSX_SYNC narrow their copy width to the pointers' alignment
  * (16, 8 or 4 bytes) and return TSX_ERR_ALIGN below 4.
  * Asynchronous on `stream`: returns once the kernel is queued.  A device-side
- * wait that exceeds its time limit (default 1 s, env TSX_TIMEOUT_MS) makes
- * the kernel record TSX_ERR_TIMEOUT in the plan's status word and return;
- * read it with tsx_plan_status.  With env TSX_CHECKED=1 the call
- * synchronizes the stream and returns the device status instead.  After a
+ * wait that exceeds its time limit (1 s unless tsx_tuning.timeout_ms says
+ * otherwise) makes the kernel record TSX_ERR_TIMEOUT in the plan's status
+ * word and return; read it with tsx_plan_status.  On a plan created with
+ * tsx_tuning.checked the call synchronizes the stream and returns the
+ * device status instead.  After a
  * plan's first call of an op (which sets up its launch) later calls of that
  * op only launch on `stream`, so they can be captured into a CUDA graph. */
 int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, void *out,
@@ -221,18 +271,24 @@ int tsx_reduce_rows(tsx_plan_t plan, tsx_op op, const void *a, const void *b, co
                     tsx_stream_t stream);
 
 /* Release the plan, its tensor-map cache and its device status word.
- * NULL is ignored.  Work already queued must not need the plan's status
+ * Source: the library's specified call list (no counterpart on the pages;
+ * the post-epilogue's mbarrier.inval of nvFuser PR #2833 "Loop Structure"
+ * is the device-side release, done by every launch).  NULL is ignored.  Work already queued must not need the plan's status
  * word afterwards (synchronize first). */
 void tsx_plan_destroy(tsx_plan_t plan);
 
 /* The first device-side error recorded by this plan's kernels since the
- * last call (TSX_OK if none), then clears it.  Call after synchronizing the
+ * last call (TSX_OK if none), then clears it.  Source: the library's
+ * specified call list; the pages have no error path (TVM docs
+ * "copy_async -> tma" only says a variant declines, closing paragraph), so
+ * the bounded mbarrier waits and this status word are this library's.  Call after synchronizing the
  * streams the plan was used on; this call itself blocks on a small
  * device-to-host copy. */
 int tsx_plan_status(tsx_plan_t plan);
 
 /* Message for the last error on the calling host thread ("" if none).  The
- * pointer stays valid until the next tsx_* call on this thread. */
+ * pointer stays valid until the next tsx_* call on this thread.  Source: the
+ * library's specified call list (no counterpart on the pages). */
 const char *tsx_last_error(void);
 
 /* The plan tsx_plan_create would build and the launch tsx_ewise would make
@@ -246,6 +302,11 @@ int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, in
 /* tsx_plan_query for rows `pitch` elements apart (see tsx_plan_create_pitched). */
 int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols,
                            int stages, tsx_variant variant, tsx_op op, tsx_plan_info *info);
+
+/* tsx_plan_query_pitched for a plan created with these launch knobs (NULL:
+ * the planner's choices; ctas_per_sm does not show, as no GPU is looked at). */
+int tsx_plan_query_tuned(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols,
+                         int stages, tsx_variant variant, const tsx_tuning *tuning, tsx_op op, tsx_plan_info *info);
 
 /* tsx_plan_query for an existing plan, including the launch it makes on its
  * device (occupancy-derived CTAs per SM and grid).  Both accept an op with
@@ -271,8 +332,9 @@ int tsx_plan_get_info(tsx_plan_t plan, tsx_op op, tsx_plan_info *info);
  *
  * Scratch: the kernel's device status word lives in a file-scope device
  * array of 256 bytes, which every GPU that loads the library holds until the
- * process exits; a call needs 4 bytes of it, and a call that needed more
- * would be rejected with TSX_ERR_UNSUPPORTED.  The first call on each device
+ * process exits; a call needs 4 bytes of it (the library checks that at
+ * compile time, so no call is ever turned away for size).  Device-side waits
+ * are bounded by 1 s.  The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  Every
  * call on a device shares the array: each call clears the status word on
@@ -283,7 +345,10 @@ int tsx_plan_get_info(tsx_plan_t plan, tsx_op op, tsx_plan_info *info);
  * Returns once the work is queued on `stream`, or an error code for a
  * host-side / launch failure (tsx_last_error() says why).  If `status_out`
  * is not NULL the call also waits for `stream` and stores the device status
- * there (TSX_OK, or TSX_ERR_TIMEOUT if a device-side wait gave up). */
+ * there (TSX_OK, or TSX_ERR_TIMEOUT if a device-side wait gave up), reading
+ * it in stream order (cudaMemcpyAsync on `stream`, then a synchronisation
+ * of that stream alone).  *status_out is written only by a call that got as
+ * far as its launch (or found the tensor empty). */
 int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
                       tsx_variant variant, tsx_op op, const void *a, const void *b, const void *c, void *out,
                       tsx_stream_t stream, int *status_out);

@@ -10,6 +10,8 @@ Contents
 * ``ewise``: the per-element definitions (C, ``tsx_oracle.c``), evaluated in
   fp64 and rounded once into the element type.
 * ``ulp_distance`` / ``same_value``: the comparisons the parity tests use.
+* ``ewise_parallel`` / ``count_mismatches``: the same routine and the same
+  comparisons, cut into ranges over every host core, for full-size checks.
 * ``structure``: the integer plans the pages fix -- the ``[outer, threads,
   vec]`` partition, the box split with its expect_tx bytes, the tensor-map
   arguments and the prologue / main / epilogue schedule.
@@ -86,11 +88,13 @@ def _bits(x: np.ndarray, dtype: str) -> np.ndarray:
     return x.view(want)
 
 
-def ewise(op: str, dtype: str, a, b=None, c=None) -> np.ndarray:
+def ewise(op: str, dtype: str, a, b=None, c=None, out=None) -> np.ndarray:
     """out = op(a[, b[, c]]) element by element; returns element bits.
 
     Operands are numpy arrays of element bits (``float32`` or ``uint32`` for
     fp32, ``uint16`` / ``float16`` for the 16-bit types), all the same shape.
+    ``out``, if given, is a contiguous array of that shape and element size
+    that receives the result (it is returned viewed as element bits).
     """
     arity = OP_ARITY[op]
     ops = [a, b, c][:arity]
@@ -100,12 +104,93 @@ def ewise(op: str, dtype: str, a, b=None, c=None) -> np.ndarray:
     ops = [_bits(o, dtype) for o in ops]
     if any(o.shape != shape for o in ops):
         raise ValueError("operand shapes differ")
-    out = np.empty(shape, dtype=NP_BITS[dtype])
+    if out is None:
+        out = np.empty(shape, dtype=NP_BITS[dtype])
+    else:
+        if out.shape != shape or not out.flags.c_contiguous:
+            raise ValueError("out must be a contiguous array of the operands' shape")
+        out = out.view(NP_BITS[dtype])
     ptrs = [o.ctypes.data for o in ops] + [None] * (3 - arity)
     rc = lib().tsxo_ewise(DTYPE_CODE[dtype], OP_CODE[op], int(out.size), *ptrs, out.ctypes.data)
     if rc != 0:
         raise RuntimeError("tsxo_ewise rejected its arguments")
     return out
+
+
+# --------------------------------------------------------------------------
+# Running the oracle on every host core
+# --------------------------------------------------------------------------
+
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _ranges(n: int, parts: int):
+    parts = max(1, min(parts, n)) if n else 1
+    return [(k * n // parts, (k + 1) * n // parts) for k in range(parts)]
+
+
+def ewise_parallel(op: str, dtype: str, a, b=None, c=None, threads: int | None = None, out=None) -> np.ndarray:
+    """``ewise`` with the elements cut into contiguous ranges, one call of the
+    same C routine per range on a pool of host threads (ctypes releases the
+    GIL for the call).  Elements are independent, so the result is the one
+    ``ewise`` gives; only the wall time changes."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    arity = OP_ARITY[op]
+    ops = [_bits(o, dtype).reshape(-1) for o in [a, b, c][:arity] if o is not None]
+    if len(ops) != arity:
+        raise ValueError(f"{op} takes exactly {arity} operand(s)")
+    shape = np.shape(a)
+    flat_out = np.empty(ops[0].size, dtype=NP_BITS[dtype]) if out is None else out.view(NP_BITS[dtype]).reshape(-1)
+    threads = threads or host_cores()
+    # ranges much smaller than the data so that uneven cores still finish together
+    parts = max(1, min(4 * threads, ops[0].size // (1 << 16) or 1))
+
+    def one(r):
+        s, e = r
+        ewise(op, dtype, *[o[s:e] for o in ops], out=flat_out[s:e])
+
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        list(pool.map(one, _ranges(ops[0].size, parts)))
+    return flat_out.reshape(shape)
+
+
+def count_mismatches(op: str, dtype: str, got, want, threads: int | None = None):
+    """Compare device bits with the oracle's under the parity rule of ``op``
+    (copy bitwise; exp within ``EXP_ULP_BOUND`` ulps; otherwise bit-exact with
+    NaN equal to NaN), in ranges on a pool of host threads.  Returns
+    ``(mismatches, first mismatching flat index or -1)``."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    g = np.asarray(got).reshape(-1).view(NP_BITS[dtype])
+    w = np.asarray(want).reshape(-1).view(NP_BITS[dtype])
+    if g.size != w.size:
+        raise ValueError("sizes differ")
+    threads = threads or host_cores()
+
+    def one(r):
+        s, e = r
+        x, y = g[s:e], w[s:e]
+        if op == "copy":
+            bad = x != y
+        elif op == "exp":
+            bad = ulp_distance(x, y, dtype) > EXP_ULP_BOUND[dtype]
+        else:
+            bad = ~same_value(x, y, dtype)
+        idx = np.flatnonzero(bad)
+        return int(idx.size), (s + int(idx[0])) if idx.size else -1
+
+    parts = max(1, min(4 * threads, g.size // (1 << 18) or 1))
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        res = list(pool.map(one, _ranges(g.size, parts)))
+    total = sum(n for n, _ in res)
+    first = next((f for n, f in res if n), -1)
+    return total, first
 
 
 def decode(bits: np.ndarray, dtype: str) -> np.ndarray:

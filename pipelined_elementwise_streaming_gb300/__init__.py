@@ -6,7 +6,7 @@ CPU fallback; importing this module fails loudly when the library is absent.
 
 The C functions are exposed under their own names (``tsx_plan_create``,
 ``tsx_ewise``, ``tsx_plan_destroy``, ``tsx_plan_status``, ``tsx_last_error``,
-``tsx_plan_query``, ``tsx_plan_get_info``) with plain-integer arguments;
+``tsx_plan_query``, ``tsx_plan_get_info``, ...) with plain-integer arguments;
 ``Plan`` wraps them for torch tensors::
 
     plan = Plan("bf16", rows, cols, box=(128, 128), stages=4, variant="tma")
@@ -54,7 +54,8 @@ class tsx_plan_info(ctypes.Structure):
                                                "threads", "vec", "outer", "copy_vec_bytes",
                                                "slot_bytes", "stage_bytes", "smem_bytes",
                                                "ctas_per_sm", "grid", "sm_count", "block_threads")] + \
-               [("pitch", ctypes.c_int64), ("tma_elem_bytes", ctypes.c_int32)]
+               [("pitch", ctypes.c_int64), ("tma_elem_bytes", ctypes.c_int32), ("store_lag", ctypes.c_int32),
+                ("timeout_ms", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {}
@@ -62,6 +63,12 @@ class tsx_plan_info(ctypes.Structure):
             v = getattr(self, name)
             d[name] = list(v) if hasattr(v, "__len__") else int(v)
         return d
+
+
+class tsx_tuning(ctypes.Structure):
+    """Launch knobs of a plan (include/tsx.h); see ``tuning()``."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("threads", "ctas_per_sm", "store_lag", "l2_promotion", "timeout_ms",
+                                               "checked")]
 
 
 def _load():
@@ -77,6 +84,15 @@ def _load():
     L.tsx_plan_create_pitched.restype = ctypes.c_void_p
     L.tsx_plan_create_pitched.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.tsx_plan_create_tuned.restype = ctypes.c_void_p
+    L.tsx_plan_create_tuned.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(tsx_tuning)]
+    L.tsx_plan_query_tuned.restype = ctypes.c_int
+    L.tsx_plan_query_tuned.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(tsx_tuning),
+                                       ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
+    L.tsx_tuning_defaults.restype = None
+    L.tsx_tuning_defaults.argtypes = [ctypes.POINTER(tsx_tuning)]
     L.tsx_plan_query_pitched.restype = ctypes.c_int
     L.tsx_plan_query_pitched.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -98,6 +114,12 @@ def _load():
     L.tsx_ewise_noalloc.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5 + \
                                    [ctypes.POINTER(ctypes.c_int)]
+    L.tsx_debug_plan_enable_trace.restype = ctypes.c_int
+    L.tsx_debug_plan_enable_trace.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    L.tsx_debug_plan_set_fault_tile.restype = ctypes.c_int
+    L.tsx_debug_plan_set_fault_tile.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+    L.tsx_debug_noalloc_set_fault.restype = None
+    L.tsx_debug_noalloc_set_fault.argtypes = [ctypes.c_int64, ctypes.c_int32]
     L.tsx_debug_trace.restype = ctypes.c_int
     L.tsx_debug_trace.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                   ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
@@ -109,6 +131,9 @@ lib = _load()
 # The C entry points under their own names (plain integers / addresses).
 tsx_plan_create = lib.tsx_plan_create
 tsx_plan_create_pitched = lib.tsx_plan_create_pitched
+tsx_plan_create_tuned = lib.tsx_plan_create_tuned
+tsx_plan_query_tuned = lib.tsx_plan_query_tuned
+tsx_tuning_defaults = lib.tsx_tuning_defaults
 tsx_plan_query_pitched = lib.tsx_plan_query_pitched
 tsx_ewise = lib.tsx_ewise
 tsx_plan_destroy = lib.tsx_plan_destroy
@@ -119,8 +144,12 @@ tsx_reduce_rows = lib.tsx_reduce_rows
 # The plan-free, allocation-free form of tsx_ewise (device status word in a
 # static device array; see include/tsx.h for who needs it and its limits).
 tsx_ewise_noalloc = lib.tsx_ewise_noalloc
-# Test hook (include/tsx_debug.h): the schedule trace of a traced launch.
+# Test hooks (include/tsx_debug.h): the schedule trace of traced launches and
+# the host-planted load skip that makes a bounded device-side wait run out.
 tsx_debug_trace = lib.tsx_debug_trace
+tsx_debug_plan_enable_trace = lib.tsx_debug_plan_enable_trace
+tsx_debug_plan_set_fault_tile = lib.tsx_debug_plan_set_fault_tile
+tsx_debug_noalloc_set_fault = lib.tsx_debug_noalloc_set_fault
 
 
 def tsx_last_error() -> str:
@@ -131,11 +160,31 @@ def _code(table: dict, key) -> int:
     return table[key] if isinstance(key, str) else int(key)
 
 
-def query(dtype, rows, cols, box, stages, variant="tma", op="copy", pitch=None) -> dict:
-    """The plan and launch shape the library would use (host only, no GPU)."""
+def tuning(**knobs) -> tsx_tuning:
+    """A tsx_tuning with the planner's choices, except the knobs given
+    (threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked)."""
+    t = tsx_tuning()
+    tsx_tuning_defaults(ctypes.byref(t))
+    for k, v in knobs.items():
+        if k not in dict(tsx_tuning._fields_):
+            raise TypeError(f"unknown tuning knob {k!r}")
+        setattr(t, k, int(v))
+    return t
+
+
+def _tuning_ref(t):
+    if t is None:
+        return None
+    return ctypes.byref(t if isinstance(t, tsx_tuning) else tuning(**t))
+
+
+def query(dtype, rows, cols, box, stages, variant="tma", op="copy", pitch=None, tuning=None) -> dict:
+    """The plan and launch shape the library would use (host only, no GPU).
+    ``tuning``: a dict of knobs or a tsx_tuning (None: the planner's)."""
     info = tsx_plan_info()
-    rc = tsx_plan_query_pitched(_code(DTYPES, dtype), rows, cols, cols if pitch is None else pitch, box[0], box[1],
-                                stages, _code(VARIANTS, variant), _code(OPS, op), ctypes.byref(info))
+    rc = tsx_plan_query_tuned(_code(DTYPES, dtype), rows, cols, cols if pitch is None else pitch, box[0], box[1],
+                              stages, _code(VARIANTS, variant), _tuning_ref(tuning), _code(OPS, op),
+                              ctypes.byref(info))
     if rc != TSX_OK:
         raise TsxError(rc, tsx_last_error())
     return info.as_dict()
@@ -148,12 +197,12 @@ class Plan:
     """A tsx plan bound to the current CUDA device."""
 
     def __init__(self, dtype: str, rows: int, cols: int, box=(32, 32), stages: int = 2, variant: str = "tma",
-                 pitch: int | None = None):
+                 pitch: int | None = None, tuning=None):
         self.dtype, self.rows, self.cols = dtype, int(rows), int(cols)
         self.pitch = self.cols if pitch is None else int(pitch)
         self.box, self.stages, self.variant = (int(box[0]), int(box[1])), int(stages), variant
-        h = tsx_plan_create_pitched(_code(DTYPES, dtype), self.rows, self.cols, self.pitch, self.box[0], self.box[1],
-                                    self.stages, _code(VARIANTS, variant))
+        h = tsx_plan_create_tuned(_code(DTYPES, dtype), self.rows, self.cols, self.pitch, self.box[0], self.box[1],
+                                  self.stages, _code(VARIANTS, variant), _tuning_ref(tuning))
         if not h:
             raise TsxError(TSX_ERR_UNSUPPORTED, tsx_last_error())
         self.handle = h
@@ -217,9 +266,21 @@ class Plan:
         """Device-side status since the last call (reads and clears it)."""
         return tsx_plan_status(self.handle)
 
+    def enable_trace(self, events_per_cta: int) -> None:
+        """Test hook: later launches record their schedule (0: off)."""
+        rc = tsx_debug_plan_enable_trace(self.handle, int(events_per_cta))
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+
+    def set_fault_tile(self, tile: int) -> None:
+        """Test hook: later launches skip the loads of `tile` (-1: none)."""
+        rc = tsx_debug_plan_set_fault_tile(self.handle, int(tile))
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+
     def trace(self):
-        """The schedule trace of the plan's last traced launch (plans created
-        with env TSX_TRACE): uint32 [grid, events per CTA, 4]."""
+        """The schedule trace of the plan's last traced launch (after
+        ``enable_trace``): uint32 [grid, events per CTA, 4]."""
         import numpy as np
 
         grid, per = ctypes.c_int32(), ctypes.c_int32()

@@ -46,14 +46,6 @@ int cuda_error(cudaError_t e, const char* what)
     return TSX_ERR_CUDA;
 }
 
-int64_t env_i64(const char* name, int64_t fallback)
-{
-    const char* v = std::getenv(name);
-    if (!v || !*v)
-        return fallback;
-    return std::strtoll(v, nullptr, 10);
-}
-
 // cuTensorMapEncodeTiled, looked up through the runtime so that the library
 // does not link against the driver library (it then loads on machines
 // without a GPU, where only tsx_plan_query is usable).
@@ -112,15 +104,13 @@ struct tsx_plan {
     int sm_count = 0;
     int max_smem = 0;
     int* d_status = nullptr;
-    uint64_t timeout_ns = 1000000000ull;
+    // test hooks (include/tsx_debug.h): the tile whose loads the producer
+    // skips, and the traced kernels' schedule record, [trace_grid][trace_cap]
+    // events of 16 bytes
     int64_t fault_tile = -1;
-    // test hook (env TSX_TRACE = events per CTA): traced kernels record their
-    // schedule into trace_buf, [trace_grid][trace_cap] events of 16 bytes
     int trace_cap = 0;
     uint32_t* trace_buf = nullptr;
     int trace_grid = 0;
-    bool checked = false;
-    int ctas_per_sm_cap = 0;
 
     struct OpLaunch {
         bool ready = false;
@@ -196,7 +186,7 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
             return set_error(rc, why);
         const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate, p->trace_cap > 0);
         if (!fn)
-            return set_error(TSX_ERR_UNSUPPORTED, "TSX_TRACE: only fp32 copy and add have a traced kernel");
+            return set_error(TSX_ERR_UNSUPPORTED, "traced launches: only fp32 copy and add have a traced kernel");
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.og.smem_bytes));
         if (e != cudaSuccess)
             return cuda_error(e, "cudaFuncSetAttribute");
@@ -206,8 +196,8 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
             return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (blocks < 1)
             return set_error(TSX_ERR_UNSUPPORTED, "the kernel cannot be resident with this shared memory / threads");
-        if (p->ctas_per_sm_cap > 0 && blocks > p->ctas_per_sm_cap)
-            blocks = p->ctas_per_sm_cap;
+        if (p->g.knobs.ctas_per_sm > 0 && blocks > p->g.knobs.ctas_per_sm)
+            blocks = p->g.knobs.ctas_per_sm;
         L.ctas_per_sm = blocks;
         // persistent grid: every resident CTA slot once, no more CTAs than tiles
         const int64_t slots = int64_t(p->sm_count) * blocks;
@@ -284,34 +274,7 @@ int get_map(tsx_plan* p, const void* ptr, CUtensorMap* out)
 // Kernel arguments of the TMA kernels for plan p and one op's geometry.
 void fill_tma_args(const tsx_plan* p, const OpGeometry& og, TmaArgs* args)
 {
-    const Geometry& g = p->g;
-    *args = TmaArgs{};
-    args->tiles = g.tiles;
-    args->tiles_c = g.tiles_c;
-    args->tiles_r = g.tiles_r;
-    args->pitch = g.pitch;
-    args->fault_tile = p->fault_tile;
-    args->status = p->d_status;
-    args->timeout_ns = p->timeout_ns;
-    args->rows = int(g.rows);
-    args->cols = int(g.cols);
-    args->box_rows = g.box_rows;
-    args->box_cols = g.box_cols;
-    args->stages = g.stages;
-    args->inner_elems = g.inner_elems;
-    args->atoms = g.atoms;
-    args->rows_per_load = g.rows_per_load;
-    args->row_chunks = g.row_chunks;
-    args->rank3 = g.variant == TSX_TMA_RANK3;
-    args->load_smem_bytes = g.load_smem_bytes;
-    args->slot_bytes = g.slot_bytes;
-    args->stage_bytes = og.stage_bytes;
-    args->bytes_per_load = uint32_t(g.bytes_per_load);
-    args->vec16_per_slot = og.vec16_per_slot;
-    args->store_lag = g.store_lag;
-    args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
-    args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
-    args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
+    tsx::fill_tma_args(p->g, og, p->d_status, p->fault_tile, args);
 }
 
 int alignment_of(const void* ptr)
@@ -372,10 +335,12 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         const int ctas = int(kSmemPerSm / (smem + kSmemPerCtaReserved));
         int threads = 768 / (ctas < 1 ? 1 : ctas) / 32 * 32;
         threads = threads < 64 ? 64 : threads > 512 ? 512 : threads;
-        const char* env = std::getenv("TSX_THREADS");
-        const int forced = env && *env ? std::atoi(env) : 0;
-        if (forced >= 32 && forced <= kMaxThreads - 32 && forced % 32 == 0)
+        const int forced = p->g.knobs.threads;
+        if (forced > 0) {
+            if (forced > kMaxThreads - 32)
+                return set_error(TSX_ERR_UNSUPPORTED, "tuning.threads: at most 992 compute threads for row sums");
             threads = forced;
+        }
         L.og.threads = threads;
         L.og.block_threads = threads + 32;
         const void* fn = rowsum_kernel(p->g.dtype, op);
@@ -388,8 +353,8 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
             return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (blocks < 1)
             return set_error(TSX_ERR_UNSUPPORTED, "the row reduction cannot be resident with this shared memory");
-        if (p->ctas_per_sm_cap > 0 && blocks > p->ctas_per_sm_cap)
-            blocks = p->ctas_per_sm_cap;
+        if (p->g.knobs.ctas_per_sm > 0 && blocks > p->g.knobs.ctas_per_sm)
+            blocks = p->g.knobs.ctas_per_sm;
         L.ctas_per_sm = blocks;
         // contiguous tile ranges, one per CTA; a band is cut between at most
         // 1 + ceil((tiles_c - 1) / floor(T / G)) consecutive CTAs
@@ -432,9 +397,18 @@ tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_
 tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
                                    int box_cols, int stages, tsx_variant variant)
 {
+    return tsx_plan_create_tuned(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, nullptr);
+}
+
+tsx_plan_t tsx_plan_create_tuned(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                 int box_cols, int stages, tsx_variant variant, const tsx_tuning* tuning)
+{
     std::string why;
     Geometry g;
-    int rc = make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, &g, &why);
+    Knobs knobs;
+    int rc = resolve_knobs(tuning, &knobs, &why);
+    if (rc == TSX_OK)
+        rc = make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, knobs, &g, &why);
     if (rc != TSX_OK) {
         set_error(rc, why);
         return nullptr;
@@ -462,16 +436,6 @@ tsx_plan_t tsx_plan_create_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, 
         delete p;
         return nullptr;
     }
-    const int64_t ms = env_i64("TSX_TIMEOUT_MS", 1000);
-    p->timeout_ns = uint64_t(ms > 0 ? ms : 1000) * 1000000ull;
-    p->fault_tile = env_i64("TSX_FAULT_SKIP_TILE", -1);
-    {
-        const int64_t cap = env_i64("TSX_TRACE", 0);
-        p->trace_cap = cap > 0 && cap <= (1 << 20) ? int(cap) : 0;
-    }
-    p->checked = env_i64("TSX_CHECKED", 0) != 0;
-    p->ctas_per_sm_cap = int(env_i64("TSX_CTAS_PER_SM", 0));
-
     set_last_error("");
     return p;
 }
@@ -504,7 +468,7 @@ int tsx_debug_trace(tsx_plan_t p, uint32_t* events, int64_t capacity, int32_t* g
     if (!p || (!events && capacity > 0) || capacity < 0)
         return set_error(TSX_ERR_INVALID, "NULL plan or events");
     if (p->trace_cap <= 0 || !p->trace_buf)
-        return set_error(TSX_ERR_INVALID, "the plan has no trace (TSX_TRACE unset, or no traced launch yet)");
+        return set_error(TSX_ERR_INVALID, "the plan has no trace (tracing not enabled, or no traced launch yet)");
     const int64_t words = int64_t(p->trace_grid) * p->trace_cap * 4;
     const int64_t n = capacity < words ? capacity : words;
     if (n > 0) {
@@ -516,6 +480,35 @@ int tsx_debug_trace(tsx_plan_t p, uint32_t* events, int64_t capacity, int32_t* g
         *grid = p->trace_grid;
     if (per_cta)
         *per_cta = p->trace_cap;
+    set_last_error("");
+    return TSX_OK;
+}
+
+int tsx_debug_plan_set_fault_tile(tsx_plan_t p, int64_t tile)
+{
+    if (!p)
+        return set_error(TSX_ERR_INVALID, "NULL plan");
+    p->fault_tile = tile >= 0 ? tile : -1;
+    set_last_error("");
+    return TSX_OK;
+}
+
+int tsx_debug_plan_enable_trace(tsx_plan_t p, int32_t events_per_cta)
+{
+    if (!p)
+        return set_error(TSX_ERR_INVALID, "NULL plan");
+    if (events_per_cta < 0 || events_per_cta > (1 << 20))
+        return set_error(TSX_ERR_INVALID, "events_per_cta must be in [0, 2^20]");
+    if (events_per_cta != p->trace_cap) {
+        // the elementwise launches pick their kernel again (traced or not);
+        // the ring is reallocated at the next traced launch
+        for (auto& L : p->ops)
+            L.ready = false;
+        cudaFree(p->trace_buf);
+        p->trace_buf = nullptr;
+        p->trace_grid = 0;
+        p->trace_cap = events_per_cta;
+    }
     set_last_error("");
     return TSX_OK;
 }
@@ -637,7 +630,7 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
     }
     if (e != cudaSuccess)
         return cuda_error(e, "kernel launch");
-    if (p->checked) {
+    if (p->g.knobs.checked) {
         e = cudaStreamSynchronize(st);
         if (e != cudaSuccess)
             return cuda_error(e, "cudaStreamSynchronize");
@@ -704,7 +697,7 @@ int tsx_reduce_rows(tsx_plan_t p, tsx_op op, const void* a, const void* b, const
                                   L->scratch, row_sums);
     if (e != cudaSuccess)
         return cuda_error(e, "kernel launch");
-    if (p->checked) {
+    if (p->g.knobs.checked) {
         e = cudaStreamSynchronize(st);
         if (e != cudaSuccess)
             return cuda_error(e, "cudaStreamSynchronize");

@@ -17,20 +17,23 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <string>
 
 #include "plan.h"
+#include "tsx_debug.h"
 
 namespace tsx {
 namespace {
 
 // The scratch of every allocation-free call on a device.  Its size is the
-// stated maximum; a call needs one 4-byte status word of it.
+// stated maximum; a call needs one 4-byte status word of it, which is
+// checked here at compile time.
 constexpr size_t kNoallocScratchBytes = 256;
 static __device__ __align__(256) int g_noalloc_scratch[kNoallocScratchBytes / sizeof(int)];
 constexpr size_t kStatusWordBytes = sizeof(int);
+static_assert(kStatusWordBytes <= kNoallocScratchBytes, "the status word must fit in the scratch array");
 
 // Device address of the scratch array, looked up once per device.
 constexpr int kMaxDevices = 64;
@@ -38,9 +41,21 @@ std::once_flag g_once[kMaxDevices];
 int* g_scratch[kMaxDevices];
 cudaError_t g_setup_error[kMaxDevices];
 
+// Fault hook of the calling host thread (tsx_debug_noalloc_set_fault).
+thread_local int64_t t_fault_tile = -1;
+thread_local int t_timeout_ms = 0;
+
 int fail(int rc, const char* msg)
 {
     set_last_error(msg);
+    return rc;
+}
+
+int fail(int rc, const char* what, const std::string& why)
+{
+    char buf[384];
+    std::snprintf(buf, sizeof buf, "tsx_ewise_noalloc: %s: %s", what, why.c_str());
+    set_last_error(buf);
     return rc;
 }
 
@@ -85,6 +100,12 @@ int alignment(const void* ptr)
 
 using namespace tsx;
 
+extern "C" void tsx_debug_noalloc_set_fault(int64_t tile, int32_t timeout_ms)
+{
+    t_fault_tile = tile >= 0 ? tile : -1;
+    t_timeout_ms = timeout_ms > 0 ? timeout_ms : 0;
+}
+
 extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols,
                                  int stages, tsx_variant variant, tsx_op op, const void* a, const void* b,
                                  const void* c, void* out, tsx_stream_t stream, int* status_out)
@@ -93,15 +114,16 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
         return fail(TSX_ERR_INVALID, "tsx_ewise_noalloc: only the TMA variants (TSX_TMA, TSX_TMA_RANK3) are offered");
     if (op < TSX_COPY || op > TSX_FMA)
         return fail(TSX_ERR_INVALID, "tsx_ewise_noalloc: unknown op");
+    Knobs knobs;
+    knobs.timeout_ms = t_timeout_ms > 0 ? t_timeout_ms : 1000;
     Geometry g;
-    int rc = make_geometry(dtype, rows, cols, box_rows, box_cols, stages, variant, &g, nullptr);
+    std::string why;
+    int rc = make_geometry(dtype, rows, cols, cols, box_rows, box_cols, stages, variant, knobs, &g, &why);
     if (rc != TSX_OK)
-        return fail(rc, "tsx_ewise_noalloc: no legal plan for these arguments (tsx_plan_query gives the reason)");
-    if (kStatusWordBytes > kNoallocScratchBytes)
-        return fail(TSX_ERR_UNSUPPORTED, "tsx_ewise_noalloc: the call needs more scratch than the 256-byte array");
-    if (status_out)
-        *status_out = TSX_OK;
+        return fail(rc, "no legal plan for these arguments", why);
     if (g.tiles == 0) {
+        if (status_out)
+            *status_out = TSX_OK;
         set_last_error("");
         return TSX_OK;   // empty tensor: nothing to do
     }
@@ -127,9 +149,9 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
     if (e != cudaSuccess)
         return fail_cuda(e, "cudaDeviceGetAttribute");
     OpGeometry og;
-    rc = make_op_geometry(g, op, max_smem, &og, nullptr);
+    rc = make_op_geometry(g, op, max_smem, &og, &why);
     if (rc != TSX_OK)
-        return fail(rc, "tsx_ewise_noalloc: the stages do not fit in shared memory");
+        return fail(rc, "no launch for these arguments", why);
     const void* fn = tma_kernel(dtype, op);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(og.smem_bytes));
     if (e != cudaSuccess)
@@ -152,31 +174,8 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
         if (rc != TSX_OK)
             return rc;
     }
-    TmaArgs args{};
-    args.tiles = g.tiles;
-    args.tiles_c = g.tiles_c;
-    args.pitch = g.pitch;
-    args.fault_tile = -1;
-    args.status = scratch;
-    const char* ms = std::getenv("TSX_TIMEOUT_MS");
-    const long long ms_v = ms && *ms ? std::atoll(ms) : 1000;
-    args.timeout_ns = uint64_t(ms_v > 0 ? ms_v : 1000) * 1000000ull;
-    args.store_lag = g.store_lag;
-    args.rows = int(g.rows);
-    args.cols = int(g.cols);
-    args.box_rows = g.box_rows;
-    args.box_cols = g.box_cols;
-    args.stages = g.stages;
-    args.inner_elems = g.inner_elems;
-    args.atoms = g.atoms;
-    args.rows_per_load = g.rows_per_load;
-    args.row_chunks = g.row_chunks;
-    args.rank3 = g.variant == TSX_TMA_RANK3;
-    args.load_smem_bytes = g.load_smem_bytes;
-    args.slot_bytes = g.slot_bytes;
-    args.stage_bytes = og.stage_bytes;
-    args.bytes_per_load = uint32_t(g.bytes_per_load);
-    args.vec16_per_slot = og.vec16_per_slot;
+    TmaArgs args;
+    fill_tma_args(g, og, scratch, t_fault_tile, &args);
 
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the status word keeps the previous call's value: start this one at zero
@@ -187,11 +186,11 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
     if (e != cudaSuccess)
         return fail_cuda(e, "kernel launch");
     if (status_out) {
-        e = cudaStreamSynchronize(st);
-        if (e != cudaSuccess)
-            return fail_cuda(e, "cudaStreamSynchronize");
+        // read the word in stream order (no device-wide synchronisation)
         int h = 0;
-        e = cudaMemcpy(&h, scratch, sizeof h, cudaMemcpyDeviceToHost);
+        e = cudaMemcpyAsync(&h, scratch, sizeof h, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(st);
         if (e != cudaSuccess)
             return fail_cuda(e, "reading the status word");
         *status_out = h;

@@ -4,7 +4,6 @@
 // so tsx_plan_query works on a machine without a GPU.
 
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -24,19 +23,11 @@ bool fail(std::string* why, const char* fmt, long long a = 0, long long b = 0)
     return false;
 }
 
-int env_int(const char* name, int fallback)
-{
-    const char* v = std::getenv(name);
-    if (!v || !*v)
-        return fallback;
-    return std::atoi(v);
-}
-
 uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-int default_threads(int variant, size_t smem_bytes, uint32_t units)
+int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units)
 {
     // Threads of the elementwise stage.  TMA paths: about 256 compute
     // threads per SM in all, shared by the CTAs that fit in its shared
@@ -48,8 +39,12 @@ int default_threads(int variant, size_t smem_bytes, uint32_t units)
     // The cp.async / synchronous ablations give each thread about four
     // 16-byte units of the slot, between 128 threads (the TVM ldgsts
     // demonstration program's count, which its 128x32 fp16 tile gets) and
-    // 512.  TSX_THREADS overrides (a multiple of 32).
+    // 512.  A forced count (tsx_tuning.threads) wins.
+    (void)op;
+    const int variant = g.variant;
     const bool tma = is_tma_variant(variant);
+    if (g.knobs.threads > 0)
+        return g.knobs.threads;
     int fallback = int((units / 4 + 31) / 32 * 32);
     fallback = fallback < 128 ? 128 : fallback > 512 ? 512 : fallback;
     if (tma) {
@@ -66,25 +61,45 @@ int default_threads(int variant, size_t smem_bytes, uint32_t units)
             fallback = fallback > cover ? fallback : cover < most ? cover : most;
         }
     }
-    const int limit = tma ? kMaxThreads - 32 * kTmaRoleWarps : kMaxThreads;
-    int t = env_int("TSX_THREADS", fallback);
-    if (t < 32 || t > limit || t % 32)
-        t = fallback;
-    return t;
+    return fallback;
 }
 
 int default_store_lag(int stages)
 {
     // tiles between a store's issue and the release of its stage: one for
     // shallow rings, two once there are enough stages to keep loads ahead
-    int lag = env_int("TSX_STORE_LAG", stages >= 6 ? 2 : 1);
-    return lag < 0 ? 0 : lag > 3 ? 3 : lag;
+    return stages >= 6 ? 2 : 1;
+}
+
+int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
+{
+    *k = Knobs{};
+    if (!t)
+        return TSX_OK;
+    if (t->threads > 0) {
+        if (t->threads % 32 || t->threads > kMaxThreads)
+            return fail(why, "tuning.threads must be a multiple of 32 of at most %lld (got %lld)", kMaxThreads,
+                        t->threads),
+                   TSX_ERR_INVALID;
+        k->threads = t->threads;
+    }
+    k->ctas_per_sm = t->ctas_per_sm > 0 ? t->ctas_per_sm : 0;
+    if (t->store_lag > 3)
+        return fail(why, "tuning.store_lag must be at most 3 (got %lld)", t->store_lag), TSX_ERR_INVALID;
+    k->store_lag = t->store_lag;
+    if (t->l2_promotion > 3)
+        return fail(why, "tuning.l2_promotion must be 0..3 (got %lld)", t->l2_promotion), TSX_ERR_INVALID;
+    k->l2_promotion = t->l2_promotion < 0 ? 2 : t->l2_promotion;
+    k->timeout_ms = t->timeout_ms > 0 ? t->timeout_ms : 1000;
+    k->checked = t->checked != 0;
+    return TSX_OK;
 }
 
 int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,
-                  int variant, Geometry* g, std::string* why)
+                  int variant, const Knobs& knobs, Geometry* g, std::string* why)
 {
     *g = Geometry{};
+    g->knobs = knobs;
     if (dtype < TSX_F16 || dtype > TSX_F32)
         return fail(why, "unknown dtype %lld", dtype), TSX_ERR_INVALID;
     if (variant < TSX_TMA || variant > TSX_TMA_PROMOTED)
@@ -207,10 +222,13 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
         g->copy_vec_bytes = vb;
         g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
     }
-    g->store_lag = default_store_lag(stages);
-    // tuning knob: the tensor maps' L2 promotion (the TVM page passes 128 B)
-    const int l2 = env_int("TSX_L2_PROMOTION", 2);
-    g->l2_promotion = l2 < 0 || l2 > 3 ? 2 : l2;
+    g->store_lag = knobs.store_lag >= 0 ? knobs.store_lag : default_store_lag(stages);
+    // the tensor maps' L2 promotion (the TVM page passes 128 B)
+    g->l2_promotion = knobs.l2_promotion;
+    if (is_tma_variant(variant) && knobs.threads > kMaxThreads - 32 * kTmaRoleWarps)
+        return fail(why, "tuning.threads: at most %lld compute threads beside the TMA role warps",
+                    kMaxThreads - 32 * kTmaRoleWarps),
+               TSX_ERR_INVALID;
     return TSX_OK;
 }
 
@@ -237,7 +255,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     if (og->smem_bytes > size_t(max_smem))
         return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
                TSX_ERR_UNSUPPORTED;
-    og->threads = default_threads(g.variant, og->smem_bytes, g.slot_bytes / 16);
+    og->threads = default_threads(g, op, og->smem_bytes, g.slot_bytes / 16);
     og->block_threads = og->threads + (tma ? 32 * kTmaRoleWarps : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;
@@ -275,6 +293,8 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->threads = og.threads;
     info->block_threads = og.block_threads;
     info->tma_elem_bytes = g.tma_es;
+    info->store_lag = is_tma_variant(g.variant) ? g.store_lag : 0;
+    info->timeout_ms = g.knobs.timeout_ms;
     info->vec = og.vec;
     info->outer = og.outer;
     info->copy_vec_bytes = g.copy_vec_bytes;
@@ -297,6 +317,37 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
         info->l2_promotion = m.l2_promotion;        // CUtensorMapL2promotion value
         info->oob_fill = 0;                         // CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE: zeros
     }
+}
+
+void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t fault_tile, TmaArgs* args)
+{
+    *args = TmaArgs{};
+    args->tiles = g.tiles;
+    args->tiles_c = g.tiles_c;
+    args->tiles_r = g.tiles_r;
+    args->pitch = g.pitch;
+    args->fault_tile = fault_tile;
+    args->status = status;
+    args->timeout_ns = uint64_t(g.knobs.timeout_ms) * 1000000ull;
+    args->rows = int(g.rows);
+    args->cols = int(g.cols);
+    args->box_rows = g.box_rows;
+    args->box_cols = g.box_cols;
+    args->stages = g.stages;
+    args->inner_elems = g.inner_elems;
+    args->atoms = g.atoms;
+    args->rows_per_load = g.rows_per_load;
+    args->row_chunks = g.row_chunks;
+    args->rank3 = g.variant == TSX_TMA_RANK3;
+    args->load_smem_bytes = g.load_smem_bytes;
+    args->slot_bytes = g.slot_bytes;
+    args->stage_bytes = og.stage_bytes;
+    args->bytes_per_load = uint32_t(g.bytes_per_load);
+    args->vec16_per_slot = og.vec16_per_slot;
+    args->store_lag = g.store_lag;
+    args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
+    args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
+    args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
 }
 
 void tensor_map_args(const Geometry& g, TensorMapArgs* m)
@@ -331,12 +382,25 @@ void tensor_map_args(const Geometry& g, TensorMapArgs* m)
 
 }  // namespace tsx
 
-extern "C" int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
-                                      int box_cols, int stages, tsx_variant variant, tsx_op op_arg,
-                                      tsx_plan_info* info)
+extern "C" void tsx_tuning_defaults(tsx_tuning* t)
+{
+    if (!t)
+        return;
+    t->threads = 0;
+    t->ctas_per_sm = 0;
+    t->store_lag = -1;
+    t->l2_promotion = -1;
+    t->timeout_ms = 0;
+    t->checked = 0;
+}
+
+extern "C" int tsx_plan_query_tuned(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                    int box_cols, int stages, tsx_variant variant, const tsx_tuning* tuning,
+                                    tsx_op op_arg, tsx_plan_info* info)
 {
     std::string why;
     tsx::Geometry g;
+    tsx::Knobs knobs;
     int op;
     bool accumulate;
     if (!tsx::split_op(op_arg, &op, &accumulate)) {
@@ -347,7 +411,9 @@ extern "C" int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t col
         tsx::set_last_error("TSX_ACCUMULATE needs TSX_TMA or TSX_TMA_RANK3");
         return TSX_ERR_UNSUPPORTED;
     }
-    int rc = tsx::make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, &g, &why);
+    int rc = tsx::resolve_knobs(tuning, &knobs, &why);
+    if (rc == TSX_OK)
+        rc = tsx::make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, knobs, &g, &why);
     if (rc == TSX_OK) {
         tsx::OpGeometry og;
         rc = tsx::make_op_geometry(g, op, tsx::kMaxDynSmem, &og, &why);
@@ -358,8 +424,14 @@ extern "C" int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t col
     return rc;
 }
 
+extern "C" int tsx_plan_query_pitched(tsx_dtype dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                                      int box_cols, int stages, tsx_variant variant, tsx_op op, tsx_plan_info* info)
+{
+    return tsx_plan_query_tuned(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, nullptr, op, info);
+}
+
 extern "C" int tsx_plan_query(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
                               tsx_variant variant, tsx_op op, tsx_plan_info* info)
 {
-    return tsx_plan_query_pitched(dtype, rows, cols, cols, box_rows, box_cols, stages, variant, op, info);
+    return tsx_plan_query_tuned(dtype, rows, cols, cols, box_rows, box_cols, stages, variant, nullptr, op, info);
 }

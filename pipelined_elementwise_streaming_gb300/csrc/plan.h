@@ -9,7 +9,19 @@
 
 namespace tsx {
 
-// Everything fixed by (dtype, shape, box, stages, variant).
+// Launch knobs of a plan, resolved from a tsx_tuning (planner's choices
+// filled in).  threads = 0 and ctas_per_sm = 0 leave those to the planner
+// and to occupancy.
+struct Knobs {
+    int threads = 0;
+    int ctas_per_sm = 0;
+    int store_lag = -1;      // < 0: default_store_lag(stages)
+    int l2_promotion = 2;    // CUtensorMapL2promotion
+    int timeout_ms = 1000;
+    bool checked = false;
+};
+
+// Everything fixed by (dtype, shape, box, stages, variant, knobs).
 struct Geometry {
     int dtype = 0, es = 0, variant = 0, stages = 0;
     int64_t rows = 0, cols = 0;
@@ -27,6 +39,7 @@ struct Geometry {
     uint32_t slot_bytes = 0;
     // copy width of the cp.async / synchronous variants (16-byte aligned bases)
     int copy_vec_bytes = 0;
+    Knobs knobs;
 };
 
 // What additionally depends on the op (operand count).
@@ -49,19 +62,25 @@ struct TensorMapArgs {
     int swizzle = 0;   // CUtensorMapSwizzle value
 };
 
-int default_threads(int variant, size_t smem_bytes, uint32_t units);
+int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units);
 int default_store_lag(int stages);
+// Validate a tsx_tuning (NULL: all defaults) into knobs.
+int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,
-                  int variant, Geometry* g, std::string* why);
-// Dense rows: pitch = cols.
-inline int make_geometry(int dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
-                         int variant, Geometry* g, std::string* why)
+                  int variant, const Knobs& knobs, Geometry* g, std::string* why);
+// Default knobs.
+inline int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols,
+                         int stages, int variant, Geometry* g, std::string* why)
 {
-    return make_geometry(dtype, rows, cols, cols, box_rows, box_cols, stages, variant, g, why);
+    return make_geometry(dtype, rows, cols, pitch, box_rows, box_cols, stages, variant, Knobs{}, g, why);
 }
 int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, std::string* why);
 void tensor_map_args(const Geometry& g, TensorMapArgs* m);
 void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info);
+// Kernel arguments of the TMA kernels (elementwise and row sums) for one op:
+// the device status word, and the tile whose loads the producer skips (test
+// hook; -1 for none).
+void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t fault_tile, TmaArgs* args);
 
 // Thread-local message behind tsx_last_error (capi.cpp).
 void set_last_error(const char* msg);

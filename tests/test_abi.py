@@ -120,11 +120,10 @@ def test_query_workload_plans(tsx):
     assert q["block_threads"] == q["threads"] + 64        # + producer warp and store warp
 
 
-def test_query_partition_of_the_smem_sqrt_demo(tsx, monkeypatch):
+def test_query_partition_of_the_smem_sqrt_demo(tsx):
     """With 256 elementwise threads, a 32x32 float32 tile is one round of
     float4 vectors (TVM "elementwise -> smem", Algorithm step 2)."""
-    monkeypatch.setenv("TSX_THREADS", "256")
-    q = tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")
+    q = tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt", tuning={"threads": 256})
     assert (q["vec"], q["outer"], q["threads"]) == (4, 1, 256)
 
 

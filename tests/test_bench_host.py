@@ -35,26 +35,60 @@ def test_reference_arm_other_ranks_print_nothing(capsys, monkeypatch):
     assert capsys.readouterr().out.strip() == ""
 
 
+def test_reference_arm_reports_its_cores(capsys):
+    """The reference arm times the oracle on every host core and names the
+    count, with a single-thread figure beside it."""
+    import oracle
+
+    rc = bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1", "--workload", "add_1024x8192_f16"])
+    assert rc == 0
+    d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    cb = d["cpu_baseline"]
+    assert cb["cores"] == oracle.host_cores() >= 1
+    assert cb["single_core"]["cores"] == 1 and cb["single_core"]["value"] > 0
+
+
 def test_parity_leg_flags_a_differing_element():
-    """The CPU-baseline leg's check of the device output: an output equal to
-    the oracle's has no mismatch, one flipped bit is one mismatch."""
+    """The CPU-baseline leg's check of the whole device output: an output
+    equal to the oracle's has no mismatch, one flipped bit is one mismatch,
+    and its position is reported."""
+    import numpy as np
+
+    w = bench.ti.WORKLOADS["fma_128x1048576_f32"].with_rows(2)
+    ins = w.inputs()
+    base, parity = bench.cpu_baseline(w, ins, None, 0.1)
+    assert parity is None and base["cores"] >= 1 and base["single_core"]["value"] > 0
+    import oracle
+
+    dev = np.asarray(oracle.ewise(w.op, w.dtype, *ins)).view(np.uint32).copy()
+    assert bench.cpu_baseline(w, ins, dev, 0.1)[1]["mismatches"] == 0
+    dev[1, 7] ^= 1
+    p = bench.cpu_baseline(w, ins, dev, 0.1)[1]
+    assert p["mismatches"] == 1 and p["elements"] == w.elems
+    assert p["first_mismatch_flat_index"] == w.cols + 7
+
+
+def test_parity_record_uses_the_exp_bound():
     import numpy as np
 
     import oracle
 
-    w = bench.ti.WORKLOADS["fma_128x1048576_f32"].with_rows(1)
-    band = bench.oracle_band_rows(w)
-    idx = np.arange(0, band * w.cols, dtype=np.uint64)
-    head = np.asarray(oracle.ewise(w.op, w.dtype, *w.inputs_at(idx))).view(np.int32).reshape(band, w.cols)
-    assert bench.cpu_baseline(w, 0.2, head)[1]["mismatches"] == 0
-    head[0, 7] ^= 1
-    assert bench.cpu_baseline(w, 0.2, head)[1]["mismatches"] == 1
+    w = bench.ti.WORKLOADS["exp_16384x16384_bf16"].with_rows(4)
+    ins = w.inputs()
+    want = oracle.ewise(w.op, w.dtype, *ins)
+    got = want.copy().reshape(-1)
+    got[3] += 1          # one ulp: within the bf16 bound
+    assert bench.parity_record(w, got, want, 2)["mismatches"] == 0
+    got[5] += 2          # two ulps: outside
+    rec = bench.parity_record(w, got, want, 2)
+    assert rec["mismatches"] == 1 and rec["first_mismatch_flat_index"] == 5 and rec["rule"] == "within 1 ulp"
 
 
-def test_cpu_baseline_is_bounded():
-    w = bench.ti.WORKLOADS["fma_128x1048576_f32"]
-    nbytes, spent, rows, cores = bench.cpu_time_oracle(w, 0.05, max_rows=8)
-    assert 1 <= rows <= 8 and cores == 1 and nbytes == rows * w.cols * 16
+def test_single_core_oracle_timing_is_bounded():
+    w = bench.ti.WORKLOADS["fma_128x1048576_f32"].with_rows(8)
+    ins = w.inputs()
+    nbytes, spent, elems = bench.oracle_single_core(w, ins, 0.01, band_elems=1 << 18)
+    assert 1 <= elems < w.elems and nbytes == elems * 16 and spent > 0
 
 
 def _free_port():
@@ -90,27 +124,20 @@ def test_aggregate_over_two_gloo_ranks():
     assert out[0] == out[1] == (2.0, 30.0)   # max of seconds, sum of units
 
 
-def test_clock_sampler_parses_samples():
-    s = bench.ClockSampler(0)
+def test_clock_summary():
+    """Median SM clock and the throttle reasons of the samples in a region."""
+    samples = [(1965.0, 0x0), (1900.0, 0x4), (2070.0, 0x1)]
+    c = bench.summarise_clocks(samples, 2070.0)
+    assert c["samples"] == 3 and c["sm_mhz"] == 1965.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]   # idle (0x1) is not a throttle reason
+    c = bench.summarise_clocks([(1200.0, 0x8 | 0x40)], 2070.0)
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.summarise_clocks([], None)["sm_mhz"] is None
 
-    class P:
-        def terminate(self):
-            pass
 
-        def wait(self, timeout=None):
-            return 0
-
-    s.proc = P()
-    s.lines = [(1.0, "0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active"),
-               (2.0, "0, 1900, 2070, 1200.0, 0x4, Not Active, Not Active, Not Active, Active"),
-               (9.0, "0, 300, 2070, 90.0, 0x0, Active, Not Active, Not Active, Not Active")]
-    import time as _t
-
-    orig = _t.sleep
-    _t.sleep = lambda x: None
-    try:
-        c = s.stop(0.5, 5.0)
-    finally:
-        _t.sleep = orig
-    assert c["samples"] == 2 and c["sm_mhz"] == pytest.approx(1932.5) and c["sm_max_mhz"] == 2070
-    assert c["reasons"] == ["sw_power_cap"]
+def test_clock_sampler_regions_without_nvml():
+    """Without NVML (no GPU here) the sampler says so instead of failing."""
+    s = bench.ClockSampler(0).start()
+    s.stop()
+    r = s.region(0.0, 1e12)
+    assert r["samples"] == 0 or r["sm_mhz"] is not None

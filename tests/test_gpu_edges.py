@@ -171,20 +171,16 @@ def test_plan_info_launch(tsx):
         assert info["smem_bytes"] <= 232448
 
 
-def test_wait_timeout_is_reported_and_the_context_survives(tsx, monkeypatch):
+def test_wait_timeout_is_reported_and_the_context_survives(tsx):
     """The producer skips the loads of one tile (but announces its bytes), so
     that stage's barrier never completes: the bounded wait gives up, the
     kernel records TSX_ERR_TIMEOUT and returns, and the GPU stays usable."""
     dtype, rows, cols = "f32", 256, 1024
     a = random_bits(dtype, (rows, cols), 5, finite_fraction=1.0)
-    monkeypatch.setenv("TSX_FAULT_SKIP_TILE", "5")
-    monkeypatch.setenv("TSX_TIMEOUT_MS", "50")
-    bad = tsx.Plan(dtype, rows, cols, box=(8, 128), stages=3)
-    monkeypatch.setenv("TSX_CHECKED", "1")
-    bad_checked = tsx.Plan(dtype, rows, cols, box=(8, 128), stages=3)
-    monkeypatch.delenv("TSX_FAULT_SKIP_TILE")
-    monkeypatch.delenv("TSX_TIMEOUT_MS")
-    monkeypatch.delenv("TSX_CHECKED")
+    bad = tsx.Plan(dtype, rows, cols, box=(8, 128), stages=3, tuning={"timeout_ms": 50})
+    bad.set_fault_tile(5)
+    bad_checked = tsx.Plan(dtype, rows, cols, box=(8, 128), stages=3, tuning={"timeout_ms": 50, "checked": 1})
+    bad_checked.set_fault_tile(5)
     da = to_dev(a, dtype)
     try:
         bad.ewise("sqrt", da)

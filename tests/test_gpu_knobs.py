@@ -1,4 +1,4 @@
-"""The tuning knobs (environment, read at plan creation) change launch
+"""The tuning knobs (tsx_tuning, given at plan creation) change launch
 shapes and timing only, never results: every setting is checked against the
 oracle on ragged shapes, and the store lag also against the schedule model
 through the traced kernel."""
@@ -28,11 +28,11 @@ def tsx():
     return m
 
 
-def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", accumulate=False):
+def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", tuning=None):
     seed = zlib.crc32(f"knob/{dtype}/{op}/{rows}/{cols}/{box}/{stages}/{variant}".encode())
     ins = [random_bits(dtype, (rows, cols), seed + k) for k in range(ARITY[op])]
     want = oracle.ewise(op, dtype, *ins)
-    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant=variant) as plan:
+    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant=variant, tuning=tuning) as plan:
         out = plan.ewise(op, *[to_dev(x, dtype) for x in ins])
         torch.cuda.synchronize()
         assert plan.status() == tsx.TSX_OK
@@ -42,42 +42,43 @@ def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", accumulate=Fals
 
 
 @pytest.mark.parametrize("knob,values", [
-    ("TSX_STORE_LAG", ["0", "1", "2", "3"]),
-    ("TSX_L2_PROMOTION", ["0", "1", "2", "3"]),
-    ("TSX_THREADS", ["32", "96", "256", "960"]),
-    ("TSX_CTAS_PER_SM", ["1", "2", "3"]),
+    ("store_lag", [0, 1, 2, 3]),
+    ("l2_promotion", [0, 1, 2, 3]),
+    ("threads", [32, 96, 256, 960]),
+    ("ctas_per_sm", [1, 2, 3]),
 ])
 @pytest.mark.parametrize("case", range(len(CASES)))
-def test_knobs_leave_results_unchanged(tsx, monkeypatch, knob, values, case):
+def test_knobs_leave_results_unchanged(tsx, knob, values, case):
     dtype, op, rows, cols, box = CASES[case]
     for v in values:
-        monkeypatch.setenv(knob, v)
         for variant in ("tma", "tma_rank3"):
             for stages in (2, 4):
                 try:
-                    tsx.query(dtype, rows, cols, box, stages, variant, op)
+                    q = tsx.query(dtype, rows, cols, box, stages, variant, op, tuning={knob: v})
                 except tsx.TsxError:
                     continue
-                info = _run(tsx, dtype, op, rows, cols, box, stages, variant)
-                if knob == "TSX_THREADS":
-                    assert info["threads"] == int(v)
-                if knob == "TSX_CTAS_PER_SM":
-                    assert info["ctas_per_sm"] <= int(v)
-        monkeypatch.delenv(knob)
+                info = _run(tsx, dtype, op, rows, cols, box, stages, variant, tuning={knob: v})
+                if knob == "threads":
+                    assert info["threads"] == q["threads"] == v
+                if knob == "ctas_per_sm":
+                    assert info["ctas_per_sm"] <= v
+                if knob == "store_lag":
+                    assert info["store_lag"] == q["store_lag"] == v
+                if knob == "l2_promotion":
+                    assert info["l2_promotion"] == q["l2_promotion"] == v
 
 
 @pytest.mark.parametrize("lag", [0, 2, 3])
 @pytest.mark.parametrize("stages", [2, 4])
-def test_store_lag_follows_the_schedule_model(tsx, monkeypatch, lag, stages):
-    """With TSX_STORE_LAG the store warp releases tile i - lag (lag capped at
-    S - 1) after tile i's stores; the trace must still satisfy the model."""
-    monkeypatch.setenv("TSX_STORE_LAG", str(lag))
-    monkeypatch.setenv("TSX_TRACE", "256")
-    monkeypatch.setenv("TSX_CTAS_PER_SM", "1")
+def test_store_lag_follows_the_schedule_model(tsx, lag, stages):
+    """With a forced store lag the store warp releases tile i - lag (lag
+    capped at S - 1) after tile i's stores; the trace must still satisfy the
+    model."""
     tiles = 1000
     rows, cols = 8 * tiles, 32
     a, b = random_bits("f32", (rows, cols), lag), random_bits("f32", (rows, cols), lag + 1)
-    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages) as plan:
+    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, tuning={"store_lag": lag, "ctas_per_sm": 1}) as plan:
+        plan.enable_trace(256)
         out = plan.ewise("add", to_dev(a, "f32"), to_dev(b, "f32"))
         torch.cuda.synchronize()
         assert plan.status() == tsx.TSX_OK

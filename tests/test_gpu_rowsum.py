@@ -38,8 +38,8 @@ def _values(dtype, shape, seed, lo=-2.0, hi=2.0):
     return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16).reshape(shape)
 
 
-def _rowsum(tsx, dtype, rows, cols, box, stages, variant, op, ins):
-    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant=variant) as plan:
+def _rowsum(tsx, dtype, rows, cols, box, stages, variant, op, ins, tuning=None):
+    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant=variant, tuning=tuning) as plan:
         out = plan.reduce_rows(op, *[to_dev(x, dtype) for x in ins])
         torch.cuda.synchronize()
         assert plan.status() == tsx.TSX_OK
@@ -100,17 +100,16 @@ def test_rowsum_integer_rows_are_exact(tsx):
     (37, 5000, (8, 64), 2),        # ragged rows and columns, 8-row bands cut
     (1, 1 << 20, (1, 512), 0),     # one row over every CTA
 ])
-def test_rowsum_bands_cut_between_ctas_are_exact(tsx, monkeypatch, rows, cols, box, ctas_per_sm):
+def test_rowsum_bands_cut_between_ctas_are_exact(tsx, rows, cols, box, ctas_per_sm):
     """Integer-valued rows, so any lost or doubled share shows: the tile
     ranges of consecutive CTAs cut bands at many points, and the shares of a
     cut band are combined by its last arriving CTA."""
-    if ctas_per_sm:
-        monkeypatch.setenv("TSX_CTAS_PER_SM", str(ctas_per_sm))
     rng = np.random.default_rng(rows * 7 + cols)
     a = rng.integers(-64, 64, (rows, cols)).astype(np.float32)
     want = a.astype(np.float64).sum(axis=1)
     for stages in (2, 4):
-        got = _rowsum(tsx, "f32", rows, cols, box, stages, "tma", "copy", [a.view(np.uint32)])
+        got = _rowsum(tsx, "f32", rows, cols, box, stages, "tma", "copy", [a.view(np.uint32)],
+                      tuning={"ctas_per_sm": ctas_per_sm})
         assert np.array_equal(got, want), (box, stages, np.nonzero(got != want)[0][:5])
 
 
@@ -186,17 +185,14 @@ def test_rowsum_launch_info(tsx):
         assert ei.value.code == tsx.TSX_ERR_UNSUPPORTED
 
 
-def test_rowsum_wait_timeout_is_reported(tsx, monkeypatch):
+def test_rowsum_wait_timeout_is_reported(tsx):
     """The producer is told to skip one tile's loads: the compute warps'
     bounded wait gives up, TSX_ERR_TIMEOUT is recorded, and the GPU stays
     usable."""
     rows, cols = 64, 1024
     a = _values("f32", (rows, cols), 6)
-    monkeypatch.setenv("TSX_FAULT_SKIP_TILE", "9")
-    monkeypatch.setenv("TSX_TIMEOUT_MS", "50")
-    bad = tsx.Plan("f32", rows, cols, box=(8, 128), stages=3)
-    monkeypatch.delenv("TSX_FAULT_SKIP_TILE")
-    monkeypatch.delenv("TSX_TIMEOUT_MS")
+    bad = tsx.Plan("f32", rows, cols, box=(8, 128), stages=3, tuning={"timeout_ms": 50})
+    bad.set_fault_tile(9)
     da = to_dev(a, "f32")
     try:
         bad.reduce_rows("copy", da)

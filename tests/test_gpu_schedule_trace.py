@@ -2,7 +2,7 @@
 of the loop structure of nvFuser PR #2833 ("Loop Structure", "Detailed
 Pseudo-Code"): oracle.structure.schedule / trip_counts.
 
-A plan created with env TSX_TRACE runs a traced kernel that records, per
+A plan with tracing enabled (tsx_debug_plan_enable_trace) runs a traced kernel that records, per
 CTA, the load of each tile (prologue or main loop), the producer's reuse of
 a released stage, the compute warps' wait and body, and the store warp's
 store and release, numbered in the order they happened.  Per CTA the test
@@ -39,15 +39,14 @@ def tsx():
     return m
 
 
-def _run(tsx, monkeypatch, op, tiles, stages, variant="tma"):
+def _run(tsx, op, tiles, stages, variant="tma"):
     """fp32 [8 * tiles, 32] with 8x32 boxes: one tile per row band, at most
     one CTA per SM.  Returns (trace [G, cap, 4], G, store lag)."""
-    monkeypatch.setenv("TSX_TRACE", "256")
-    monkeypatch.setenv("TSX_CTAS_PER_SM", "1")
     rows, cols = 8 * tiles, 32
     a = random_bits("f32", (rows, cols), tiles + stages)
     b = random_bits("f32", (rows, cols), tiles + stages + 1)
-    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, variant=variant) as plan:
+    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, variant=variant, tuning={"ctas_per_sm": 1}) as plan:
+        plan.enable_trace(256)
         da, db = to_dev(a, "f32"), to_dev(b, "f32")
         out = plan.ewise(op, da, db if op == "add" else None)
         torch.cuda.synchronize()
@@ -99,8 +98,8 @@ def _check_cta(ev, N, S, lag, op):
 @pytest.mark.parametrize("op", ["add", "copy"])
 @pytest.mark.parametrize("tiles,stages", [(1000, 1), (1000, 2), (1000, 3), (1000, 4),
                                           (456, 4), (100, 4), (160, 3)])
-def test_device_schedule_matches_the_model(tsx, monkeypatch, op, tiles, stages):
-    trace, lag = _run(tsx, monkeypatch, op, tiles, stages)
+def test_device_schedule_matches_the_model(tsx, op, tiles, stages):
+    trace, lag = _run(tsx, op, tiles, stages)
     G = trace.shape[0]
     assert G == min(tiles, G) and G <= tiles
     for c in range(G):
@@ -108,20 +107,24 @@ def test_device_schedule_matches_the_model(tsx, monkeypatch, op, tiles, stages):
         _check_cta(trace[c], N, stages, lag, op)
 
 
-def test_rank3_plan_traces_too(tsx, monkeypatch):
-    trace, lag = _run(tsx, monkeypatch, "add", 700, 3, variant="tma_rank3")
+def test_rank3_plan_traces_too(tsx):
+    trace, lag = _run(tsx, "add", 700, 3, variant="tma_rank3")
     for c in range(trace.shape[0]):
         _check_cta(trace[c], len(st.cta_tiles(700, trace.shape[0], c)), 3, lag, "add")
 
 
-def test_trace_is_refused_where_no_traced_kernel_exists(tsx, monkeypatch):
-    monkeypatch.setenv("TSX_TRACE", "64")
+def test_trace_is_refused_where_no_traced_kernel_exists(tsx):
     a = torch.zeros(64, 64, device="cuda")
     with tsx.Plan("f32", 64, 64, box=(8, 32), stages=2) as plan:
+        plan.enable_trace(64)
         with pytest.raises(tsx.TsxError) as ei:
             plan.ewise("exp", a)
         assert ei.value.code == tsx.TSX_ERR_UNSUPPORTED
-    monkeypatch.delenv("TSX_TRACE")
+        # turning tracing off again gives the plain kernel back
+        plan.enable_trace(0)
+        plan.ewise("exp", a)
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
     with tsx.Plan("f32", 64, 64, box=(8, 32), stages=2) as plan:
         plan.ewise("add", a, a)
         with pytest.raises(tsx.TsxError) as ei:

@@ -248,6 +248,17 @@ class Workload:
     def inputs(self) -> list:
         return [generate(self.rows, self.cols, self.dtype, self.dist, self.seed, t) for t in range(self.n_in)]
 
+    def inputs_range(self, start: int, n: int) -> list:
+        """Input values at the flat positions start .. start + n - 1, filled
+        chunk by chunk on a thread pool as ``generate`` does."""
+        np_dtype = np.float32 if self.dtype == "f32" else np.uint16
+        out = []
+        for t in range(self.n_in):
+            flat = np.empty(n, dtype=np_dtype)
+            _fill(flat, lambda idx, t=t: self.dist.at(idx + np.uint64(start), self.dtype, self.seed, t))
+            out.append(flat)
+        return out
+
     def inputs_at(self, flat_index: np.ndarray) -> list:
         """Input values at the given flat positions only (for sampled checks)."""
         return [self.dist.at(flat_index, self.dtype, self.seed, t) for t in range(self.n_in)]
