@@ -71,6 +71,9 @@ def parse_args(argv=None):
                    help="tuning sweep instead of the benchmark: time the workload's op over candidate boxes, stage "
                         "counts and thread counts (the plans the host accepts), check each result against the "
                         "workload's own plan bit for bit, and print one JSON line per candidate, fastest first")
+    p.add_argument("--tune", action="append", default=[], metavar="KNOB=VALUE",
+                   help="launch knob of the timed plan (threads, ctas_per_sm, store_lag, store_warps, l2_promotion); "
+                        "repeatable")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-second", action="store_true",
@@ -442,7 +445,9 @@ def run_ours(args, w, stages, variant):
     out = torch.zeros_like(dev_in[0])
     row_sums = torch.empty(w.rows, dtype=torch.float32, device="cuda")
     mode = args.mode
-    plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant)
+    tuning = {k: int(v) for k, v in (t.split("=", 1) for t in args.tune)} or None
+    plan = tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant,
+                    tuning=tuning)
     info = plan.info(w.op, row_sums=mode == "rowsum")
     peak, peak_kind = measured_peak()
     sampler = None
@@ -513,6 +518,7 @@ def run_ours(args, w, stages, variant):
             "workload": w.name + ("" if args.rows is None else f" (first {w.rows} rows)"), "op": w.op, "rows": w.rows,
             "cols": w.cols, "box": [w.box_rows, w.box_cols],
             "stages": stages, "variant": variant, "threads": info["threads"], "grid": info["grid"],
+            "store_lag": info["store_lag"], "tuning": tuning,
             "ctas_per_sm": info["ctas_per_sm"], "loads_per_operand": info["loads_per_operand"],
             "mode": mode, "algorithmic_bytes_per_step": nbytes,
             "l2": "L2 flushed between timed steps (kernel time only)" if t["small"]
@@ -730,36 +736,64 @@ def second_checks(args, second, second_data, cores):
 
 SWEEP_BOXES = [(8, 128), (16, 128), (32, 128), (64, 128), (128, 128), (8, 256), (32, 256), (64, 64), (128, 64),
                (256, 64), (16, 512), (64, 512)]
+# row sums: wide, short tiles as well (a band's rows are summed by one CTA
+# wherever its tile range allows)
+SWEEP_BOXES_ROWSUM = [(1, 1024), (2, 1024), (4, 512), (4, 1024), (8, 256), (8, 512), (8, 1024), (16, 256),
+                      (16, 512), (32, 128), (32, 256), (64, 128), (128, 128), (128, 64), (256, 64)]
 
 
 def run_sweep(args, w, stages, variant):
     """Time every accepted (box, stages, threads) candidate of the workload's
-    op and variant; each candidate's output must equal the workload's own
-    plan's output bit for bit.  Returns the result lines, fastest first."""
+    op and variant.  Elementwise: each candidate's output must equal the
+    workload's own plan's output bit for bit.  Row sums (--mode rowsum): the
+    order of additions depends on the plan, so each candidate's sums must lie
+    within the summation error bound of the workload plan's, taken from the
+    device's own sums of |x| scale (a sanity check; the tests hold every plan
+    to the oracle).  Returns the result lines, fastest first."""
     import torch
 
     import pipelined_elementwise_streaming_gb300 as tsx
 
     torch.cuda.set_device(0)
+    rowsum = args.mode == "rowsum"
     dev_in = [h.to("cuda") for h in to_host_tensors(w, torch)]
     ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))
-    ref = torch.zeros_like(dev_in[0])
-    out = torch.zeros_like(dev_in[0])
+    ref = torch.zeros(w.rows, dtype=torch.float32, device="cuda") if rowsum else torch.zeros_like(dev_in[0])
+    out = torch.zeros_like(ref)
     s = torch.cuda.current_stream().cuda_stream
+
+    def launch(plan, dst):
+        if rowsum:
+            rc = tsx.tsx_reduce_rows(plan.handle, tsx.OPS[w.op], ptrs[0], ptrs[1], ptrs[2], dst.data_ptr(), s)
+            if rc != tsx.TSX_OK:
+                raise tsx.TsxError(rc, tsx.tsx_last_error())
+        else:
+            plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], dst.data_ptr(), s)
+
     with tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant) as p:
-        p.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], ref.data_ptr(), s)
+        launch(p, ref)
     torch.cuda.synchronize()
-    nbytes = step_bytes(w, "ewise")
+    if rowsum:
+        # tolerance: twice the summation bound gamma(cols) * sum |x| of any
+        # order, with x = op(...) from the elementwise path
+        with tsx.Plan(w.dtype, w.rows, w.cols, box=(w.box_rows, w.box_cols), stages=stages, variant=variant) as p:
+            x = torch.empty_like(dev_in[0])
+            p.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], x.data_ptr(), s)
+        abs_sum = x.float().abs().sum(dim=1)
+        del x
+        tol = abs_sum * (2.0 * w.cols * 2.0 ** -24) + 1e-30
+    nbytes = step_bytes(w, args.mode)
     K = max(20, min(args.steps, 200))
     lines = []
     seen = set()
-    for box in SWEEP_BOXES:
-        for st in (2, 3, 4, 6):
-            for threads in (None, 128, 256):
+    boxes = SWEEP_BOXES_ROWSUM if rowsum else SWEEP_BOXES
+    for box in boxes:
+        for st in (2, 3, 4, 6, 8):
+            for threads in (None, 128, 256, 512):
                 tuning = None if threads is None else {"threads": threads}
                 try:
                     plan = tsx.Plan(w.dtype, w.rows, w.cols, box=box, stages=st, variant=variant, tuning=tuning)
-                    info = plan.info(w.op)
+                    info = plan.info(w.op, row_sums=rowsum)
                 except tsx.TsxError:
                     continue
                 key = (box, st, info["threads"])
@@ -769,18 +803,22 @@ def run_sweep(args, w, stages, variant):
                 seen.add(key)
                 out.zero_()
                 for _ in range(3):
-                    plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
+                    launch(plan, out)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 for _ in range(K):
-                    plan.ewise_ptr(w.op, ptrs[0], ptrs[1], ptrs[2], out.data_ptr(), s)
+                    launch(plan, out)
                 e1.record()
                 torch.cuda.synchronize()
-                ok = plan.status() == tsx.TSX_OK and torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+                if rowsum:
+                    ok = plan.status() == tsx.TSX_OK and bool(((out - ref).abs() <= tol).all())
+                else:
+                    ok = plan.status() == tsx.TSX_OK and torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
                 plan.close()
                 sec = e0.elapsed_time(e1) / 1e3 / K
-                lines.append({"sweep": w.name, "op": w.op, "variant": variant, "box": list(box), "stages": st,
-                              "threads": info["threads"], "grid": info["grid"], "gbs": round(nbytes / sec / 1e9, 1),
+                lines.append({"sweep": w.name, "mode": args.mode, "op": w.op, "variant": variant, "box": list(box),
+                              "stages": st, "threads": info["threads"], "grid": info["grid"],
+                              "ctas_per_sm": info["ctas_per_sm"], "gbs": round(nbytes / sec / 1e9, 1),
                               "same_as_workload_plan": bool(ok)})
     lines.sort(key=lambda d: -d["gbs"])
     return lines

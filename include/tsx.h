@@ -156,6 +156,9 @@ typedef struct tsx_plan_info {
     int32_t store_lag;
     /* limit of every device-side wait, in milliseconds */
     int32_t timeout_ms;
+    /* TMA variants: store warps, which take a CTA's tiles in turn (each
+     * counts store_lag in its own tiles) */
+    int32_t store_warps;
 } tsx_plan_info;
 
 /* Launch knobs of a plan.  Every field has a "planner's choice" value; start
@@ -167,9 +170,14 @@ typedef struct tsx_plan_info {
  *                multiple of 32; <= 0: the planner's choice
  *  ctas_per_sm   at most this many resident CTAs per SM in the persistent
  *                grid; <= 0: as many as occupancy allows
- *  store_lag     TMA variants: 0..3 tiles between a store's issue and the
- *                release of its stage; < 0: the planner's (1, or 2 from six
- *                stages on)
+ *  store_lag     TMA variants: 0..3 of a store warp's tiles between a
+ *                store's issue and the release of its stage; < 0: the
+ *                planner's
+ *  store_warps   TMA variants: 1 or 2 store warps, taking a CTA's tiles in
+ *                turn, so that one can wait for its store to leave shared
+ *                memory while the other stores the next tile (at most the
+ *                stage count: one stage takes one store warp); <= 0: the
+ *                planner's
  *  l2_promotion  CUtensorMapL2promotion of the tensor maps, 0..3 (none, 64,
  *                128, 256 B); < 0: 128 B, the value of TVM docs
  *                "copy_async -> tma" ("Generated TIRx IR")
@@ -177,7 +185,7 @@ typedef struct tsx_plan_info {
  *  checked       non-zero: tsx_ewise / tsx_reduce_rows synchronize the
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
-    int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked;
+    int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

@@ -62,6 +62,19 @@ int tsx_debug_plan_set_fault_tile(tsx_plan_t plan, int64_t tile);
  * default 1000 ms). */
 void tsx_debug_noalloc_set_fault(int64_t tile, int32_t timeout_ms);
 
+/* The raw shared-memory image of one staged tile: tile `tile` (row-major
+ * tile order) of operand `a` is loaded by the plan's TMA loads into a
+ * cleared slot exactly as the elementwise kernel stages it (its box split,
+ * each box on its own 1024-byte boundary, the plan's swizzle), and the
+ * slot's slot_bytes bytes (tsx_plan_get_info) are copied unchanged to
+ * `image`, a 16-byte aligned device buffer.  Bytes no load writes read as
+ * zero.  One CTA of one warp, asynchronous on `stream`; a wait that runs out
+ * is recorded in the plan's status word (image then all zero).  TMA
+ * variants only (else TSX_ERR_UNSUPPORTED); TSX_ERR_INVALID for a NULL
+ * argument or a tile outside [0, tiles); TSX_ERR_ALIGN for `a` or `image`
+ * below 16-byte alignment. */
+int tsx_debug_stage_image(tsx_plan_t plan, const void *a, int64_t tile, void *image, tsx_stream_t stream);
+
 /* Copy the trace of the plan's last traced launch to host memory.
  * events: host buffer of `capacity` uint32 words, filled with [grid][per_cta][4]
  * words (as many as fit).  *grid and *per_cta (if not NULL) receive the

@@ -15,6 +15,9 @@ structure; the library has its own implementation and never imports this.
 * ``encode_args`` -- the ``cuTensorMapEncodeTiled`` argument list in the
   order the TVM page emits it ("copy_async -> tma", "Algorithm" step 3 and
   "Generated TIRx IR").
+* ``swizzle``     -- where a byte of a box lands in shared memory under the
+  32/64/128-byte swizzle modes (CUDA's definition; the pages name the mode
+  only: parity unpinned beyond its invariants).
 * ``schedule``    -- the pre-prologue / prologue / main / epilogue /
   post-epilogue event sequence of an S-stage circular buffer (nvFuser PR
   #2833, "Loop Structure" and "Detailed Pseudo-Code").
@@ -169,6 +172,31 @@ def encode_args(dtype: str, rows: int, cols: int, sp: Split) -> tuple:
     rank = len(shape)
     return (DTYPE_NAME[dtype], rank, *reversed(shape), *reversed(strides[:-1]), *reversed(box),
             *([1] * rank), 0, SWIZZLE_CODE[sp.swizzle_bytes], L2_PROMO_128B, OOB_FILL_NONE)
+
+
+# --------------------------------------------------------------------------
+# The swizzled shared-memory layout of a box
+# --------------------------------------------------------------------------
+
+def swizzle(offset: int, swizzle_bytes: int) -> int:
+    """Shared-memory byte offset, within a box that starts on a 1024-byte
+    boundary, of the byte at row-major offset ``offset`` of the box.
+
+    The pages name the 128-byte swizzle of TMA loads (TVM docs
+    "copy_async -> tma", "Demonstration program") but print no swizzled
+    address, so this follows CUDA's documented definition of the tensor-map
+    swizzle modes: the 16-byte chunk index (address bits 4..6) is XOR-ed
+    with the 128-byte line index (bits 7..9), keeping three bits for the
+    128-byte mode, two for the 64-byte mode and one for the 32-byte mode;
+    mode 0 leaves the layout row-major.  Parity unpinned against the pages:
+    only its invariants (a permutation of whole 16-byte chunks within each
+    period, its own inverse, line 0 fixed) are checked on the CPU.
+    """
+    bits = {0: 0, 32: 1, 64: 2, 128: 3}[swizzle_bytes]
+    if not bits:
+        return offset
+    mask = (1 << bits) - 1
+    return offset ^ (((offset >> 7) & mask) << 4)
 
 
 # --------------------------------------------------------------------------

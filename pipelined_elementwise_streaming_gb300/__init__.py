@@ -55,7 +55,7 @@ class tsx_plan_info(ctypes.Structure):
                                                "slot_bytes", "stage_bytes", "smem_bytes",
                                                "ctas_per_sm", "grid", "sm_count", "block_threads")] + \
                [("pitch", ctypes.c_int64), ("tma_elem_bytes", ctypes.c_int32), ("store_lag", ctypes.c_int32),
-                ("timeout_ms", ctypes.c_int32)]
+                ("timeout_ms", ctypes.c_int32), ("store_warps", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {}
@@ -68,7 +68,7 @@ class tsx_plan_info(ctypes.Structure):
 class tsx_tuning(ctypes.Structure):
     """Launch knobs of a plan (include/tsx.h); see ``tuning()``."""
     _fields_ = [(n, ctypes.c_int32) for n in ("threads", "ctas_per_sm", "store_lag", "l2_promotion", "timeout_ms",
-                                               "checked")]
+                                               "checked", "store_warps")]
 
 
 def _load():
@@ -120,6 +120,9 @@ def _load():
     L.tsx_debug_plan_set_fault_tile.argtypes = [ctypes.c_void_p, ctypes.c_int64]
     L.tsx_debug_noalloc_set_fault.restype = None
     L.tsx_debug_noalloc_set_fault.argtypes = [ctypes.c_int64, ctypes.c_int32]
+    L.tsx_debug_stage_image.restype = ctypes.c_int
+    L.tsx_debug_stage_image.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_void_p]
     L.tsx_debug_trace.restype = ctypes.c_int
     L.tsx_debug_trace.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                   ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
@@ -150,6 +153,7 @@ tsx_debug_trace = lib.tsx_debug_trace
 tsx_debug_plan_enable_trace = lib.tsx_debug_plan_enable_trace
 tsx_debug_plan_set_fault_tile = lib.tsx_debug_plan_set_fault_tile
 tsx_debug_noalloc_set_fault = lib.tsx_debug_noalloc_set_fault
+tsx_debug_stage_image = lib.tsx_debug_stage_image
 
 
 def tsx_last_error() -> str:
@@ -162,7 +166,7 @@ def _code(table: dict, key) -> int:
 
 def tuning(**knobs) -> tsx_tuning:
     """A tsx_tuning with the planner's choices, except the knobs given
-    (threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked)."""
+    (threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps)."""
     t = tsx_tuning()
     tsx_tuning_defaults(ctypes.byref(t))
     for k, v in knobs.items():
@@ -277,6 +281,19 @@ class Plan:
         rc = tsx_debug_plan_set_fault_tile(self.handle, int(tile))
         if rc != TSX_OK:
             raise TsxError(rc, tsx_last_error())
+
+    def stage_image(self, a, tile: int):
+        """Test hook: the raw shared-memory bytes of tile `tile` of `a` as the
+        plan's TMA loads stage it (uint8 CUDA tensor of slot_bytes)."""
+        import torch
+
+        info = self.info("copy")
+        img = torch.zeros(info["slot_bytes"], dtype=torch.uint8, device=a.device)
+        s = torch.cuda.current_stream(a.device)
+        rc = tsx_debug_stage_image(self.handle, self._check(a, "a"), int(tile), img.data_ptr(), s.cuda_stream)
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+        return img
 
     def trace(self):
         """The schedule trace of the plan's last traced launch (after

@@ -484,6 +484,38 @@ int tsx_debug_trace(tsx_plan_t p, uint32_t* events, int64_t capacity, int32_t* g
     return TSX_OK;
 }
 
+int tsx_debug_stage_image(tsx_plan_t p, const void* a, int64_t tile, void* image, tsx_stream_t stream)
+{
+    if (!p || !a || !image)
+        return set_error(TSX_ERR_INVALID, "NULL plan, operand or image");
+    const Geometry& g = p->g;
+    if (!is_tma_variant(g.variant))
+        return set_error(TSX_ERR_UNSUPPORTED, "the staged image needs a TMA variant");
+    if (tile < 0 || tile >= g.tiles)
+        return set_error(TSX_ERR_INVALID, "tile outside the tensor's tiles");
+    if (alignment_of(a) < 16 || alignment_of(image) < 16)
+        return set_error(TSX_ERR_ALIGN, "a and image must be 16-byte aligned");
+    std::string why;
+    OpGeometry og;
+    int rc = make_op_geometry(g, TSX_COPY, p->max_smem, &og, &why);
+    if (rc != TSX_OK)
+        return set_error(rc, why);
+    CUtensorMap maps[4];
+    std::memset(maps, 0, sizeof maps);
+    rc = get_map(p, a, &maps[0]);
+    if (rc != TSX_OK)
+        return rc;
+    TmaArgs args;
+    tsx::fill_tma_args(g, og, p->d_status, -1, &args);
+    if (stage_image_smem(args) > size_t(p->max_smem))
+        return set_error(TSX_ERR_UNSUPPORTED, "the slot does not fit in shared memory");
+    const cudaError_t e = launch_stage_image(maps, args, tile, image, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_error(e, "kernel launch");
+    set_last_error("");
+    return TSX_OK;
+}
+
 int tsx_debug_plan_set_fault_tile(tsx_plan_t p, int64_t tile)
 {
     if (!p)

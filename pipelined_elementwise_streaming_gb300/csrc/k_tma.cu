@@ -12,11 +12,12 @@
 //               have landed (TVM docs "copy_async -> tma", "Demonstration
 //               program"; nvFuser PR #2833 "Add TMA support for circular
 //               buffering pass", "Lowering Details").
-//   warp 1      the store warp: waits until the tile is computed, each lane
-//               issues its share of the TMA stores from the stage, and lane
-//               0 hands the stage back to the producer (`empty`) once every
-//               lane's stores have finished reading shared memory.
-//   warps 2..   the compute warps: wait on `full` (parity (i / S) mod 2 for
+//   warps 1..W  the store warps (W = 1 or 2; warp 1 + w takes the CTA's
+//               tiles w, w + W, ...): each waits until its tile is computed,
+//               each lane issues its share of the TMA stores from the stage,
+//               and lane 0 hands the stage back to the producer (`empty`)
+//               once every lane's stores have finished reading shared memory.
+//   the rest    the compute warps: wait on `full` (parity (i / S) mod 2 for
 //               their i-th tile), apply the op to 16-byte vectors (f *
 //               threads + tid) of each operand's slot, write the result over
 //               operand a's slot and arrive on `computed` (TVM docs
@@ -33,10 +34,13 @@
 // issues tile i + S - 1 into stage (i + S - 1) mod S while the compute warps
 // wait on tile i in stage i mod S, and a post-epilogue that invalidates the
 // barriers; the consumers' loop over their tiles is the main loop plus the
-// epilogue.  Stage reuse is ordered by the `empty` barrier: the store warp
+// epilogue.  Stage reuse is ordered by the `empty` barrier: a store warp
 // releases tile i's stage once the bulk stores up to tile i have read shared
-// memory, which it checks `lag` tiles later (cp.async.bulk.wait_group.read)
-// so that a draining store never holds up the compute warps.
+// memory, which it checks `lag` of its own tiles later
+// (cp.async.bulk.wait_group.read) so that a draining store does not hold up
+// the next tile's stores; with two store warps the other warp stores the
+// next tile meanwhile, so each can release its stage as soon as its own
+// stores have read it.
 //
 // Every mbarrier wait is bounded in time and also gives up when another
 // thread has raised the CTA's abort flag.  A wait that runs out records
@@ -186,7 +190,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     uint32_t* trace_counter = reinterpret_cast<uint32_t*>(smem + (empty + 8u * S - base) + 4);
 
     const int warp = threadIdx.x / 32;
-    const int compute_warps = blockDim.x / 32 - 2;
+    const int role_warps = tma_role_warps(p.store_warps);
+    const int compute_warps = blockDim.x / 32 - role_warps;
     const int64_t G = gridDim.x;
     const int64_t cta = blockIdx.x;
     const int64_t N = cta < p.tiles ? (p.tiles - 1 - cta) / G + 1 : 0;
@@ -246,46 +251,53 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             for (int64_t k = first; k < issued; ++k)
                 (void)mbar_wait(full + 8u * (k % S), static_cast<uint32_t>((k / S) & 1), p.timeout_ns);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------- store warp
+    } else if (warp < role_warps) {
+        // ------------------------------------------------ store warps
+        const int W = p.store_warps;
+        const int sw = warp - 1;   // this warp takes the CTA's tiles sw, sw + W, ...
         const int n_boxes = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
         // lanes issuing stores: one per box, except that reduce-stores go out
         // from lane 0 alone (measured faster on GB300)
         const int lanes = ACC ? 1 : n_boxes < 32 ? n_boxes : 32;
         const BoxRef mine = box_ref(maps, p, lane < n_boxes ? lane : 0, 3);
-        const int lag = p.store_lag < S - 1 ? p.store_lag : S - 1;
-        TileCursor tc(p, cta, G);
-        StageCursor st, released;   // tile i and tile i - lag
-        for (int64_t i = 0; i < N; ++i) {
+        // the lag is counted in this warp's tiles: tile i releases tile
+        // i - lag W, which must come before the producer needs its stage
+        // again for tile i - lag W + S, so lag W <= S - 1
+        const int most = (S - 1) / W;
+        const int lag = p.store_lag < most ? p.store_lag : most;
+        TileCursor tc(p, cta + sw * G, W * G);
+        StageCursor st = StageCursor::at(sw, S), released = st;   // tile i and tile i - lag W
+        int64_t stored = 0;   // tiles this warp has stored
+        for (int64_t i = sw; i < N; i += W, ++stored) {
             // copy has no compute step: the loaded tile goes straight back
             const uint32_t ready = OP == TSX_COPY ? full : computed;
             if (!role_wait<kAllLanes>(ready + 8u * st.s, st.phase, p, abort_flag))
                 break;
             if (lane == 0)
                 trace_event<TRACE>(p, trace_counter, kTraceStore, i, st.s, st.phase);
-            // release tile i - lag once every lane's stores of it have read
+            // release tile i - lag W once every lane's stores of it have read
             // shared memory (lanes without boxes keep out of the bulk groups)
             if (lane < lanes) {
                 store_tile<ACC>(maps, p, tc, mine, n_boxes, lanes, base + st.s * p.stage_bytes);
                 bulk_wait_read(lag);
             }
             __syncwarp();
-            if (i >= lag) {
+            if (stored >= lag) {
                 if (lane == 0) {
-                    trace_event<TRACE>(p, trace_counter, kTraceRelease, i - lag, released.s, 0);
+                    trace_event<TRACE>(p, trace_counter, kTraceRelease, i - int64_t(lag) * W, released.s, 0);
                     mbar_arrive(empty + 8u * released.s);
                 }
-                released.next(S);
+                released.advance(W, S);
             }
             tc.next(p);
-            st.next(S);
+            st.advance(W, S);
         }
         if (lane < lanes)
             bulk_wait_all();
     } else if (OP != TSX_COPY) {
         // ---------------------------------------------- compute warps
-        const uint32_t tid = threadIdx.x - 64;
-        const uint32_t threads = blockDim.x - 64;
+        const uint32_t tid = threadIdx.x - 32u * role_warps;
+        const uint32_t threads = blockDim.x - 32u * role_warps;
         StageCursor st;
         // mixed variant: b of the next tile, loaded ahead into registers
         constexpr bool kSet = MIXED && NIN >= 2;

@@ -57,7 +57,7 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
         fallback = share < 64 ? 64 : share > cap ? cap : warps * 32;
         if (mixed) {
             const int cover = int((units + kSetUnits - 1) / kSetUnits + 31) / 32 * 32;
-            const int most = kMaxThreads - 32 * kTmaRoleWarps;
+            const int most = kMaxThreads - 32 * tma_role_warps(g.store_warps);
             fallback = fallback > cover ? fallback : cover < most ? cover : most;
         }
     }
@@ -87,6 +87,10 @@ int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
     if (t->store_lag > 3)
         return fail(why, "tuning.store_lag must be at most 3 (got %lld)", t->store_lag), TSX_ERR_INVALID;
     k->store_lag = t->store_lag;
+    if (t->store_warps > kMaxStoreWarps)
+        return fail(why, "tuning.store_warps must be at most %lld (got %lld)", kMaxStoreWarps, t->store_warps),
+               TSX_ERR_INVALID;
+    k->store_warps = t->store_warps > 0 ? t->store_warps : 0;
     if (t->l2_promotion > 3)
         return fail(why, "tuning.l2_promotion must be 0..3 (got %lld)", t->l2_promotion), TSX_ERR_INVALID;
     k->l2_promotion = t->l2_promotion < 0 ? 2 : t->l2_promotion;
@@ -223,11 +227,18 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
         g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
     }
     g->store_lag = knobs.store_lag >= 0 ? knobs.store_lag : default_store_lag(stages);
+    // A store warp waits on a stage's barrier for the phase of its tile i
+    // having seen only its own earlier tiles (i - W, i - 2 W, ...) complete.
+    // A parity wait is exact only once the stage's previous phase (tile
+    // i - S) has completed, and tiles complete in order, so W <= S.
+    g->store_warps = knobs.store_warps > 0 ? knobs.store_warps : 1;
+    if (g->store_warps > stages)
+        g->store_warps = stages;
     // the tensor maps' L2 promotion (the TVM page passes 128 B)
     g->l2_promotion = knobs.l2_promotion;
-    if (is_tma_variant(variant) && knobs.threads > kMaxThreads - 32 * kTmaRoleWarps)
+    if (is_tma_variant(variant) && knobs.threads > kMaxThreads - 32 * tma_role_warps(g->store_warps))
         return fail(why, "tuning.threads: at most %lld compute threads beside the TMA role warps",
-                    kMaxThreads - 32 * kTmaRoleWarps),
+                    kMaxThreads - 32 * tma_role_warps(g->store_warps)),
                TSX_ERR_INVALID;
     return TSX_OK;
 }
@@ -256,7 +267,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
                TSX_ERR_UNSUPPORTED;
     og->threads = default_threads(g, op, og->smem_bytes, g.slot_bytes / 16);
-    og->block_threads = og->threads + (tma ? 32 * kTmaRoleWarps : 0);
+    og->block_threads = og->threads + (tma ? 32 * tma_role_warps(g.store_warps) : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;
     const uint32_t units = g.slot_bytes / 16;
@@ -294,6 +305,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->block_threads = og.block_threads;
     info->tma_elem_bytes = g.tma_es;
     info->store_lag = is_tma_variant(g.variant) ? g.store_lag : 0;
+    info->store_warps = is_tma_variant(g.variant) ? g.store_warps : 0;
     info->timeout_ms = g.knobs.timeout_ms;
     info->vec = og.vec;
     info->outer = og.outer;
@@ -345,6 +357,7 @@ void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t
     args->bytes_per_load = uint32_t(g.bytes_per_load);
     args->vec16_per_slot = og.vec16_per_slot;
     args->store_lag = g.store_lag;
+    args->store_warps = g.store_warps;
     args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
     args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
@@ -389,6 +402,7 @@ extern "C" void tsx_tuning_defaults(tsx_tuning* t)
     t->threads = 0;
     t->ctas_per_sm = 0;
     t->store_lag = -1;
+    t->store_warps = 0;
     t->l2_promotion = -1;
     t->timeout_ms = 0;
     t->checked = 0;

@@ -16,6 +16,7 @@ struct Knobs {
     int threads = 0;
     int ctas_per_sm = 0;
     int store_lag = -1;      // < 0: default_store_lag(stages)
+    int store_warps = 0;     // 0: the planner's
     int l2_promotion = 2;    // CUtensorMapL2promotion
     int timeout_ms = 1000;
     bool checked = false;
@@ -28,7 +29,8 @@ struct Geometry {
     int64_t pitch = 0;       // elements between row starts (>= cols)
     int box_rows = 0, box_cols = 0;
     int64_t tiles_r = 0, tiles_c = 0, tiles = 0;
-    int store_lag = 1;       // TMA: tiles between a store's issue and its stage's release
+    int store_lag = 1;       // TMA: a store warp's tiles between a store's issue and its stage's release
+    int store_warps = 1;     // TMA: store warps, taking the CTA's tiles in turn
     // TMA split
     int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
     int loads_per_operand = 0, bytes_per_load = 0, swizzle_bytes = 0;

@@ -216,7 +216,16 @@ __device__ __forceinline__ void cp_async_wait(int n)
 template <int OP>
 __device__ __forceinline__ float op_f32(float a, float b, float c)
 {
-    if constexpr (OP == TSX_SQRT) return __fsqrt_rn(a);
+    if constexpr (OP == TSX_SQRT) {
+        // The square root of a negative number is NaN (IEEE 754).  Those
+        // lanes are answered by selection, and the correctly rounded square
+        // root is evaluated on 1 in their place, so it never meets a negative
+        // operand; its out-of-range handling is left to zeros, subnormals,
+        // infinities and NaN.  -0 is not negative: sqrt(-0) = -0.
+        const bool neg = a < 0.f;
+        const float r = __fsqrt_rn(neg ? 1.f : a);
+        return neg ? __uint_as_float(0x7fffffffu) : r;
+    }
     else if constexpr (OP == TSX_EXP) return expf(a);
     else if constexpr (OP == TSX_ADD) return __fadd_rn(a, b);
     else if constexpr (OP == TSX_MUL) return __fmul_rn(a, b);

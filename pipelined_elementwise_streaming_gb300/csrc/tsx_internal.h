@@ -25,7 +25,9 @@ constexpr int kSwizzleAtom = 128;      // bytes
 constexpr int kMaxDynSmem = 232448;    // 227 KiB opt-in per CTA on sm_100 / sm_103
 constexpr int kSmemPerSm = 233472;     // 228 KiB of shared memory per SM
 constexpr int kSmemPerCtaReserved = 1024;  // the system's share of each resident CTA
-constexpr int kTmaRoleWarps = 2;       // producer warp + store warp ahead of the compute warps
+constexpr int kMaxStoreWarps = 2;      // TMA: store warps beside the producer warp
+// TMA CTAs: the producer warp and the store warps come ahead of the compute warps
+TSX_HD constexpr int tma_role_warps(int store_warps) { return 1 + store_warps; }
 constexpr int kTmaBarrierBytes = 24;   // full, computed and empty mbarriers of one stage
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
@@ -53,7 +55,8 @@ struct TmaArgs {
     int64_t fault_tile;     // test hook: the producer skips this tile's loads (-1: none)
     int* status;            // device status word (TSX_OK until a wait gives up)
     uint64_t timeout_ns;    // limit of every mbarrier wait
-    int store_lag;          // tiles between a store's issue and its stage's release
+    int store_lag;          // a store warp's tiles between a store's issue and its stage's release
+    int store_warps;        // store warp w of W takes the CTA's tiles w, w + W, ...
     int promote_shift;      // log2(tensor-map element / element): box x coordinates are in map elements
     int rows, cols;         // tensor extent (< 2^31)
     int box_rows, box_cols;
@@ -137,6 +140,11 @@ const void* rowsum_kernel(int dtype, int op);
 cudaError_t launch_rowsum(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
                           const CUtensorMap* maps, const TmaArgs& args, const RowsumScratch& scratch,
                           float* row_sums);
+// Test hook (k_stage_image.cu): one warp stages tile `tile` of maps[0]'s
+// operand and copies the slot's raw bytes to `image` (slot_bytes).
+size_t stage_image_smem(const TmaArgs& args);
+cudaError_t launch_stage_image(const CUtensorMap* maps, const TmaArgs& args, int64_t tile, void* image,
+                               cudaStream_t stream);
 const void* ldgsts_kernel(int dtype, int op);
 cudaError_t launch_ldgsts(int dtype, int op, int grid, int threads, size_t smem, cudaStream_t stream,
                           const void* a, const void* b, const void* c, void* out, const CopyArgs& args);

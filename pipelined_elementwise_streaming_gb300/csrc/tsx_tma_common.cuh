@@ -77,6 +77,22 @@ struct StageCursor {
             phase ^= 1;
         }
     }
+    // The cursor of tile counter k, and a step of w tiles (w < 2 S).
+    __device__ __forceinline__ static StageCursor at(int64_t k, int S)
+    {
+        StageCursor c;
+        c.s = static_cast<uint32_t>(k % S);
+        c.phase = static_cast<uint32_t>((k / S) & 1);
+        return c;
+    }
+    __device__ __forceinline__ void advance(int w, int S)
+    {
+        s += static_cast<uint32_t>(w);
+        while (s >= static_cast<uint32_t>(S)) {
+            s -= static_cast<uint32_t>(S);
+            phase ^= 1;
+        }
+    }
 };
 
 // One box of a full tile's TMA loads (operand slot j) or stores: where it

@@ -235,3 +235,16 @@ def test_query_promoted_matches_oracle(tsx):
 def test_query_empty_tensor_is_legal(tsx):
     q = tsx.query("f32", 0, 128, (8, 32), 2, "tma", "copy")
     assert q["tiles"] == 0
+
+
+def test_query_store_warps_never_exceed_the_stages(tsx):
+    """A store warp's parity wait is exact only if the stage's previous phase
+    has completed, which holds when there are no more store warps than
+    stages: the planner clamps the knob."""
+    for stages in (1, 2, 3):
+        q = tsx.query("f32", 64, 1024, (8, 128), stages, "tma", "add", tuning={"store_warps": 2})
+        assert q["store_warps"] == min(2, stages)
+        assert q["block_threads"] == q["threads"] + 32 * (1 + q["store_warps"])
+    with pytest.raises(tsx.TsxError) as ei:
+        tsx.query("f32", 64, 1024, (8, 128), 2, "tma", "add", tuning={"store_warps": 3})
+    assert ei.value.code == tsx.TSX_ERR_INVALID

@@ -43,6 +43,7 @@ def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", tuning=None):
 
 @pytest.mark.parametrize("knob,values", [
     ("store_lag", [0, 1, 2, 3]),
+    ("store_warps", [1, 2]),
     ("l2_promotion", [0, 1, 2, 3]),
     ("threads", [32, 96, 256, 960]),
     ("ctas_per_sm", [1, 2, 3]),
@@ -62,8 +63,8 @@ def test_knobs_leave_results_unchanged(tsx, knob, values, case):
                     assert info["threads"] == q["threads"] == v
                 if knob == "ctas_per_sm":
                     assert info["ctas_per_sm"] <= v
-                if knob == "store_lag":
-                    assert info["store_lag"] == q["store_lag"] == v
+                if knob in ("store_lag", "store_warps"):
+                    assert info[knob] == q[knob] == v
                 if knob == "l2_promotion":
                     assert info["l2_promotion"] == q["l2_promotion"] == v
 
@@ -71,13 +72,14 @@ def test_knobs_leave_results_unchanged(tsx, knob, values, case):
 @pytest.mark.parametrize("lag", [0, 2, 3])
 @pytest.mark.parametrize("stages", [2, 4])
 def test_store_lag_follows_the_schedule_model(tsx, lag, stages):
-    """With a forced store lag the store warp releases tile i - lag (lag
+    """With a forced store lag one store warp releases tile i - lag (lag
     capped at S - 1) after tile i's stores; the trace must still satisfy the
-    model."""
+    model (two store warps: test_gpu_schedule_trace.py)."""
     tiles = 1000
     rows, cols = 8 * tiles, 32
     a, b = random_bits("f32", (rows, cols), lag), random_bits("f32", (rows, cols), lag + 1)
-    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, tuning={"store_lag": lag, "ctas_per_sm": 1}) as plan:
+    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, tuning={"store_lag": lag, "ctas_per_sm": 1,
+                                                                                  "store_warps": 1}) as plan:
         plan.enable_trace(256)
         out = plan.ewise("add", to_dev(a, "f32"), to_dev(b, "f32"))
         torch.cuda.synchronize()

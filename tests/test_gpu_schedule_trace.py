@@ -39,26 +39,33 @@ def tsx():
     return m
 
 
-def _run(tsx, op, tiles, stages, variant="tma"):
+def _run(tsx, op, tiles, stages, variant="tma", tuning=None):
     """fp32 [8 * tiles, 32] with 8x32 boxes: one tile per row band, at most
-    one CTA per SM.  Returns (trace [G, cap, 4], G, store lag)."""
+    one CTA per SM.  Returns (trace [G, cap, 4], effective store lag, store
+    warps)."""
     rows, cols = 8 * tiles, 32
     a = random_bits("f32", (rows, cols), tiles + stages)
     b = random_bits("f32", (rows, cols), tiles + stages + 1)
-    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, variant=variant, tuning={"ctas_per_sm": 1}) as plan:
+    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, variant=variant,
+                  tuning=dict(tuning or {}, ctas_per_sm=1)) as plan:
         plan.enable_trace(256)
         da, db = to_dev(a, "f32"), to_dev(b, "f32")
         out = plan.ewise(op, da, db if op == "add" else None)
         torch.cuda.synchronize()
         assert plan.status() == tsx.TSX_OK
         trace = plan.trace()
-        lag = min(plan.info(op)["stages"] - 1, 1)
+        info = plan.info(op)
+        W = info["store_warps"]
+        lag = min(info["store_lag"], (stages - 1) // W)
     want = oracle.ewise(op, "f32", a, b) if op == "add" else a
     compare(op, "f32", bits_of(out, "f32"), want, f"traced {op}")
-    return trace, lag
+    return trace, lag, W
 
 
-def _check_cta(ev, N, S, lag, op):
+def _check_cta(ev, N, S, lag, op, W=1):
+    """One CTA's events against the model; W store warps take the CTA's
+    tiles in turn (warp w: tiles w, w + W, ...), each releasing its tile j
+    after storing its tile j + lag."""
     ev = ev[ev[:, 1] != 0]
     assert np.array_equal(ev[:, 0], np.arange(len(ev))), "sequence numbers are not dense"
     kind, k, a, b = ev[:, 1], ev[:, 2].astype(np.int64), ev[:, 3] & 0xFFFF, ev[:, 3] >> 16
@@ -77,9 +84,19 @@ def _check_cta(ev, N, S, lag, op):
     assert loads == sim_loads
     assert list(b[kind == LOAD]) == [0] * pro + [1] * (N - pro), "prologue / main-loop split"
     stores = [(int(x), int(y)) for x, y in zip(k[kind == STORE], a[kind == STORE])]
-    assert stores == [(i, i % S) for i in range(N)]
     releases = [(int(x), int(y)) for x, y in zip(k[kind == RELEASE], a[kind == RELEASE])]
-    assert releases == [(i, i % S) for i in range(max(0, N - lag))]
+    assert sorted(stores) == [(i, i % S) for i in range(N)]
+    want_released = []
+    for w in range(W):
+        mine = list(range(w, N, W))
+        # each store warp stores its tiles in order and releases all but its last `lag`
+        assert [x for x in stores if x[0] % W == w] == [(i, i % S) for i in mine]
+        kept = mine[:max(0, len(mine) - lag)]
+        assert [x for x in releases if x[0] % W == w] == [(i, i % S) for i in kept]
+        want_released += kept
+    assert sorted(x[0] for x in releases) == sorted(want_released)
+    for i in want_released:
+        assert seq[(STORE, i)] < seq[(RELEASE, i)], f"tile {i} released before its store"
     reuses = [(int(x), int(y), int(z)) for x, y, z in zip(k[kind == REUSE], a[kind == REUSE], b[kind == REUSE])]
     assert reuses == [(i, i % S, ((i // S) - 1) & 1) for i in range(S, N)]
     if op != "copy":
@@ -99,18 +116,32 @@ def _check_cta(ev, N, S, lag, op):
 @pytest.mark.parametrize("tiles,stages", [(1000, 1), (1000, 2), (1000, 3), (1000, 4),
                                           (456, 4), (100, 4), (160, 3)])
 def test_device_schedule_matches_the_model(tsx, op, tiles, stages):
-    trace, lag = _run(tsx, op, tiles, stages)
+    trace, lag, W = _run(tsx, op, tiles, stages)
     G = trace.shape[0]
     assert G == min(tiles, G) and G <= tiles
     for c in range(G):
         N = len(st.cta_tiles(tiles, G, c))
-        _check_cta(trace[c], N, stages, lag, op)
+        _check_cta(trace[c], N, stages, lag, op, W)
+
+
+@pytest.mark.parametrize("op", ["add", "copy"])
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("store_warps,store_lag", [(1, 0), (2, 0), (2, 1)])
+def test_store_warps_follow_the_model(tsx, op, stages, store_warps, store_lag):
+    """One or two store warps, each releasing its stage `lag` of its own
+    tiles later (lag capped so that lag * W <= S - 1)."""
+    tiles = 900
+    trace, lag, W = _run(tsx, op, tiles, stages, tuning={"store_warps": store_warps, "store_lag": store_lag})
+    assert W == min(store_warps, stages) and lag == min(store_lag, (stages - 1) // W)
+    G = trace.shape[0]
+    for c in range(G):
+        _check_cta(trace[c], len(st.cta_tiles(tiles, G, c)), stages, lag, op, W)
 
 
 def test_rank3_plan_traces_too(tsx):
-    trace, lag = _run(tsx, "add", 700, 3, variant="tma_rank3")
+    trace, lag, W = _run(tsx, "add", 700, 3, variant="tma_rank3")
     for c in range(trace.shape[0]):
-        _check_cta(trace[c], len(st.cta_tiles(700, trace.shape[0], c)), 3, lag, "add")
+        _check_cta(trace[c], len(st.cta_tiles(700, trace.shape[0], c)), 3, lag, "add", W)
 
 
 def test_trace_is_refused_where_no_traced_kernel_exists(tsx):

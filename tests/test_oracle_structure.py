@@ -204,3 +204,31 @@ def test_tile_origin_row_major():
     assert st.tile_origin(0, 500, 4096, 32, 32) == (0, 0)
     assert st.tile_origin(129, 500, 4096, 32, 32) == (32, 32)
     assert st.tile_origin(16 * 128 - 1, 500, 4096, 32, 32) == (480, 4064)
+
+
+@pytest.mark.parametrize("mode,period", [(32, 256), (64, 512), (128, 1024)])
+def test_swizzle_invariants(mode, period):
+    """The swizzle model moves whole 16-byte chunks, permutes the chunks of
+    each period (its own inverse, so a bijection), keeps the first 128-byte
+    line in place, and only ever moves a chunk within its own 128-byte line.
+    (The pages print no swizzled address; these are the properties any
+    reading of "128-byte swizzle" as a chunk XOR must have.)"""
+    for base in (0, period, 5 * period):
+        images = [st.swizzle(base + o, mode) for o in range(period)]
+        assert sorted(images) == list(range(base, base + period))
+        for o in range(period):
+            x = base + o
+            y = st.swizzle(x, mode)
+            assert st.swizzle(y, mode) == x
+            assert y % 16 == x % 16 and y // 128 == x // 128
+            if o < 128:
+                assert y == x
+    # the 128-byte mode uses three line bits: lines 0..7 permute the chunks
+    # of their line in eight different ways, and line 8 starts over
+    perms = {tuple(st.swizzle(line * 128 + c * 16, 128) // 16 % 8 for c in range(8)) for line in range(8)}
+    assert len(perms) == 8
+    assert [st.swizzle(8 * 128 + c * 16, 128) for c in range(8)] == [8 * 128 + c * 16 for c in range(8)]
+
+
+def test_swizzle_mode_none_is_row_major():
+    assert all(st.swizzle(o, 0) == o for o in range(4096))
