@@ -155,7 +155,9 @@ def source_digest() -> str:
 
 def recorded_traffic(workload: str, variant: str, stages: int):
     """DRAM bytes per launch from the committed ncu summary of this kernel
-    and workload, if it was taken on the current kernel sources."""
+    and workload (``dram_bytes_per_launch[S=<stages>]``, or
+    ``dram_bytes_per_launch`` with a matching ``stages``), if it was taken on
+    the current kernel sources."""
     path = os.path.join(ROOT, "profiles", f"tma_ewise_{workload}.md")
     try:
         text = open(path).read()
@@ -166,13 +168,14 @@ def recorded_traffic(workload: str, variant: str, stages: int):
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_sources_sha256_16") != source_digest():
+    if fields.get("kernel_sources_sha256_16") != source_digest() or fields.get("variant") != variant:
         return None
-    if fields.get("variant") != variant or fields.get("stages") != str(stages):
-        return None
+    value = fields.get(f"dram_bytes_per_launch[S={stages}]")
+    if value is None and fields.get("stages") == str(stages):
+        value = fields.get("dram_bytes_per_launch")
     try:
-        return float(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(value) if value is not None else None
+    except ValueError:
         return None
 
 

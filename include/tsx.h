@@ -157,8 +157,9 @@ typedef struct tsx_plan_info {
     /* limit of every device-side wait, in milliseconds */
     int32_t timeout_ms;
     /* TMA variants: store warps, which take a CTA's tiles in turn (each
-     * counts store_lag in its own tiles) */
-    int32_t store_warps;
+     * counts store_lag in its own tiles), and how the producer and store
+     * warps wait on their mbarriers (1 every lane, 2 lane 0 alone) */
+    int32_t store_warps, role_wait;
 } tsx_plan_info;
 
 /* Launch knobs of a plan.  Every field has a "planner's choice" value; start
@@ -178,6 +179,9 @@ typedef struct tsx_plan_info {
  *                memory while the other stores the next tile (at most the
  *                stage count: one stage takes one store warp); <= 0: the
  *                planner's
+ *  role_wait     TMA variants: how the producer and store warps wait on an
+ *                mbarrier, 1 with every lane, 2 with lane 0 alone while the
+ *                others take its answer; <= 0: the planner's
  *  l2_promotion  CUtensorMapL2promotion of the tensor maps, 0..3 (none, 64,
  *                128, 256 B); < 0: 128 B, the value of TVM docs
  *                "copy_async -> tma" ("Generated TIRx IR")
@@ -185,7 +189,7 @@ typedef struct tsx_plan_info {
  *  checked       non-zero: tsx_ewise / tsx_reduce_rows synchronize the
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
-    int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps;
+    int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

@@ -177,7 +177,6 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
     constexpr int NIN = op_arity(OP);
     // operands in the stage: all of them, or all but b in the mixed variant
     constexpr int NT = MIXED ? tma_operands(TSX_TMA_MIXED, OP) : NIN;
-    constexpr bool kAllLanes = OP != TSX_EXP;   // how the producer and store warps wait
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
@@ -234,7 +233,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         // Main loop: tile k = i + S - 1 into stage k mod S, once the store
         // warp has released that stage's previous tile (k - S).
         for (; issued < N; ++issued) {
-            if (issued >= S && !role_wait<kAllLanes>(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag))
+            if (issued >= S && !role_wait(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag, p.lane0_wait != 0))
                 break;
             if (lane == 0) {
                 if (issued >= S)
@@ -271,7 +270,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         for (int64_t i = sw; i < N; i += W, ++stored) {
             // copy has no compute step: the loaded tile goes straight back
             const uint32_t ready = OP == TSX_COPY ? full : computed;
-            if (!role_wait<kAllLanes>(ready + 8u * st.s, st.phase, p, abort_flag))
+            if (!role_wait(ready + 8u * st.s, st.phase, p, abort_flag, p.lane0_wait != 0))
                 break;
             if (lane == 0)
                 trace_event<TRACE>(p, trace_counter, kTraceStore, i, st.s, st.phase);

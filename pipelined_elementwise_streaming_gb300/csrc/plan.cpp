@@ -27,7 +27,7 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units)
+int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {
     // Threads of the elementwise stage.  TMA paths: about 256 compute
     // threads per SM in all, shared by the CTAs that fit in its shared
@@ -57,18 +57,60 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
         fallback = share < 64 ? 64 : share > cap ? cap : warps * 32;
         if (mixed) {
             const int cover = int((units + kSetUnits - 1) / kSetUnits + 31) / 32 * 32;
-            const int most = kMaxThreads - 32 * tma_role_warps(g.store_warps);
+            const int most = kMaxThreads - 32 * tma_role_warps(store_warps);
             fallback = fallback > cover ? fallback : cover < most ? cover : most;
         }
     }
     return fallback;
 }
 
-int default_store_lag(int stages)
+StoreSchedule store_schedule(const Geometry& g, int op)
 {
-    // tiles between a store's issue and the release of its stage: one for
-    // shallow rings, two once there are enough stages to keep loads ahead
-    return stages >= 6 ? 2 : 1;
+    // How a stage comes back to the producer.  A store warp stores tile i
+    // and releases the stage of its tile i - lag once that tile's stores
+    // have read shared memory; with two store warps taking tiles in turn, a
+    // warp can wait for its own store (lag 0) while the other stores the
+    // next tile.  Measured on GB300 (all settings give identical results):
+    //  - 2 stages: two store warps, lag 0, for every op: with one warp the
+    //    ring holds a stage back for a whole tile (bf16 exp [16384, 16384]
+    //    4298 -> 5893 GB/s, fp32 fma [128, 2^20] 6690 -> 7135);
+    //  - 3 to 5 stages: one store warp, lag 1 (bf16 exp 6457 against 5763
+    //    at lag 0; fp32 fma 7160 at 4 stages against 6827), except that the
+    //    one-operand ops sqrt and exp at 4 or more stages take two warps at
+    //    lag 0 (bf16 exp 6545 against 5755);
+    //  - 6 stages and more: one store warp, lag 2 (fp32 fma 7129 against
+    //    6757 at lag 1).
+    // The producer and store warps of the one-operand ops sqrt and exp
+    // wait on lane 0 alone, the others with every lane (bf16 sqrt at 3
+    // stages 6502 against 6020; bf16 mul at 3 stages 6830 against 6295 the
+    // other way round).
+    const int S = g.stages;
+    const bool one_operand = op == TSX_SQRT || op == TSX_EXP;
+    StoreSchedule r;
+    if (S <= 2) {
+        r.store_warps = 2;
+        r.store_lag = 0;
+    } else if (S < 6) {
+        r.store_warps = one_operand && S >= 4 ? 2 : 1;
+        r.store_lag = r.store_warps == 2 ? 0 : 1;
+    } else {
+        r.store_warps = 1;
+        r.store_lag = 2;
+    }
+    r.lane0_wait = one_operand;
+    if (g.knobs.store_warps > 0)
+        r.store_warps = g.knobs.store_warps;
+    if (g.knobs.store_lag >= 0)
+        r.store_lag = g.knobs.store_lag;
+    if (g.knobs.role_wait > 0)
+        r.lane0_wait = g.knobs.role_wait == 2;
+    // A store warp waits on a stage's barrier for the phase of its tile i
+    // having seen only its own earlier tiles (i - W, i - 2 W, ...) complete.
+    // A parity wait is exact only once the stage's previous phase (tile
+    // i - S) has completed, and tiles complete in order, so W <= S.
+    if (r.store_warps > S)
+        r.store_warps = S;
+    return r;
 }
 
 int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
@@ -91,6 +133,9 @@ int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
         return fail(why, "tuning.store_warps must be at most %lld (got %lld)", kMaxStoreWarps, t->store_warps),
                TSX_ERR_INVALID;
     k->store_warps = t->store_warps > 0 ? t->store_warps : 0;
+    if (t->role_wait > 2)
+        return fail(why, "tuning.role_wait must be 0, 1 or 2 (got %lld)", t->role_wait), TSX_ERR_INVALID;
+    k->role_wait = t->role_wait > 0 ? t->role_wait : 0;
     if (t->l2_promotion > 3)
         return fail(why, "tuning.l2_promotion must be 0..3 (got %lld)", t->l2_promotion), TSX_ERR_INVALID;
     k->l2_promotion = t->l2_promotion < 0 ? 2 : t->l2_promotion;
@@ -226,19 +271,11 @@ int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_
         g->copy_vec_bytes = vb;
         g->slot_bytes = round_up(uint32_t(tile_bytes), 16);
     }
-    g->store_lag = knobs.store_lag >= 0 ? knobs.store_lag : default_store_lag(stages);
-    // A store warp waits on a stage's barrier for the phase of its tile i
-    // having seen only its own earlier tiles (i - W, i - 2 W, ...) complete.
-    // A parity wait is exact only once the stage's previous phase (tile
-    // i - S) has completed, and tiles complete in order, so W <= S.
-    g->store_warps = knobs.store_warps > 0 ? knobs.store_warps : 1;
-    if (g->store_warps > stages)
-        g->store_warps = stages;
     // the tensor maps' L2 promotion (the TVM page passes 128 B)
     g->l2_promotion = knobs.l2_promotion;
-    if (is_tma_variant(variant) && knobs.threads > kMaxThreads - 32 * tma_role_warps(g->store_warps))
+    if (is_tma_variant(variant) && knobs.threads > kMaxThreads - 32 * tma_role_warps(kMaxStoreWarps))
         return fail(why, "tuning.threads: at most %lld compute threads beside the TMA role warps",
-                    kMaxThreads - 32 * tma_role_warps(g->store_warps)),
+                    kMaxThreads - 32 * tma_role_warps(kMaxStoreWarps)),
                TSX_ERR_INVALID;
     return TSX_OK;
 }
@@ -266,8 +303,14 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     if (og->smem_bytes > size_t(max_smem))
         return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
                TSX_ERR_UNSUPPORTED;
-    og->threads = default_threads(g, op, og->smem_bytes, g.slot_bytes / 16);
-    og->block_threads = og->threads + (tma ? 32 * tma_role_warps(g.store_warps) : 0);
+    if (tma) {
+        const StoreSchedule ss = store_schedule(g, op);
+        og->store_warps = ss.store_warps;
+        og->store_lag = ss.store_lag;
+        og->lane0_wait = ss.lane0_wait;
+    }
+    og->threads = default_threads(g, op, og->smem_bytes, g.slot_bytes / 16, og->store_warps);
+    og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;
     const uint32_t units = g.slot_bytes / 16;
@@ -304,8 +347,9 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->threads = og.threads;
     info->block_threads = og.block_threads;
     info->tma_elem_bytes = g.tma_es;
-    info->store_lag = is_tma_variant(g.variant) ? g.store_lag : 0;
-    info->store_warps = is_tma_variant(g.variant) ? g.store_warps : 0;
+    info->store_lag = is_tma_variant(g.variant) ? og.store_lag : 0;
+    info->store_warps = is_tma_variant(g.variant) ? og.store_warps : 0;
+    info->role_wait = is_tma_variant(g.variant) ? (og.lane0_wait ? 2 : 1) : 0;
     info->timeout_ms = g.knobs.timeout_ms;
     info->vec = og.vec;
     info->outer = og.outer;
@@ -356,8 +400,9 @@ void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t
     args->stage_bytes = og.stage_bytes;
     args->bytes_per_load = uint32_t(g.bytes_per_load);
     args->vec16_per_slot = og.vec16_per_slot;
-    args->store_lag = g.store_lag;
-    args->store_warps = g.store_warps;
+    args->store_lag = og.store_lag;
+    args->store_warps = og.store_warps;
+    args->lane0_wait = og.lane0_wait ? 1 : 0;
     args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
     args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
@@ -403,6 +448,7 @@ extern "C" void tsx_tuning_defaults(tsx_tuning* t)
     t->ctas_per_sm = 0;
     t->store_lag = -1;
     t->store_warps = 0;
+    t->role_wait = 0;
     t->l2_promotion = -1;
     t->timeout_ms = 0;
     t->checked = 0;

@@ -15,8 +15,9 @@ namespace tsx {
 struct Knobs {
     int threads = 0;
     int ctas_per_sm = 0;
-    int store_lag = -1;      // < 0: default_store_lag(stages)
+    int store_lag = -1;      // < 0: the planner's
     int store_warps = 0;     // 0: the planner's
+    int role_wait = 0;       // 0: the planner's; 1: every lane waits; 2: lane 0 waits
     int l2_promotion = 2;    // CUtensorMapL2promotion
     int timeout_ms = 1000;
     bool checked = false;
@@ -29,8 +30,6 @@ struct Geometry {
     int64_t pitch = 0;       // elements between row starts (>= cols)
     int box_rows = 0, box_cols = 0;
     int64_t tiles_r = 0, tiles_c = 0, tiles = 0;
-    int store_lag = 1;       // TMA: a store warp's tiles between a store's issue and its stage's release
-    int store_warps = 1;     // TMA: store warps, taking the CTA's tiles in turn
     // TMA split
     int inner_bytes = 0, inner_elems = 0, atoms = 0, row_chunks = 0, rows_per_load = 0;
     int loads_per_operand = 0, bytes_per_load = 0, swizzle_bytes = 0;
@@ -53,6 +52,10 @@ struct OpGeometry {
     int threads = 0;         // threads of the elementwise stage ([outer, threads, vec])
     int block_threads = 0;   // threads of a CTA (TMA: + producer and store warps)
     int vec = 0, outer = 0;
+    // TMA: how the store side runs (StoreSchedule)
+    int store_warps = 1;     // store warps, taking the CTA's tiles in turn
+    int store_lag = 1;       // a store warp's tiles between a store's issue and its stage's release
+    bool lane0_wait = false; // the producer and store warps wait on lane 0 alone
 };
 
 struct TensorMapArgs {
@@ -64,8 +67,14 @@ struct TensorMapArgs {
     int swizzle = 0;   // CUtensorMapSwizzle value
 };
 
-int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units);
-int default_store_lag(int stages);
+int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps);
+// The store side of a TMA launch for `op` on geometry g: store warps, lag
+// and wait style (the planner's table, unless the knobs force them).
+struct StoreSchedule {
+    int store_warps, store_lag;
+    bool lane0_wait;
+};
+StoreSchedule store_schedule(const Geometry& g, int op);
 // Validate a tsx_tuning (NULL: all defaults) into knobs.
 int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,

@@ -236,13 +236,38 @@ __device__ __forceinline__ float op_f32(float a, float b, float c)
 __device__ __forceinline__ float u32_as_f32(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f32_as_u32(float x) { return __float_as_uint(x); }
 
-// exp of a 16-bit element, evaluated in fp32 with CUDA's fast intrinsic
-// __expf.  Its documented error is at most 2 + floor(|1.173 x|) fp32 ulps,
-// i.e. a relative error below 2^-14 for every |x| <= 100, where the results
-// of both 16-bit types are neither 0 nor infinite.  That is far below half
-// an ulp of fp16 (2^-11 relative) and bf16 (2^-8), so after rounding to the
-// element type the result is within 1 ulp of exp(x).
-__device__ __forceinline__ float exp_for_16bit(float x) { return __expf(x); }
+// exp of two 16-bit elements (widened to fp32), from the identity
+// exp(x) = (2^(x log2(e) / 2))^2.  The halved argument t = RN(x * c),
+// c = RN(log2(e) / 2), goes through the hardware base-2 exponential
+// (ex2.approx.ftz.f32, PTX ISA) and the result is squared by an ordinary
+// fp32 multiply.  Halving keeps 2^t a normal fp32 number for every result a
+// 16-bit type can hold: a bf16 result is subnormal from 2^-126 down to
+// 2^-133, where t >= -67; the square, which does not flush, produces the
+// subnormal.  Above, t > 64 squares to infinity as exp(x) overflows.
+// Error: t is within 2^-17 of x log2(e) / 2 (|t| <= 67), a relative 2^-17.5
+// on 2^t and 2^-16.5 after squaring; ex2.approx adds a few fp32 ulps,
+// doubled by the square, and the multiply one rounding.  In all well under
+// 2^-15 relative: far below half an ulp of fp16 (2^-11) and bf16 (2^-8),
+// so after rounding to the element type the result is within 1 ulp of
+// exp(x).  The multiplies run on packed pairs (mul.rn.f32x2).
+__device__ __forceinline__ float2 exp2_for_16bit(float2 x)
+{
+    const float c = 0.72134752044448170368f;   // log2(e) / 2
+    uint64_t v, cc, t2;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x.x), "f"(x.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t2) : "l"(v), "l"(cc));
+    float t0, t1, e0, e1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(t0), "=f"(t1) : "l"(t2));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+    uint64_t e, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(e) : "f"(e0), "f"(e1));
+    asm("mul.rn.f32x2 %0, %1, %1;" : "=l"(r) : "l"(e));
+    float2 out;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(out.x), "=f"(out.y) : "l"(r));
+    return out;
+}
 
 // Two 16-bit elements packed in 32 bits (low half first).  fma and sqrt use
 // the native 16-bit instructions (one rounding of the exact result); the
@@ -263,10 +288,12 @@ __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
             float2 fb = make_float2(0.f, 0.f);
             if constexpr (OP == TSX_ADD || OP == TSX_MUL)
                 fb = __half22float2(*reinterpret_cast<const __half2*>(&b));
-            if constexpr (OP == TSX_EXP)
-                r = __floats2half2_rn(exp_for_16bit(fa.x), exp_for_16bit(fa.y));
-            else
+            if constexpr (OP == TSX_EXP) {
+                const float2 e = exp2_for_16bit(fa);
+                r = __floats2half2_rn(e.x, e.y);
+            } else {
                 r = __floats2half2_rn(op_f32<OP>(fa.x, fb.x, 0.f), op_f32<OP>(fa.y, fb.y, 0.f));
+            }
         }
         return *reinterpret_cast<uint32_t*>(&r);
     } else {
@@ -282,10 +309,12 @@ __device__ __forceinline__ uint32_t op_x2(uint32_t a, uint32_t b, uint32_t c)
             float2 fb = make_float2(0.f, 0.f);
             if constexpr (OP == TSX_ADD || OP == TSX_MUL)
                 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
-            if constexpr (OP == TSX_EXP)
-                r = __floats2bfloat162_rn(exp_for_16bit(fa.x), exp_for_16bit(fa.y));
-            else
+            if constexpr (OP == TSX_EXP) {
+                const float2 e = exp2_for_16bit(fa);
+                r = __floats2bfloat162_rn(e.x, e.y);
+            } else {
                 r = __floats2bfloat162_rn(op_f32<OP>(fa.x, fb.x, 0.f), op_f32<OP>(fa.y, fb.y, 0.f));
+            }
         }
         return *reinterpret_cast<uint32_t*>(&r);
     }

@@ -57,6 +57,7 @@ struct TmaArgs {
     uint64_t timeout_ns;    // limit of every mbarrier wait
     int store_lag;          // a store warp's tiles between a store's issue and its stage's release
     int store_warps;        // store warp w of W takes the CTA's tiles w, w + W, ...
+    int lane0_wait;         // 1: the producer and store warps wait on lane 0 alone
     int promote_shift;      // log2(tensor-map element / element): box x coordinates are in map elements
     int rows, cols;         // tensor extent (< 2^31)
     int box_rows, box_cols;

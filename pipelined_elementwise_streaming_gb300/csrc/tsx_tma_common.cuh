@@ -195,23 +195,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     }
 }
 
-// A wait of the producer or store warp, with one answer for the whole warp.
-// ALL_LANES: every lane waits on the barrier itself; otherwise lane 0 waits
-// and the others take its answer.  Which is faster depends on the compute
-// stage beside it: every op streams faster with all lanes waiting except
-// exp, whose fp32 evaluation streams faster with lane 0 alone waiting
-// (measured on GB300 for both 16-bit and fp32 tensors).
-template <bool ALL_LANES>
-__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, const TmaArgs& p, volatile int* abort_flag)
+// A wait of the producer or store warp, with one answer for the whole warp:
+// every lane waits on the barrier itself, or (lane0) lane 0 waits and the
+// others take its answer.  Which is faster depends on the launch (measured
+// on GB300; the planner chooses, see store_schedule in plan.cpp).
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, const TmaArgs& p, volatile int* abort_flag,
+                                          bool lane0)
 {
-    if constexpr (ALL_LANES) {
+    if (!lane0)
         return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
-    } else {
-        bool ok = true;
-        if ((threadIdx.x & 31) == 0)
-            ok = wait_or_abort(bar, parity, p, abort_flag);
-        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    }
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = wait_or_abort(bar, parity, p, abort_flag);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 }  // namespace dev

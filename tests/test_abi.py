@@ -117,7 +117,8 @@ def test_query_workload_plans(tsx):
     assert (q["loads_per_operand"], q["tx_bytes"], q["box_dim"][:2]) == (2, 32768, [64, 128])
     q = tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")
     assert (q["vec"], q["tiles"]) == (4, 16 * 128)
-    assert q["block_threads"] == q["threads"] + 64        # + producer warp and store warp
+    # + the producer warp and the store warps
+    assert q["block_threads"] == q["threads"] + 32 * (1 + q["store_warps"])
 
 
 def test_query_partition_of_the_smem_sqrt_demo(tsx):
@@ -248,3 +249,20 @@ def test_query_store_warps_never_exceed_the_stages(tsx):
     with pytest.raises(tsx.TsxError) as ei:
         tsx.query("f32", 64, 1024, (8, 128), 2, "tma", "add", tuning={"store_warps": 3})
     assert ei.value.code == tsx.TSX_ERR_INVALID
+
+
+@pytest.mark.parametrize("op,stages,want", [
+    # (store warps, lag, wait style: 1 every lane, 2 lane 0)
+    ("fma", 2, (2, 0, 1)), ("fma", 3, (1, 1, 1)), ("fma", 4, (1, 1, 1)), ("fma", 6, (1, 2, 1)),
+    ("exp", 2, (2, 0, 2)), ("exp", 3, (1, 1, 2)), ("exp", 4, (2, 0, 2)), ("exp", 8, (1, 2, 2)),
+    ("sqrt", 4, (2, 0, 2)), ("copy", 2, (2, 0, 1)), ("copy", 4, (1, 1, 1)), ("mul", 3, (1, 1, 1)),
+    ("exp", 1, (1, 0, 2)),
+])
+def test_query_store_schedule(tsx, op, stages, want):
+    """The planner's store side per op and stage count, and the knobs that
+    override it (the table is the planner's, from GB300 measurements)."""
+    q = tsx.query("bf16", 256, 4096, (32, 128), stages, "tma", op)
+    assert (q["store_warps"], q["store_lag"], q["role_wait"]) == want
+    f = tsx.query("bf16", 256, 4096, (32, 128), stages, "tma", op,
+                  tuning={"store_warps": 1, "store_lag": 1, "role_wait": 1})
+    assert (f["store_warps"], f["store_lag"], f["role_wait"]) == (1, 1, 1)

@@ -141,3 +141,29 @@ def test_clock_sampler_regions_without_nvml():
     s.stop()
     r = s.region(0.0, 1e12)
     assert r["samples"] == 0 or r["sm_mhz"] is not None
+
+
+def test_recorded_traffic_per_stage(tmp_path, monkeypatch):
+    """The roofline's traffic comes from a committed profile summary only
+    while its kernel-source hash matches, per stage count."""
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    digest = bench.source_digest()
+    (prof / "tma_ewise_w.md").write_text(
+        f"- kernel_sources_sha256_16: `{digest}`\n- variant: `tma`\n"
+        "- dram_bytes_per_launch[S=2]: `100`\n- dram_bytes_per_launch[S=3]: `200`\n")
+    (prof / "tma_ewise_old.md").write_text(
+        "- kernel_sources_sha256_16: `0000000000000000`\n- variant: `tma`\n- stages: `4`\n"
+        "- dram_bytes_per_launch: `300`\n")
+    (prof / "tma_ewise_one.md").write_text(
+        f"- kernel_sources_sha256_16: `{digest}`\n- variant: `tma`\n- stages: `4`\n"
+        "- dram_bytes_per_launch: `400`\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_digest", lambda: digest)
+    assert bench.recorded_traffic("w", "tma", 2) == 100.0
+    assert bench.recorded_traffic("w", "tma", 3) == 200.0
+    assert bench.recorded_traffic("w", "tma", 4) is None
+    assert bench.recorded_traffic("w", "tma_rank3", 2) is None
+    assert bench.recorded_traffic("old", "tma", 4) is None        # taken on other kernel sources
+    assert bench.recorded_traffic("one", "tma", 4) == 400.0
+    assert bench.recorded_traffic("missing", "tma", 4) is None
