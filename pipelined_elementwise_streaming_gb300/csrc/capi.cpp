@@ -196,8 +196,8 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
             return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (blocks < 1)
             return set_error(TSX_ERR_UNSUPPORTED, "the kernel cannot be resident with this shared memory / threads");
-        if (p->g.knobs.ctas_per_sm > 0 && blocks > p->g.knobs.ctas_per_sm)
-            blocks = p->g.knobs.ctas_per_sm;
+        if (L.og.ctas_cap > 0 && blocks > L.og.ctas_cap)
+            blocks = L.og.ctas_cap;
         L.ctas_per_sm = blocks;
         // persistent grid: every resident CTA slot once, no more CTAs than tiles
         const int64_t slots = int64_t(p->sm_count) * blocks;

@@ -82,7 +82,7 @@ __device__ __forceinline__ void add_unit(float& part, const TmaArgs& p, const ui
     const uint4 va = S[u];
     const uint4 vb = NIN > 1 ? S[p.slot_bytes / 16 + u] : va;
     const uint4 vc = NIN > 2 ? S[2 * (p.slot_bytes / 16) + u] : va;
-    add_vec<DT>(part, op_vec16<DT, OP>(va, vb, vc));
+    add_vec<DT>(part, op_vec16<DT, OP, true>(va, vb, vc));
 }
 
 // Whether unit u of a staged slot holds columns inside the tensor (a ragged

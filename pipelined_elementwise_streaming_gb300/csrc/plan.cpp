@@ -29,6 +29,7 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {
+    (void)op;
     // Threads of the elementwise stage.  TMA paths: about 256 compute
     // threads per SM in all, shared by the CTAs that fit in its shared
     // memory, between 2 and 8 compute warps per CTA (beside the producer
@@ -40,7 +41,6 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
     // 16-byte units of the slot, between 128 threads (the TVM ldgsts
     // demonstration program's count, which its 128x32 fp16 tile gets) and
     // 512.  A forced count (tsx_tuning.threads) wins.
-    (void)op;
     const int variant = g.variant;
     const bool tma = is_tma_variant(variant);
     if (g.knobs.threads > 0)
@@ -64,7 +64,29 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
     return fallback;
 }
 
-StoreSchedule store_schedule(const Geometry& g, int op)
+// One-operand compute ops (their compute warps do more per byte than copy
+// and reach a stage from one operand only).
+static bool one_operand_compute(int op) { return op == TSX_SQRT || op == TSX_EXP; }
+
+static bool two_large_ctas(const Geometry& g, int op, uint32_t stage_bytes)
+{
+    return is_tma_variant(g.variant) && g.stages == 2 && one_operand_compute(op) && stage_bytes >= 16384;
+}
+
+int default_ctas_cap(const Geometry& g, int op, uint32_t stage_bytes)
+{
+    // A two-stage ring of large one-operand tiles streams best from two CTAs
+    // per SM of 256 compute threads: bf16 exp [16384, 16384] with 128x128
+    // tiles (32 KB stages) 6467 GB/s against 5760 with the three CTAs that
+    // fit, and bf16 sqrt 6282 against 5683 (GB300; at one CTA 4352 / 4222).
+    // Smaller stages and other ops keep every CTA that fits (fp32 fma with
+    // 12 KB stages: 7177 GB/s at six CTAs, 4520 at two).
+    if (g.knobs.ctas_per_sm > 0)
+        return g.knobs.ctas_per_sm;
+    return two_large_ctas(g, op, stage_bytes) ? 2 : 0;
+}
+
+StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes)
 {
     // How a stage comes back to the producer.  A store warp stores tile i
     // and releases the stage of its tile i - lag once that tile's stores
@@ -76,8 +98,9 @@ StoreSchedule store_schedule(const Geometry& g, int op)
     //    4298 -> 5893 GB/s, fp32 fma [128, 2^20] 6690 -> 7135);
     //  - 3 to 5 stages: one store warp, lag 1 (bf16 exp 6457 against 5763
     //    at lag 0; fp32 fma 7160 at 4 stages against 6827), except that the
-    //    one-operand ops sqrt and exp at 4 or more stages take two warps at
-    //    lag 0 (bf16 exp 6545 against 5755);
+    //    one-operand ops sqrt and exp with stages of 16 KB or more take two
+    //    warps at lag 0 from 4 stages (bf16 exp 6545 against 5755; with
+    //    4 KB stages fp32 exp keeps lag 1, 6415 against 6282);
     //  - 6 stages and more: one store warp, lag 2 (fp32 fma 7129 against
     //    6757 at lag 1).
     // The producer and store warps of the one-operand ops sqrt and exp
@@ -85,13 +108,13 @@ StoreSchedule store_schedule(const Geometry& g, int op)
     // stages 6502 against 6020; bf16 mul at 3 stages 6830 against 6295 the
     // other way round).
     const int S = g.stages;
-    const bool one_operand = op == TSX_SQRT || op == TSX_EXP;
+    const bool one_operand = one_operand_compute(op);
     StoreSchedule r;
     if (S <= 2) {
         r.store_warps = 2;
         r.store_lag = 0;
     } else if (S < 6) {
-        r.store_warps = one_operand && S >= 4 ? 2 : 1;
+        r.store_warps = one_operand && S >= 4 && stage_bytes >= 16384 ? 2 : 1;
         r.store_lag = r.store_warps == 2 ? 0 : 1;
     } else {
         r.store_warps = 1;
@@ -304,12 +327,15 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         return fail(why, "%lld bytes of shared memory needed, %lld available", (long long)og->smem_bytes, max_smem),
                TSX_ERR_UNSUPPORTED;
     if (tma) {
-        const StoreSchedule ss = store_schedule(g, op);
+        const StoreSchedule ss = store_schedule(g, op, og->stage_bytes);
         og->store_warps = ss.store_warps;
         og->store_lag = ss.store_lag;
         og->lane0_wait = ss.lane0_wait;
     }
+    og->ctas_cap = default_ctas_cap(g, op, og->stage_bytes);
     og->threads = default_threads(g, op, og->smem_bytes, g.slot_bytes / 16, og->store_warps);
+    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && two_large_ctas(g, op, og->stage_bytes))
+        og->threads = 256;   // the two large CTAs of a two-stage sqrt / exp ring (default_ctas_cap)
     og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;

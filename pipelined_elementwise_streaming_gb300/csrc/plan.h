@@ -56,6 +56,7 @@ struct OpGeometry {
     int store_warps = 1;     // store warps, taking the CTA's tiles in turn
     int store_lag = 1;       // a store warp's tiles between a store's issue and its stage's release
     bool lane0_wait = false; // the producer and store warps wait on lane 0 alone
+    int ctas_cap = 0;        // at most this many CTAs per SM (0: occupancy)
 };
 
 struct TensorMapArgs {
@@ -74,7 +75,10 @@ struct StoreSchedule {
     int store_warps, store_lag;
     bool lane0_wait;
 };
-StoreSchedule store_schedule(const Geometry& g, int op);
+StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes);
+// At most this many CTAs per SM for `op` (0: as occupancy allows), unless
+// the knobs say otherwise.
+int default_ctas_cap(const Geometry& g, int op, uint32_t stage_bytes);
 // Validate a tsx_tuning (NULL: all defaults) into knobs.
 int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,

@@ -251,18 +251,33 @@ def test_query_store_warps_never_exceed_the_stages(tsx):
     assert ei.value.code == tsx.TSX_ERR_INVALID
 
 
-@pytest.mark.parametrize("op,stages,want", [
+@pytest.mark.parametrize("op,stages,box,want", [
     # (store warps, lag, wait style: 1 every lane, 2 lane 0)
-    ("fma", 2, (2, 0, 1)), ("fma", 3, (1, 1, 1)), ("fma", 4, (1, 1, 1)), ("fma", 6, (1, 2, 1)),
-    ("exp", 2, (2, 0, 2)), ("exp", 3, (1, 1, 2)), ("exp", 4, (2, 0, 2)), ("exp", 8, (1, 2, 2)),
-    ("sqrt", 4, (2, 0, 2)), ("copy", 2, (2, 0, 1)), ("copy", 4, (1, 1, 1)), ("mul", 3, (1, 1, 1)),
-    ("exp", 1, (1, 0, 2)),
+    ("fma", 2, (32, 128), (2, 0, 1)), ("fma", 3, (32, 128), (1, 1, 1)), ("fma", 4, (32, 128), (1, 1, 1)),
+    ("fma", 6, (32, 128), (1, 2, 1)),
+    ("exp", 2, (128, 128), (2, 0, 2)), ("exp", 3, (128, 128), (1, 1, 2)), ("exp", 4, (128, 128), (2, 0, 2)),
+    ("exp", 4, (32, 128), (1, 1, 2)),         # stages under 16 KB keep lag 1
+    ("exp", 8, (32, 128), (1, 2, 2)), ("sqrt", 4, (128, 128), (2, 0, 2)),
+    ("copy", 2, (32, 128), (2, 0, 1)), ("copy", 4, (128, 128), (1, 1, 1)), ("mul", 3, (32, 128), (1, 1, 1)),
+    ("exp", 1, (32, 128), (1, 0, 2)),
 ])
-def test_query_store_schedule(tsx, op, stages, want):
-    """The planner's store side per op and stage count, and the knobs that
-    override it (the table is the planner's, from GB300 measurements)."""
-    q = tsx.query("bf16", 256, 4096, (32, 128), stages, "tma", op)
+def test_query_store_schedule(tsx, op, stages, box, want):
+    """The planner's store side per op, stage count and stage size, and the
+    knobs that override it (the table is the planner's, from GB300
+    measurements)."""
+    q = tsx.query("bf16", 256, 4096, box, stages, "tma", op)
     assert (q["store_warps"], q["store_lag"], q["role_wait"]) == want
-    f = tsx.query("bf16", 256, 4096, (32, 128), stages, "tma", op,
+    f = tsx.query("bf16", 256, 4096, box, stages, "tma", op,
                   tuning={"store_warps": 1, "store_lag": 1, "role_wait": 1})
     assert (f["store_warps"], f["store_lag"], f["role_wait"]) == (1, 1, 1)
+
+
+def test_query_two_stage_large_tiles_take_256_threads(tsx):
+    """A two-stage ring of 32 KB sqrt / exp tiles runs as at most two CTAs
+    per SM of 256 compute threads (the CTA cap shows in a plan's launch on a
+    GPU); other ops, smaller stages and forced knobs keep the usual share."""
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "exp")["threads"] == 256
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "sqrt")["threads"] == 256
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "copy")["threads"] == 64
+    assert tsx.query("bf16", 16384, 16384, (64, 64), 2, "tma", "exp")["threads"] == 64
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "exp", tuning={"ctas_per_sm": 3})["threads"] == 64

@@ -202,3 +202,34 @@ def test_rowsum_wait_timeout_is_reported(tsx):
         bad.close()
     got = _rowsum(tsx, "f32", rows, cols, (8, 128), 3, "tma", "copy", [a])
     _check(got, "copy", "f32", [a], cols, "after the timeout")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_rowsum_exp_meets_every_16bit_input(tsx, dtype):
+    """The row reduction evaluates exp its own way (halving and squaring), so
+    it is checked on every 16-bit input: row r is bit pattern r followed by
+    seven -inf.  exp(-inf) = 0 adds nothing, so the row sum is the reduction's
+    exp of pattern r rounded into the element type and widened exactly; it
+    must be within the exp bound of the oracle's (NaN for NaN)."""
+    rows, cols = 1 << 16, 8
+    neg_inf = 0xFC00 if dtype == "f16" else 0xFF80
+    a = np.full((rows, cols), neg_inf, dtype=np.uint16)
+    a[:, 0] = np.arange(rows, dtype=np.uint32).astype(np.uint16)
+    for box, stages in (((256, 8), 2), ((64, 8), 3)):
+        got = _rowsum(tsx, dtype, rows, cols, box, stages, "tma", "exp", [a]).astype(np.float32)
+        nan = np.isnan(got)
+        fin = got[~nan]
+        if dtype == "bf16":
+            bits = (got.view(np.uint32) >> 16).astype(np.uint16)
+            assert np.array_equal((bits[~nan].astype(np.uint32) << 16), fin.view(np.uint32)), "not a widened bf16"
+            bits[nan] = 0x7FC0
+        else:
+            h = got.astype(np.float16)
+            assert np.array_equal(h[~nan].astype(np.float32).view(np.uint32), fin.view(np.uint32)), \
+                "not a widened fp16"
+            bits = h.view(np.uint16).copy()
+            bits[nan] = 0x7E00
+        want = oracle.ewise("exp", dtype, a[:, 0])
+        d = oracle.ulp_distance(bits, want, dtype)
+        bad = np.flatnonzero(d > oracle.EXP_ULP_BOUND[dtype])
+        assert bad.size == 0, f"box {box}: {bad.size} inputs off, first {int(a[bad[0], 0]):#06x}"
