@@ -610,11 +610,12 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
         if (align < 16)
             return set_error(TSX_ERR_ALIGN, "TMA needs 16-byte aligned base pointers");
         const bool mixed = mixed_launch(g.variant, op);
-        // operands of the TMA ring in slot order; b is read directly when mixed
+        // operands of the TMA ring in slot order; b is read directly when
+        // mixed, and its map (slot 2) serves the L2 prefetch only
         const void* staged[4] = {a, b, c, out};
         if (mixed) {
             staged[1] = c;
-            staged[2] = nullptr;
+            staged[2] = b;
         }
         CUtensorMap maps[4];
         std::memset(maps, 0, sizeof maps);

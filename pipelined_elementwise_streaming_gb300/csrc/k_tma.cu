@@ -98,38 +98,76 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
 // computes; any further units load on use.  The planner gives the mixed
 // variant enough threads that every unit is among the first kSetUnits.
 
-// b at staged unit u of the tile with boxes tb (zero outside the tensor and
-// in the padding after a box).  Loaded through L2 only: b may be the output,
-// whose other tiles TMA stores overwrite meanwhile.
+// The producer of the mixed variant asks the TMA unit to bring b's boxes of
+// each tile it loads into L2 (tensor map slot 2 holds b's map), S - 2 tiles
+// before the compute threads read them into registers, so those plain loads
+// mostly hit L2.  Measured on GB300, fp32 fma [128, 2^20]: 6547 -> 6765 GB/s
+// at 4 stages, 6010 -> 6354 at 6, unchanged at 3.
+__device__ __forceinline__ void prefetch_b_tile(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc)
+{
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int per_op = p.row_chunks * p.atoms;
+    for (int L = lane; L < per_op; L += 32) {
+        const TileBoxes b = boxes_at(p, tc.band, tc.ct);
+        const int r = L / p.atoms, a = L - r * p.atoms;
+        if (r < b.chunks && a < b.atoms)
+            tma_prefetch_l2_2d(&maps.m[2], b.col0 + a * p.inner_elems, b.row0 + r * p.rows_per_load);
+    }
+}
+
+// Where unit u of a staged slot sits in its tile: every tile of a plan is
+// staged with the same layout, so the unit holds the same (row, column) of
+// every tile.  The box, the swizzle inverse and the divisions are worked out
+// once per thread, not per tile.  Padding after a box has row -1.
+struct UnitPos {
+    int row, col;
+};
+
 template <int DT>
-__device__ __forceinline__ uint4 load_b_unit(const TmaArgs& p, const TileBoxes& tb, uint32_t u)
+__device__ __forceinline__ UnitPos unit_pos(const TmaArgs& p, uint32_t u)
 {
     constexpr int ES = DT == TSX_F32 ? 4 : 2;
     const uint32_t inner_bytes = static_cast<uint32_t>(p.inner_elems) * ES;
     const uint32_t off = u * 16;
     const uint32_t load = off / p.load_smem_bytes;
     const uint32_t within = off - load * p.load_smem_bytes;
-    uint4 vb = make_uint4(0, 0, 0, 0);
-    if (within < p.box_bytes) {
+    UnitPos q{-1, 0};
+    if (u < p.vec16_per_slot && within < p.box_bytes) {
         const uint32_t lo = unswizzle(within, p.swizzle_mask);
-        const int64_t row = tb.row0 + static_cast<int64_t>(load / p.atoms) * p.rows_per_load + lo / inner_bytes;
-        const int64_t col = tb.col0 + static_cast<int64_t>(load % p.atoms) * p.inner_elems + (lo % inner_bytes) / ES;
-        if (row < p.rows && col < p.cols)
-            vb = __ldcg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.set_operand) +
-                                                       (row * p.pitch + col) * ES));
+        q.row = static_cast<int>((load / p.atoms) * p.rows_per_load + lo / inner_bytes);
+        q.col = static_cast<int>((load % p.atoms) * p.inner_elems + (lo % inner_bytes) / ES);
     }
+    return q;
+}
+
+// b at the unit at position q of the tile with boxes tb (zero outside the
+// tensor and in the padding after a box).  Loaded through L2 only: b may be
+// the output, whose other tiles TMA stores overwrite meanwhile.
+template <int DT>
+__device__ __forceinline__ uint4 load_b_at(const TmaArgs& p, const TileBoxes& tb, const UnitPos& q)
+{
+    constexpr int ES = DT == TSX_F32 ? 4 : 2;
+    uint4 vb = make_uint4(0, 0, 0, 0);
+    const int64_t row = static_cast<int64_t>(tb.row0) + q.row;
+    const int64_t col = static_cast<int64_t>(tb.col0) + q.col;
+    if (q.row >= 0 && row < p.rows && col < p.cols)
+        vb = __ldcg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.set_operand) + (row * p.pitch + col) * ES));
     return vb;
 }
 
 template <int DT>
-__device__ __forceinline__ void load_b_ahead(const TmaArgs& p, const TileBoxes& tb, uint32_t tid, uint32_t threads,
+__device__ __forceinline__ uint4 load_b_unit(const TmaArgs& p, const TileBoxes& tb, uint32_t u)
+{
+    return load_b_at<DT>(p, tb, unit_pos<DT>(p, u));
+}
+
+template <int DT>
+__device__ __forceinline__ void load_b_ahead(const TmaArgs& p, const TileBoxes& tb, const UnitPos (&pos)[kSetUnits],
                                              uint4 (&v)[kSetUnits])
 {
 #pragma unroll
-    for (int k = 0; k < kSetUnits; ++k) {
-        const uint32_t u = tid + k * threads;
-        v[k] = u < p.vec16_per_slot ? load_b_unit<DT>(p, tb, u) : make_uint4(0, 0, 0, 0);
-    }
+    for (int k = 0; k < kSetUnits; ++k)
+        v[k] = load_b_at<DT>(p, tb, pos[k]);
 }
 
 // The op on one staged tile of the mixed variant: a (and c) from the slots,
@@ -172,7 +210,8 @@ __device__ __forceinline__ void trace_event(const TmaArgs& p, uint32_t* counter,
 }
 
 template <int DT, int OP, bool MIXED, bool ACC, bool TRACE = false>
-__global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__ TmaMaps maps, const TmaArgs p)
+__global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
+    tma_ewise(const __grid_constant__ TmaMaps maps, const TmaArgs p)
 {
     constexpr int NIN = op_arity(OP);
     // operands in the stage: all of them, or all but b in the mixed variant
@@ -227,6 +266,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
             if (lane == 0)
                 trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 0);
             issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+            if constexpr (MIXED && NIN >= 2)
+                prefetch_b_tile(maps, p, tc);
             tc.next(p);
             st.next(S);
         }
@@ -241,6 +282,8 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
                 trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 1);
             }
             issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+            if constexpr (MIXED && NIN >= 2)
+                prefetch_b_tile(maps, p, tc);
             tc.next(p);
             st.next(S);
         }
@@ -301,10 +344,14 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
         // mixed variant: b of the next tile, loaded ahead into registers
         constexpr bool kSet = MIXED && NIN >= 2;
         uint4 b_next[kSetUnits];
+        UnitPos b_pos[kSetUnits];
         TileCursor tc(p, cta, G);
         if constexpr (kSet) {
+#pragma unroll
+            for (int k = 0; k < kSetUnits; ++k)
+                b_pos[k] = unit_pos<DT>(p, tid + k * threads);
             if (N > 0)
-                load_b_ahead<DT>(p, boxes_at(p, tc.band, tc.ct), tid, threads, b_next);
+                load_b_ahead<DT>(p, boxes_at(p, tc.band, tc.ct), b_pos, b_next);
         }
         for (int64_t i = 0; i < N; ++i) {
             uint4 b_cur[kSetUnits];
@@ -316,7 +363,7 @@ __global__ void __launch_bounds__(kMaxThreads) tma_ewise(const __grid_constant__
                 tb = boxes_at(p, tc.band, tc.ct);
                 tc.next(p);
                 if (i + 1 < N)
-                    load_b_ahead<DT>(p, boxes_at(p, tc.band, tc.ct), tid, threads, b_next);
+                    load_b_ahead<DT>(p, boxes_at(p, tc.band, tc.ct), b_pos, b_next);
             }
             if (!wait_or_abort(full + 8u * st.s, st.phase, p, abort_flag))
                 break;

@@ -57,7 +57,7 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
         fallback = share < 64 ? 64 : share > cap ? cap : warps * 32;
         if (mixed) {
             const int cover = int((units + kSetUnits - 1) / kSetUnits + 31) / 32 * 32;
-            const int most = kMaxThreads - 32 * tma_role_warps(store_warps);
+            const int most = kMixedMaxThreads - 32 * tma_role_warps(store_warps);
             fallback = fallback > cover ? fallback : cover < most ? cover : most;
         }
     }
@@ -334,6 +334,11 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     }
     og->ctas_cap = default_ctas_cap(g, op, og->stage_bytes);
     og->threads = default_threads(g, op, og->smem_bytes, g.slot_bytes / 16, og->store_warps);
+    if (g.variant == TSX_TMA_MIXED && og->n_in >= 2 &&
+        og->threads + 32 * tma_role_warps(og->store_warps) > kMixedMaxThreads)
+        return fail(why, "the mixed variant runs at most %lld threads per CTA (%lld asked)", kMixedMaxThreads,
+                    og->threads + 32 * tma_role_warps(og->store_warps)),
+               TSX_ERR_UNSUPPORTED;
     if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && two_large_ctas(g, op, og->stage_bytes))
         og->threads = 256;   // the two large CTAs of a two-stage sqrt / exp ring (default_ctas_cap)
     og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);

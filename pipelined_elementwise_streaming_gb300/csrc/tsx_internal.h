@@ -19,6 +19,9 @@ namespace tsx {
 
 constexpr int kMaxStages = 16;
 constexpr int kMaxThreads = 1024;
+// CTA threads of the mixed variant's kernel (its compute threads hold b in
+// registers one tile ahead: the lower bound leaves them 102 registers)
+constexpr int kMixedMaxThreads = 640;
 constexpr int kSmemAlign = 1024;       // 128-B swizzle pattern period
 constexpr int kBoxMax = 256;           // per TMA box dimension
 constexpr int kSwizzleAtom = 128;      // bytes
