@@ -335,7 +335,7 @@ def time_steps(torch, tsx, w, plan, mode, dev_in, out, row_sums, K, W, sampler):
     sh = stream.cuda_stream
     ptrs = [t.data_ptr() for t in dev_in] + [None] * (3 - len(dev_in))
     po = out.data_ptr()
-    small = nbytes < 4 * L2_BYTES
+    small = nbytes < 2 * L2_BYTES   # inputs of twice the L2 or more stream through it without reuse
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
     op_code = tsx.OPS[w.op] | (tsx.TSX_ACCUMULATE if mode == "accumulate" else 0)
 
