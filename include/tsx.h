@@ -170,15 +170,18 @@ typedef struct tsx_plan_info {
  *                synthesizes from the thread count, "Algorithm" step 2); a
  *                multiple of 32; <= 0: the planner's choice
  *  ctas_per_sm   at most this many resident CTAs per SM in the persistent
- *                grid; <= 0: as many as occupancy allows
+ *                grid; <= 0: the planner's (as many as occupancy allows,
+ *                but two, of 256 compute threads, for a two-stage ring of
+ *                sqrt or exp stages of 16 KB or more)
  *  store_lag     TMA variants: 0..3 of a store warp's tiles between a
  *                store's issue and the release of its stage; < 0: the
  *                planner's
  *  store_warps   TMA variants: 1 or 2 store warps, taking a CTA's tiles in
  *                turn, so that one can wait for its store to leave shared
- *                memory while the other stores the next tile (at most the
- *                stage count: one stage takes one store warp); <= 0: the
- *                planner's
+ *                memory while the other stores the next tile; clamped to
+ *                the stage count (a store warp's wait on a stage's phase is
+ *                exact only if the stage's previous phase is behind it);
+ *                <= 0: the planner's
  *  role_wait     TMA variants: how the producer and store warps wait on an
  *                mbarrier, 1 with every lane, 2 with lane 0 alone while the
  *                others take its answer; <= 0: the planner's

@@ -295,7 +295,13 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         }
     } else if (warp < role_warps) {
         // ------------------------------------------------ store warps
-        const int W = p.store_warps;
+        // A store warp's parity wait on a stage is exact only once the
+        // stage's previous phase has completed.  The computed barriers
+        // complete in tile order; copy waits on the full barriers, which the
+        // loads complete in any order, so there the stage's previous tile
+        // must be this warp's own: W must divide S (the planner ensures it;
+        // a second store warp that would break it stays idle).
+        const int W = OP == TSX_COPY && S % p.store_warps != 0 ? 1 : p.store_warps;
         const int sw = warp - 1;   // this warp takes the CTA's tiles sw, sw + W, ...
         const int n_boxes = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
         // lanes issuing stores: one per box, except that reduce-stores go out
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         TileCursor tc(p, cta + sw * G, W * G);
         StageCursor st = StageCursor::at(sw, S), released = st;   // tile i and tile i - lag W
         int64_t stored = 0;   // tiles this warp has stored
-        for (int64_t i = sw; i < N; i += W, ++stored) {
+        for (int64_t i = sw; sw < W && i < N; i += W, ++stored) {
             // copy has no compute step: the loaded tile goes straight back
             const uint32_t ready = OP == TSX_COPY ? full : computed;
             if (!role_wait(ready + 8u * st.s, st.phase, p, abort_flag, p.lane0_wait != 0))

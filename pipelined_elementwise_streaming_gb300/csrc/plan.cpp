@@ -130,9 +130,15 @@ StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes)
     // A store warp waits on a stage's barrier for the phase of its tile i
     // having seen only its own earlier tiles (i - W, i - 2 W, ...) complete.
     // A parity wait is exact only once the stage's previous phase (tile
-    // i - S) has completed, and tiles complete in order, so W <= S.
+    // i - S) has completed.  The compute warps complete tiles in order, so
+    // for every op with a compute step (the store waits on `computed`)
+    // W <= S is enough.  Copy's store waits on `full`, whose phases the TMA
+    // loads complete in any order across stages: there the stage's previous
+    // phase must be the same warp's own tile, i.e. W must divide S.
     if (r.store_warps > S)
         r.store_warps = S;
+    if (op == TSX_COPY && S % r.store_warps != 0)
+        r.store_warps = 1;
     return r;
 }
 

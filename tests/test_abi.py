@@ -281,3 +281,16 @@ def test_query_two_stage_large_tiles_take_256_threads(tsx):
     assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "copy")["threads"] == 64
     assert tsx.query("bf16", 16384, 16384, (64, 64), 2, "tma", "exp")["threads"] == 64
     assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "exp", tuning={"ctas_per_sm": 3})["threads"] == 64
+
+
+@pytest.mark.parametrize("op,stages,want", [
+    ("copy", 2, 2), ("copy", 3, 1), ("copy", 4, 2), ("copy", 5, 1), ("copy", 1, 1),
+    ("add", 3, 2), ("add", 5, 2), ("exp", 3, 2), ("add", 1, 1),
+])
+def test_query_two_store_warps_and_the_stage_count(tsx, op, stages, want):
+    """Two store warps need at most as many warps as stages; for copy, whose
+    store waits on the loads' barriers (completed in any order across
+    stages), they must also divide the stage count, so that a stage's
+    previous tile was the same warp's."""
+    q = tsx.query("bf16", 256, 4096, (32, 128), stages, "tma", op, tuning={"store_warps": 2, "store_lag": 0})
+    assert q["store_warps"] == want
