@@ -330,10 +330,20 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         if (smem > size_t(p->max_smem))
             return set_error(TSX_ERR_UNSUPPORTED, "the row reduction's stages do not fit in shared memory");
         L.og.smem_bytes = smem;
-        // about 768 compute threads per SM, shared by the CTAs that fit (the
-        // row sums do more arithmetic per byte than the elementwise stage)
-        const int ctas = int(kSmemPerSm / (smem + kSmemPerCtaReserved));
-        int threads = 768 / (ctas < 1 ? 1 : ctas) / 32 * 32;
+        // Compute threads per SM: a 16-bit element is half an fp32 one's
+        // bytes, so 16-bit row sums need about twice the threads per byte.
+        // 16-bit: about 768 per SM, shared by every CTA that fits.  fp32: at
+        // most three CTAs of 192 threads.  Measured on GB300: fp32 fma
+        // [128, 2^20] row sums at 4 stages (12 KB) 6236 GB/s with the four
+        // CTAs that fit, 6884 with three of 192 threads (6 stages: 6757);
+        // bf16 exp [16384, 16384] with 32x256 tiles at 2 stages 5942 with
+        // five CTAs of 128 threads, 5247 with three of 160.
+        const int fit0 = int(kSmemPerSm / (smem + kSmemPerCtaReserved));
+        const int fit = fit0 < 1 ? 1 : fit0;
+        const bool wide = p->g.es == 4;
+        const int ctas = wide && fit > 3 ? 3 : fit;
+        L.ctas_per_sm = ctas;   // the cap, before occupancy below
+        int threads = (wide ? 576 : 768) / ctas / 32 * 32;
         threads = threads < 64 ? 64 : threads > 512 ? 512 : threads;
         const int forced = p->g.knobs.threads;
         if (forced > 0) {
@@ -353,8 +363,9 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
             return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (blocks < 1)
             return set_error(TSX_ERR_UNSUPPORTED, "the row reduction cannot be resident with this shared memory");
-        if (p->g.knobs.ctas_per_sm > 0 && blocks > p->g.knobs.ctas_per_sm)
-            blocks = p->g.knobs.ctas_per_sm;
+        const int cap = p->g.knobs.ctas_per_sm > 0 ? p->g.knobs.ctas_per_sm : L.ctas_per_sm;
+        if (blocks > cap)
+            blocks = cap;
         L.ctas_per_sm = blocks;
         // contiguous tile ranges, one per CTA; a band is cut between at most
         // 1 + ceil((tiles_c - 1) / floor(T / G)) consecutive CTAs
