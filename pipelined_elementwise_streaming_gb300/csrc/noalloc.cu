@@ -162,6 +162,8 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
         return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (blocks < 1)
         return fail(TSX_ERR_UNSUPPORTED, "tsx_ewise_noalloc: the kernel cannot be resident with this shared memory");
+    if (og.ctas_cap > 0 && blocks > og.ctas_cap)
+        blocks = og.ctas_cap;   // the same launch as tsx_ewise
     const int64_t slots = int64_t(sm_count) * blocks;
     const int grid = int(g.tiles < slots ? g.tiles : slots);
 

@@ -46,6 +46,7 @@ def _noalloc(tsx, dtype, rows, cols, box, stages, variant, op, ins, out, status)
 @pytest.mark.parametrize("dtype,rows,cols,box,stages,variant,op", [
     ("f32", 203, 640, (8, 128), 4, "tma", "fma"),
     ("bf16", 300, 1024, (128, 128), 3, "tma", "exp"),
+    ("bf16", 300, 1024, (128, 128), 2, "tma", "exp"),     # two-stage ring: two store warps, capped CTAs
     ("f16", 77, 512, (16, 256), 2, "tma_rank3", "add"),
 ])
 def test_noalloc_matches_tsx_ewise_on_two_calls_in_a_row(tsx, dtype, rows, cols, box, stages, variant, op):
