@@ -160,6 +160,10 @@ typedef struct tsx_plan_info {
      * counts store_lag in its own tiles), and how the producer and store
      * warps wait on their mbarriers (1 every lane, 2 lane 0 alone) */
     int32_t store_warps, role_wait;
+    /* TSX_TMA_MIXED: how many of a CTA's tiles beyond the tile it loads the
+     * producer prefetches b into L2 (from the CTAs per SM: tsx_plan_query
+     * assumes the CTAs that shared memory alone fits) */
+    int32_t b_prefetch;
 } tsx_plan_info;
 
 /* Launch knobs of a plan.  Every field has a "planner's choice" value; start
@@ -185,6 +189,9 @@ typedef struct tsx_plan_info {
  *  role_wait     TMA variants: how the producer and store warps wait on an
  *                mbarrier, 1 with every lane, 2 with lane 0 alone while the
  *                others take its answer; <= 0: the planner's
+ *  b_prefetch    TSX_TMA_MIXED: the producer asks for b's boxes in L2 this
+ *                many of the CTA's tiles beyond the tile it loads (0..8);
+ *                < 0: the planner's
  *  l2_promotion  CUtensorMapL2promotion of the tensor maps, 0..3 (none, 64,
  *                128, 256 B); < 0: 128 B, the value of TVM docs
  *                "copy_async -> tma" ("Generated TIRx IR")
@@ -193,6 +200,7 @@ typedef struct tsx_plan_info {
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
     int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait;
+    int32_t b_prefetch;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

@@ -199,6 +199,8 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
         if (L.og.ctas_cap > 0 && blocks > L.og.ctas_cap)
             blocks = L.og.ctas_cap;
         L.ctas_per_sm = blocks;
+        if (mixed_launch(p->g.variant, op))
+            L.og.b_prefetch_ahead = mixed_prefetch_ahead(p->g, blocks);
         // persistent grid: every resident CTA slot once, no more CTAs than tiles
         const int64_t slots = int64_t(p->sm_count) * blocks;
         L.grid = int(p->g.tiles < slots ? p->g.tiles : slots);

@@ -98,11 +98,12 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
 // computes; any further units load on use.  The planner gives the mixed
 // variant enough threads that every unit is among the first kSetUnits.
 
-// The producer of the mixed variant asks the TMA unit to bring b's boxes of
-// each tile it loads into L2 (tensor map slot 2 holds b's map), S - 2 tiles
-// before the compute threads read them into registers, so those plain loads
-// mostly hit L2.  Measured on GB300, fp32 fma [128, 2^20]: 6547 -> 6765 GB/s
-// at 4 stages, 6010 -> 6354 at 6, unchanged at 3.
+// The producer of the mixed variant asks the TMA unit to bring b's boxes
+// into L2 (tensor map slot 2 holds b's map) for the CTA's tile
+// b_prefetch_ahead tiles beyond the one it loads, a few tiles before the
+// compute threads read them into registers, so those plain loads mostly hit
+// L2.  Measured on GB300, fp32 fma [128, 2^20] at 4 stages: 6547 GB/s
+// without it, 6765 prefetching the loaded tile, 6932 two tiles beyond.
 __device__ __forceinline__ void prefetch_b_tile(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc)
 {
     const int lane = static_cast<int>(threadIdx.x & 31);
@@ -258,6 +259,8 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         const int n_loads = NT * (p.rank3 ? p.row_chunks : p.row_chunks * p.atoms);
         const BoxRef mine = box_ref(maps, p, lane < n_loads ? lane : 0, 0);
         TileCursor tc(p, cta, G);
+        // mixed variant: the tile whose b the producer prefetches into L2
+        TileCursor pf(p, cta + static_cast<int64_t>(MIXED ? p.b_prefetch_ahead : 0) * G, G);
         StageCursor st;
         int64_t issued = 0;
         const int64_t pro = N < S - 1 ? N : S - 1;
@@ -266,8 +269,11 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
             if (lane == 0)
                 trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 0);
             issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
-            if constexpr (MIXED && NIN >= 2)
-                prefetch_b_tile(maps, p, tc);
+            if constexpr (MIXED && NIN >= 2) {
+                if (pf.tile(p) < p.tiles)
+                    prefetch_b_tile(maps, p, pf);
+                pf.next(p);
+            }
             tc.next(p);
             st.next(S);
         }
@@ -282,8 +288,11 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
                 trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 1);
             }
             issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
-            if constexpr (MIXED && NIN >= 2)
-                prefetch_b_tile(maps, p, tc);
+            if constexpr (MIXED && NIN >= 2) {
+                if (pf.tile(p) < p.tiles)
+                    prefetch_b_tile(maps, p, pf);
+                pf.next(p);
+            }
             tc.next(p);
             st.next(S);
         }

@@ -18,6 +18,7 @@ struct Knobs {
     int store_lag = -1;      // < 0: the planner's
     int store_warps = 0;     // 0: the planner's
     int role_wait = 0;       // 0: the planner's; 1: every lane waits; 2: lane 0 waits
+    int b_prefetch = -1;     // < 0: the planner's
     int l2_promotion = 2;    // CUtensorMapL2promotion
     int timeout_ms = 1000;
     bool checked = false;
@@ -57,6 +58,7 @@ struct OpGeometry {
     int store_lag = 1;       // a store warp's tiles between a store's issue and its stage's release
     bool lane0_wait = false; // the producer and store warps wait on lane 0 alone
     int ctas_cap = 0;        // at most this many CTAs per SM (0: occupancy)
+    int b_prefetch_ahead = 0;  // mixed variant: b's L2 prefetch, tiles beyond the producer's loads
 };
 
 struct TensorMapArgs {
@@ -79,6 +81,9 @@ StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes);
 // At most this many CTAs per SM for `op` (0: as occupancy allows), unless
 // the knobs say otherwise.
 int default_ctas_cap(const Geometry& g, int op, uint32_t stage_bytes);
+// Mixed variant: how many of a CTA's tiles beyond the tile it loads the
+// producer prefetches b into L2, for ctas_per_sm resident CTAs.
+int mixed_prefetch_ahead(const Geometry& g, int ctas_per_sm);
 // Validate a tsx_tuning (NULL: all defaults) into knobs.
 int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why);
 int make_geometry(int dtype, int64_t rows, int64_t cols, int64_t pitch, int box_rows, int box_cols, int stages,

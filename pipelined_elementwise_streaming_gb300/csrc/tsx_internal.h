@@ -75,8 +75,11 @@ struct TmaArgs {
     uint32_t stage_bytes;      // n_in slots
     uint32_t bytes_per_load;   // bytes one box delivers (out-of-bounds part zero-filled)
     uint32_t vec16_per_slot;   // 16-byte units of one slot
-    // mixed variant: operand b, read by the compute threads from global memory
+    // mixed variant: operand b, read by the compute threads from global memory,
+    // and how many of the CTA's tiles ahead of its loads the producer asks
+    // for b's boxes in L2
     const void* set_operand;
+    int b_prefetch_ahead;
     uint32_t box_bytes;        // rows_per_load * inner bytes: the data part of one load
     int swizzle_mask;          // 7, 3, 1 for the 128/64/32-byte swizzle, 0 for none
     // test hook (traced kernels only): per CTA a ring of trace_cap events of

@@ -294,3 +294,19 @@ def test_query_two_store_warps_and_the_stage_count(tsx, op, stages, want):
     previous tile was the same warp's."""
     q = tsx.query("bf16", 256, 4096, (32, 128), stages, "tma", op, tuning={"store_warps": 2, "store_lag": 0})
     assert q["store_warps"] == want
+
+
+def test_query_mixed_prefetch_lead(tsx):
+    """The mixed variant's L2 prefetch of b keeps about 40 KB of prefetched b
+    per SM: T = max(1, round(40 KB / (b tile bytes x CTAs))) tiles of lead,
+    of which the producer's own S - 2 come for free.  tsx_plan_query counts
+    the CTAs that shared memory alone fits; the knob overrides."""
+    for dtype, box, stages in (("f32", (8, 128), 2), ("f32", (8, 128), 4), ("bf16", (128, 128), 2),
+                               ("bf16", (128, 128), 3), ("bf16", (64, 128), 2)):
+        q = tsx.query(dtype, 1024, 1 << 16, box, stages, "tma_mixed", "mul")
+        ctas = 233472 // (q["smem_bytes"] + 1024)
+        per_sm = q["slot_bytes"] * ctas
+        lead = max(1, (2 * 40960 + per_sm) // (2 * per_sm))
+        assert q["b_prefetch"] == max(0, min(8, lead - (stages - 2))), (dtype, box, stages)
+    assert tsx.query("f32", 1024, 1 << 16, (8, 128), 4, "tma_mixed", "mul", tuning={"b_prefetch": 5})["b_prefetch"] == 5
+    assert tsx.query("f32", 1024, 1 << 16, (8, 128), 4, "tma", "mul")["b_prefetch"] == 0
