@@ -164,6 +164,9 @@ typedef struct tsx_plan_info {
      * producer prefetches b into L2 (from the CTAs per SM: tsx_plan_query
      * assumes the CTAs that shared memory alone fits) */
     int32_t b_prefetch;
+    /* TMA variants: L2 eviction priority of the TMA copies (bit 0 loads,
+     * bit 1 stores marked evict-first; 0 the normal priority) */
+    int32_t l2_hint;
 } tsx_plan_info;
 
 /* Launch knobs of a plan.  Every field has a "planner's choice" value; start
@@ -192,6 +195,10 @@ typedef struct tsx_plan_info {
  *  b_prefetch    TSX_TMA_MIXED: the producer asks for b's boxes in L2 this
  *                many of the CTA's tiles beyond the tile it loads (0..8);
  *                < 0: the planner's
+ *  l2_hint       TMA variants: 0..3, bit 0 marks the lines of the TMA loads
+ *                evict-first in L2, bit 1 those of the TMA stores (the
+ *                reduce-store of TSX_ACCUMULATE keeps the normal priority);
+ *                < 0: the planner's
  *  l2_promotion  CUtensorMapL2promotion of the tensor maps, 0..3 (none, 64,
  *                128, 256 B); < 0: 128 B, the value of TVM docs
  *                "copy_async -> tma" ("Generated TIRx IR")
@@ -200,7 +207,7 @@ typedef struct tsx_plan_info {
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
     int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait;
-    int32_t b_prefetch;
+    int32_t b_prefetch, l2_hint;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

@@ -59,7 +59,8 @@ using namespace dev;
 // `slot`: each of the first `lanes` lanes stores the boxes numbered lane,
 // lane + lanes, ... of the n_boxes of a full tile (`mine` is its first) and
 // commits them as one bulk group of its own; with ACC a reduce-store that
-// adds the tile into global memory.
+// adds the tile into global memory.  With bit 1 of l2_hint a plain store
+// marks its lines evict-first in L2.
 template <bool ACC>
 __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc,
                                            const BoxRef& mine, int n_boxes, int lanes, uint32_t slot)
@@ -76,12 +77,16 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
             const int z = static_cast<int>(tc.ct * p.atoms);
             if constexpr (ACC)
                 tma_reduce_add_3d(x.map, src, 0, y, z);
+            else if (p.l2_hint & 2)
+                tma_store_3d_hint(x.map, src, 0, y, z, l2_evict_first_policy());
             else
                 tma_store_3d(x.map, src, 0, y, z);
         } else {
             const int xc = (b.col0 >> p.promote_shift) + x.dx;
             if constexpr (ACC)
                 tma_reduce_add_2d(x.map, src, xc, y);
+            else if (p.l2_hint & 2)
+                tma_store_2d_hint(x.map, src, xc, y, l2_evict_first_policy());
             else
                 tma_store_2d(x.map, src, xc, y);
         }

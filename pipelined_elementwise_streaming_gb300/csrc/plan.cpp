@@ -188,6 +188,9 @@ int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
     if (t->b_prefetch > 8)
         return fail(why, "tuning.b_prefetch must be at most 8 (got %lld)", t->b_prefetch), TSX_ERR_INVALID;
     k->b_prefetch = t->b_prefetch;
+    if (t->l2_hint > 3)
+        return fail(why, "tuning.l2_hint must be 0..3 (got %lld)", t->l2_hint), TSX_ERR_INVALID;
+    k->l2_hint = t->l2_hint;
     if (t->l2_promotion > 3)
         return fail(why, "tuning.l2_promotion must be 0..3 (got %lld)", t->l2_promotion), TSX_ERR_INVALID;
     k->l2_promotion = t->l2_promotion < 0 ? 2 : t->l2_promotion;
@@ -360,6 +363,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         og->store_warps = ss.store_warps;
         og->store_lag = ss.store_lag;
         og->lane0_wait = ss.lane0_wait;
+        og->l2_hint = g.knobs.l2_hint >= 0 ? g.knobs.l2_hint : 0;
     }
     og->ctas_cap = default_ctas_cap(g, op, og->stage_bytes);
     // the mixed variant's L2 prefetch of b, for the CTAs that shared memory
@@ -417,6 +421,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->store_warps = is_tma_variant(g.variant) ? og.store_warps : 0;
     info->role_wait = is_tma_variant(g.variant) ? (og.lane0_wait ? 2 : 1) : 0;
     info->b_prefetch = og.b_prefetch_ahead;
+    info->l2_hint = og.l2_hint;
     info->timeout_ms = g.knobs.timeout_ms;
     info->vec = og.vec;
     info->outer = og.outer;
@@ -471,6 +476,7 @@ void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t
     args->store_warps = og.store_warps;
     args->lane0_wait = og.lane0_wait ? 1 : 0;
     args->b_prefetch_ahead = og.b_prefetch_ahead;
+    args->l2_hint = og.l2_hint;
     args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
     args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
@@ -518,6 +524,7 @@ extern "C" void tsx_tuning_defaults(tsx_tuning* t)
     t->store_warps = 0;
     t->role_wait = 0;
     t->b_prefetch = -1;
+    t->l2_hint = -1;
     t->l2_promotion = -1;
     t->timeout_ms = 0;
     t->checked = 0;

@@ -19,6 +19,7 @@ struct Knobs {
     int store_warps = 0;     // 0: the planner's
     int role_wait = 0;       // 0: the planner's; 1: every lane waits; 2: lane 0 waits
     int b_prefetch = -1;     // < 0: the planner's
+    int l2_hint = -1;        // < 0: the planner's; bit 0 loads, bit 1 stores evict-first
     int l2_promotion = 2;    // CUtensorMapL2promotion
     int timeout_ms = 1000;
     bool checked = false;
@@ -59,6 +60,7 @@ struct OpGeometry {
     bool lane0_wait = false; // the producer and store warps wait on lane 0 alone
     int ctas_cap = 0;        // at most this many CTAs per SM (0: occupancy)
     int b_prefetch_ahead = 0;  // mixed variant: b's L2 prefetch, tiles beyond the producer's loads
+    int l2_hint = 0;         // TMA copies marked evict-first in L2: bit 0 loads, bit 1 stores
 };
 
 struct TensorMapArgs {

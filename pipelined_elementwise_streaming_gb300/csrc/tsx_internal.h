@@ -61,6 +61,7 @@ struct TmaArgs {
     int store_lag;          // a store warp's tiles between a store's issue and its stage's release
     int store_warps;        // store warp w of W takes the CTA's tiles w, w + W, ...
     int lane0_wait;         // 1: the producer and store warps wait on lane 0 alone
+    int l2_hint;            // bit 0: TMA loads, bit 1: TMA stores mark their L2 lines evict-first
     int promote_shift;      // log2(tensor-map element / element): box x coordinates are in map elements
     int rows, cols;         // tensor extent (< 2^31)
     int box_rows, box_cols;

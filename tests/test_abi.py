@@ -310,3 +310,16 @@ def test_query_mixed_prefetch_lead(tsx):
         assert q["b_prefetch"] == max(0, min(8, lead - (stages - 2))), (dtype, box, stages)
     assert tsx.query("f32", 1024, 1 << 16, (8, 128), 4, "tma_mixed", "mul", tuning={"b_prefetch": 5})["b_prefetch"] == 5
     assert tsx.query("f32", 1024, 1 << 16, (8, 128), 4, "tma", "mul")["b_prefetch"] == 0
+
+
+def test_query_l2_hint(tsx):
+    """The L2 eviction hint of the TMA copies: 0..3 (bit 0 loads, bit 1
+    stores evict-first), the planner's default, and out-of-range values
+    declined with the reason."""
+    base = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma")
+    assert base["l2_hint"] in (0, 1, 2, 3)
+    for h in range(4):
+        assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"l2_hint": h})["l2_hint"] == h
+    with pytest.raises(tsx.TsxError, match="l2_hint"):
+        tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"l2_hint": 4})
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "fma", tuning={"l2_hint": 3})["l2_hint"] == 0
