@@ -167,6 +167,13 @@ typedef struct tsx_plan_info {
     /* TMA variants: L2 eviction priority of the TMA copies (bit 0 loads,
      * bit 1 stores marked evict-first; 0 the normal priority) */
     int32_t l2_hint;
+    /* TMA variants: the order CTAs take tiles in, 1 static (CTA c of G takes
+     * c, c + G, ...), 2 dynamic (TSX_COPY: each CTA's first tiles as in the
+     * static order, every later one claimed from a per-launch counter) */
+    int32_t tile_order;
+    /* dynamic order: the share of the tiles, in percent, claimed from the
+     * counter (the launch takes the CTAs' static tiles from it) */
+    int32_t dynamic_share;
 } tsx_plan_info;
 
 /* Launch knobs of a plan.  Every field has a "planner's choice" value; start
@@ -195,6 +202,18 @@ typedef struct tsx_plan_info {
  *  b_prefetch    TSX_TMA_MIXED: the producer asks for b's boxes in L2 this
  *                many of the CTA's tiles beyond the tile it loads (0..8);
  *                < 0: the planner's
+ *  tile_order    TMA variants, TSX_COPY: 1 static (CTA c of G takes tiles
+ *                c, c + G, ...), 2 dynamic (a CTA's first tiles as in the
+ *                static order, then tiles claimed in order from a counter,
+ *                so that CTAs streaming faster take more tiles); <= 0: the
+ *                planner's: dynamic for launches of at least 16 tiles per
+ *                CTA (the host-only query, which knows no grid, reports
+ *                that case).  The other ops, and TSX_ACCUMULATE, always
+ *                take the static order
+ *  dynamic_share dynamic order: about this percentage of the tiles (the
+ *                last ones) is claimed from the counter, 1..100 (a CTA
+ *                takes at least max(1, S - 1) tiles in the static order
+ *                first); <= 0: the planner's (100)
  *  l2_hint       TMA variants: 0..3, bit 0 marks the lines of the TMA loads
  *                evict-first in L2, bit 1 those of the TMA stores (the
  *                reduce-store of TSX_ACCUMULATE keeps the normal priority);
@@ -207,7 +226,7 @@ typedef struct tsx_plan_info {
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
     int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait;
-    int32_t b_prefetch, l2_hint;
+    int32_t b_prefetch, l2_hint, tile_order, dynamic_share;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

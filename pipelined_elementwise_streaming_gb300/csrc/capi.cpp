@@ -104,6 +104,13 @@ struct tsx_plan {
     int sm_count = 0;
     int max_smem = 0;
     int* d_status = nullptr;
+    // counters of the dynamic tile order, one slot (two words) per stream the
+    // plan has launched on, keyed by the stream's unique id: launches on one
+    // stream run in order, and each launch's last CTA zeroes its slot
+    unsigned long long* d_tile_counters = nullptr;
+    std::mutex slot_mutex;
+    unsigned long long slot_stream[kTileCounterSlots] = {};
+    int slots_used = 0;
     // test hooks (include/tsx_debug.h): the tile whose loads the producer
     // skips, and the traced kernels' schedule record, [trace_grid][trace_cap]
     // events of 16 bytes
@@ -184,6 +191,10 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
         const int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
         if (rc != TSX_OK)
             return set_error(rc, why);
+        if (accumulate) {
+            L.og.tile_order = 1;   // the reduce-store kernels take the static order
+            L.og.dynamic_share = 0;
+        }
         const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate, p->trace_cap > 0);
         if (!fn)
             return set_error(TSX_ERR_UNSUPPORTED, "traced launches: only fp32 copy and add have a traced kernel");
@@ -204,6 +215,12 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
         // persistent grid: every resident CTA slot once, no more CTAs than tiles
         const int64_t slots = int64_t(p->sm_count) * blocks;
         L.grid = int(p->g.tiles < slots ? p->g.tiles : slots);
+        // the planner's dynamic order pays only with enough tiles per CTA
+        if (L.og.tile_order == 2 && p->g.knobs.tile_order <= 0 &&
+            p->g.tiles < int64_t(kDynamicMinTilesPerCta) * L.grid) {
+            L.og.tile_order = 1;
+            L.og.dynamic_share = 0;
+        }
         L.ready = true;
     }
     *out = &L;
@@ -279,6 +296,36 @@ void fill_tma_args(const tsx_plan* p, const OpGeometry& og, TmaArgs* args)
     tsx::fill_tma_args(p->g, og, p->d_status, p->fault_tile, args);
 }
 
+// The dynamic tile order's counter slot for launches on `st`, or NULL
+// (static order) while the stream is being captured into a graph (a graph
+// may be replayed on any stream), when the stream's id cannot be read, or
+// once the plan has served kTileCounterSlots streams.
+unsigned long long* tile_counter_for(tsx_plan* p, cudaStream_t st)
+{
+    if (!p->d_tile_counters)
+        return nullptr;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &capture) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (capture != cudaStreamCaptureStatusNone)
+        return nullptr;
+    unsigned long long id = 0;
+    if (cudaStreamGetId(st, &id) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(p->slot_mutex);
+    for (int i = 0; i < p->slots_used; ++i)
+        if (p->slot_stream[i] == id)
+            return p->d_tile_counters + 2 * i;
+    if (p->slots_used == kTileCounterSlots)
+        return nullptr;
+    p->slot_stream[p->slots_used] = id;
+    return p->d_tile_counters + 2 * p->slots_used++;
+}
+
 int alignment_of(const void* ptr)
 {
     const uintptr_t v = reinterpret_cast<uintptr_t>(ptr);
@@ -325,6 +372,7 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         int rc = make_op_geometry(p->g, op, p->max_smem, &L.og, &why);
         if (rc != TSX_OK)
             return set_error(rc, why);
+        L.og.tile_order = 0;   // contiguous tile ranges per CTA, no counter
         // one fp32 partial per 16-byte unit of a staged slot
         const size_t partials = size_t(L.og.vec16_per_slot) * 4;
         const size_t smem = size_t(p->g.stages) * L.og.stage_bytes + size_t(p->g.stages) * 16 + 16 + 16 +
@@ -442,10 +490,18 @@ tsx_plan_t tsx_plan_create_tuned(tsx_dtype dtype, int64_t rows, int64_t cols, in
         if (e == cudaSuccess)
             e = cudaMemset(p->d_status, 0, sizeof(int));
     }
+    if (e == cudaSuccess && is_tma_variant(g.variant)) {
+        const size_t bytes = size_t(kTileCounterSlots) * 2 * sizeof(unsigned long long);
+        e = cudaMalloc(&p->d_tile_counters, bytes);
+        if (e == cudaSuccess)
+            e = cudaMemset(p->d_tile_counters, 0, bytes);
+    }
     if (e != cudaSuccess) {
         cuda_error(e, "tsx_plan_create");
         if (p->d_status)
             cudaFree(p->d_status);
+        if (p->d_tile_counters)
+            cudaFree(p->d_tile_counters);
         delete p;
         return nullptr;
     }
@@ -459,6 +515,7 @@ void tsx_plan_destroy(tsx_plan_t p)
         return;
     if (p->d_status)
         cudaFree(p->d_status);
+    cudaFree(p->d_tile_counters);
     cudaFree(p->trace_buf);
     for (auto& L : p->rowsum_ops) {
         cudaFree(L.scratch.piece);
@@ -642,6 +699,10 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
         TmaArgs args{};
         fill_tma_args(p, L->og, &args);
         args.set_operand = mixed ? b : nullptr;
+        if (L->og.tile_order == 2 && !mixed) {
+            args.tile_counter = tile_counter_for(p, st);
+            args.static_tiles = static_tiles_per_cta(g, L->og, L->grid);
+        }
         if (p->trace_cap > 0) {
             rc = prepare_trace(p, L->grid, st);
             if (rc != TSX_OK)

@@ -230,8 +230,10 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     const uint32_t full = base + static_cast<uint32_t>(S) * p.stage_bytes;   // S barriers each
     const uint32_t computed = full + 8u * S;
     const uint32_t empty = computed + 8u * S;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 8u * S - base));
-    uint32_t* trace_counter = reinterpret_cast<uint32_t*>(smem + (empty + 8u * S - base) + 4);
+    // dynamic tile order: the tile each stage holds (-1: no more tiles)
+    volatile int64_t* tile_of = reinterpret_cast<volatile int64_t*>(smem + (empty + 8u * S - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 16u * S - base));
+    uint32_t* trace_counter = reinterpret_cast<uint32_t*>(smem + (empty + 16u * S - base) + 4);
 
     const int warp = threadIdx.x / 32;
     const int role_warps = tma_role_warps(p.store_warps);
@@ -240,6 +242,22 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     const int64_t cta = blockIdx.x;
     const int64_t N = cta < p.tiles ? (p.tiles - 1 - cta) / G + 1 : 0;
     const bool elected = warp < 2 && elect_one();   // one lane of warp 0 and of warp 1
+    // Dynamic tile order (copy only): the CTA's first P tiles are c, c + G,
+    // ..., c + (P - 1) G as in the static order (P >= 1, set by the host);
+    // every later tile is claimed from the launch's counter (tiles P G,
+    // P G + 1, ... in claim order), so CTAs that stream faster take more of
+    // the last tiles and all finish together.  The producer hands each
+    // claimed tile's index to the store warps through shared memory and
+    // ends the CTA's stream with one "no more tiles" stage per store warp.
+    // In a static-order launch the CTAs of a copy finished up to 40 % apart
+    // (GB300); ops with a compute step measured slower with the dynamic
+    // order, and slower still with its code merely compiled in, so their
+    // instantiations are built without it.
+    constexpr bool kDynamic = OP == TSX_COPY && !MIXED && !ACC;
+    const bool dyn = kDynamic && p.tile_counter != nullptr;
+    const int64_t P = p.static_tiles > 0 ? p.static_tiles : 1;
+    // store warps that take tiles (copy: only if they divide S, see below)
+    const int W = OP == TSX_COPY && S % p.store_warps != 0 ? 1 : p.store_warps;
 
     // Pre-prologue: the barriers of every stage; descriptor prefetch.
     if (warp == 0 && elected) {
@@ -268,38 +286,87 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         TileCursor pf(p, cta + static_cast<int64_t>(MIXED ? p.b_prefetch_ahead : 0) * G, G);
         StageCursor st;
         int64_t issued = 0;
-        const int64_t pro = N < S - 1 ? N : S - 1;
-        // Prologue: the first S - 1 tiles, into stages that start empty.
-        for (; issued < pro; ++issued) {
-            if (lane == 0)
-                trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 0);
-            issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
-            if constexpr (MIXED && NIN >= 2) {
-                if (pf.tile(p) < p.tiles)
-                    prefetch_b_tile(maps, p, pf);
-                pf.next(p);
+        if (!dyn) {
+            const int64_t pro = N < S - 1 ? N : S - 1;
+            // Prologue: the first S - 1 tiles, into stages that start empty.
+            for (; issued < pro; ++issued) {
+                if (lane == 0)
+                    trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 0);
+                issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+                if constexpr (MIXED && NIN >= 2) {
+                    if (pf.tile(p) < p.tiles)
+                        prefetch_b_tile(maps, p, pf);
+                    pf.next(p);
+                }
+                tc.next(p);
+                st.next(S);
             }
-            tc.next(p);
-            st.next(S);
-        }
-        // Main loop: tile k = i + S - 1 into stage k mod S, once the store
-        // warp has released that stage's previous tile (k - S).
-        for (; issued < N; ++issued) {
-            if (issued >= S && !role_wait(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag, p.lane0_wait != 0))
-                break;
-            if (lane == 0) {
-                if (issued >= S)
-                    trace_event<TRACE>(p, trace_counter, kTraceReuse, issued, st.s, st.phase ^ 1u);
-                trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 1);
+            // Main loop: tile k = i + S - 1 into stage k mod S, once the
+            // store warp has released that stage's previous tile (k - S).
+            for (; issued < N; ++issued) {
+                if (issued >= S && !role_wait(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag, p.lane0_wait != 0))
+                    break;
+                if (lane == 0) {
+                    if (issued >= S)
+                        trace_event<TRACE>(p, trace_counter, kTraceReuse, issued, st.s, st.phase ^ 1u);
+                    trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, 1);
+                }
+                issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
+                if constexpr (MIXED && NIN >= 2) {
+                    if (pf.tile(p) < p.tiles)
+                        prefetch_b_tile(maps, p, pf);
+                    pf.next(p);
+                }
+                tc.next(p);
+                st.next(S);
             }
-            issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes, full + 8u * st.s);
-            if constexpr (MIXED && NIN >= 2) {
-                if (pf.tile(p) < p.tiles)
-                    prefetch_b_tile(maps, p, pf);
-                pf.next(p);
+        } else {
+            // The same prologue and main loop over the CTA's k-th tile, k =
+            // 0, 1, ... until the tiles run out.  The first P tiles follow
+            // the static cursor; every role knows them without being told.
+            // Lane 0 claims the tile of k + 1 as soon as it knows the tile
+            // of k, so the atomic's round trip overlaps the wait for a free
+            // stage, and publishes each claimed tile in the stage's slot.
+            const int64_t static_end = P * G;
+            int64_t claim = p.tiles;   // lane 0: the claimed tile of the next k (>= tiles: none)
+            int ended = 0;             // "no more tiles" stages issued
+            for (;; ++issued) {
+                const bool claimed = issued >= P;
+                const int64_t t = claimed ? __shfl_sync(0xffffffffu, static_cast<long long>(claim), 0)
+                                          : cta + issued * G;
+                if (lane == 0 && issued + 1 >= P && t < p.tiles)
+                    claim = static_end + static_cast<int64_t>(atomicAdd(p.tile_counter, 1ull));
+                if (issued >= S && !role_wait(empty + 8u * st.s, st.phase ^ 1u, p, abort_flag, p.lane0_wait != 0))
+                    break;
+                if (t < p.tiles) {
+                    if (lane == 0) {
+                        if (issued >= S)
+                            trace_event<TRACE>(p, trace_counter, kTraceReuse, issued, st.s, st.phase ^ 1u);
+                        trace_event<TRACE>(p, trace_counter, kTraceTile, issued, static_cast<uint32_t>(t) & 0xffffu,
+                                           static_cast<uint32_t>(t) >> 16);
+                        trace_event<TRACE>(p, trace_counter, kTraceLoad, issued, st.s, issued < S - 1 ? 0 : 1);
+                        if (claimed)
+                            tile_of[st.s] = t;   // published by the arrival on `full`
+                    }
+                    if (claimed)
+                        tc.seek(p, t);
+                    issue_tile_lanes<NT>(maps, p, tc, mine, n_loads, base + st.s * p.stage_bytes,
+                                         full + 8u * st.s);
+                    if (!claimed)
+                        tc.next(p);
+                } else {
+                    if (lane == 0) {
+                        tile_of[st.s] = -1;
+                        mbar_arrive(full + 8u * st.s);
+                    }
+                    __syncwarp();
+                    if (++ended == W) {
+                        ++issued;
+                        break;
+                    }
+                }
+                st.next(S);
             }
-            tc.next(p);
-            st.next(S);
         }
         if (*abort_flag && lane == 0) {
             // let the loads still in flight land before shared memory goes away
@@ -315,7 +382,6 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         // loads complete in any order, so there the stage's previous tile
         // must be this warp's own: W must divide S (the planner ensures it;
         // a second store warp that would break it stays idle).
-        const int W = OP == TSX_COPY && S % p.store_warps != 0 ? 1 : p.store_warps;
         const int sw = warp - 1;   // this warp takes the CTA's tiles sw, sw + W, ...
         const int n_boxes = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
         // lanes issuing stores: one per box, except that reduce-stores go out
@@ -330,11 +396,28 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         TileCursor tc(p, cta + sw * G, W * G);
         StageCursor st = StageCursor::at(sw, S), released = st;   // tile i and tile i - lag W
         int64_t stored = 0;   // tiles this warp has stored
-        for (int64_t i = sw; sw < W && i < N; i += W, ++stored) {
+        int64_t i = sw;
+        for (; sw < W && (dyn || i < N); i += W, ++stored) {
             // copy has no compute step: the loaded tile goes straight back
             const uint32_t ready = OP == TSX_COPY ? full : computed;
             if (!role_wait(ready + 8u * st.s, st.phase, p, abort_flag, p.lane0_wait != 0))
                 break;
+            if (dyn) {
+                if (i < P) {
+                    // a static tile: past the last band means no more tiles
+                    if (tc.band >= p.tiles_r)
+                        break;
+                } else {
+                    // a claimed tile: lane 0 has seen the barrier complete
+                    int64_t t = 0;
+                    if (lane == 0)
+                        t = tile_of[st.s];
+                    t = __shfl_sync(0xffffffffu, static_cast<long long>(t), 0);
+                    if (t < 0)
+                        break;
+                    tc.seek(p, t);
+                }
+            }
             if (lane == 0)
                 trace_event<TRACE>(p, trace_counter, kTraceStore, i, st.s, st.phase);
             // release tile i - lag W once every lane's stores of it have read
@@ -351,8 +434,22 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
                 }
                 released.advance(W, S);
             }
-            tc.next(p);
+            tc.next(p);   // the static order (a claimed tile seeks its own)
             st.advance(W, S);
+        }
+        if (dyn && !*abort_flag && sw < W) {
+            // No more tiles: hand back the stages still held for the lag, so
+            // that the producer can end the other store warp's stream too.
+            if (lane < lanes)
+                bulk_wait_read(0);
+            __syncwarp();
+            for (int64_t r = stored > lag ? stored - lag : 0; r < stored; ++r) {
+                if (lane == 0) {
+                    trace_event<TRACE>(p, trace_counter, kTraceRelease, sw + r * W, released.s, 0);
+                    mbar_arrive(empty + 8u * released.s);
+                }
+                released.advance(W, S);
+            }
         }
         if (lane < lanes)
             bulk_wait_all();
@@ -420,6 +517,15 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
             mbar_inval(full + 8u * s);
             mbar_inval(computed + 8u * s);
             mbar_inval(empty + 8u * s);
+        }
+    }
+    if (dyn && threadIdx.x == 0) {
+        // the launch's last CTA to finish zeroes the counter for the next
+        // launch on the stream (every CTA has made its last claim by now)
+        __threadfence();
+        if (atomicAdd(p.tile_counter + 1, 1ull) == static_cast<unsigned long long>(G) - 1) {
+            atomicExch(p.tile_counter, 0ull);
+            atomicExch(p.tile_counter + 1, 0ull);
         }
     }
 }

@@ -191,6 +191,14 @@ int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
     if (t->l2_hint > 3)
         return fail(why, "tuning.l2_hint must be 0..3 (got %lld)", t->l2_hint), TSX_ERR_INVALID;
     k->l2_hint = t->l2_hint;
+    if (t->tile_order > 2)
+        return fail(why, "tuning.tile_order must be 1 (static) or 2 (dynamic) (got %lld)", t->tile_order),
+               TSX_ERR_INVALID;
+    k->tile_order = t->tile_order > 0 ? t->tile_order : 0;
+    if (t->dynamic_share > 100)
+        return fail(why, "tuning.dynamic_share must be 1..100 percent (got %lld)", t->dynamic_share),
+               TSX_ERR_INVALID;
+    k->dynamic_share = t->dynamic_share > 0 ? t->dynamic_share : 0;
     if (t->l2_promotion > 3)
         return fail(why, "tuning.l2_promotion must be 0..3 (got %lld)", t->l2_promotion), TSX_ERR_INVALID;
     k->l2_promotion = t->l2_promotion < 0 ? 2 : t->l2_promotion;
@@ -364,6 +372,10 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         og->store_lag = ss.store_lag;
         og->lane0_wait = ss.lane0_wait;
         og->l2_hint = g.knobs.l2_hint >= 0 ? g.knobs.l2_hint : 0;
+        // the dynamic order is built into the copy kernels only (ops with a
+        // compute step measured slower with it on GB300)
+        og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : 2) : 1;
+        og->dynamic_share = og->tile_order == 2 ? (g.knobs.dynamic_share > 0 ? g.knobs.dynamic_share : 100) : 0;
     }
     og->ctas_cap = default_ctas_cap(g, op, og->stage_bytes);
     // the mixed variant's L2 prefetch of b, for the CTAs that shared memory
@@ -422,6 +434,8 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->role_wait = is_tma_variant(g.variant) ? (og.lane0_wait ? 2 : 1) : 0;
     info->b_prefetch = og.b_prefetch_ahead;
     info->l2_hint = og.l2_hint;
+    info->tile_order = og.tile_order;
+    info->dynamic_share = og.dynamic_share;
     info->timeout_ms = g.knobs.timeout_ms;
     info->vec = og.vec;
     info->outer = og.outer;
@@ -482,6 +496,16 @@ void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
 }
 
+int64_t static_tiles_per_cta(const Geometry& g, const OpGeometry& og, int64_t grid)
+{
+    const int64_t least = g.stages > 1 ? g.stages - 1 : 1;
+    if (grid < 1)
+        return least;
+    const int64_t share = og.dynamic_share > 0 ? og.dynamic_share : 100;
+    const int64_t most = (g.tiles / grid) * (100 - share) / 100;
+    return most > least ? most : least;
+}
+
 void tensor_map_args(const Geometry& g, TensorMapArgs* m)
 {
     *m = TensorMapArgs{};
@@ -525,6 +549,8 @@ extern "C" void tsx_tuning_defaults(tsx_tuning* t)
     t->role_wait = 0;
     t->b_prefetch = -1;
     t->l2_hint = -1;
+    t->tile_order = 0;
+    t->dynamic_share = 0;
     t->l2_promotion = -1;
     t->timeout_ms = 0;
     t->checked = 0;

@@ -20,6 +20,8 @@ struct Knobs {
     int role_wait = 0;       // 0: the planner's; 1: every lane waits; 2: lane 0 waits
     int b_prefetch = -1;     // < 0: the planner's
     int l2_hint = -1;        // < 0: the planner's; bit 0 loads, bit 1 stores evict-first
+    int tile_order = 0;      // 0: the planner's; 1 static; 2 dynamic
+    int dynamic_share = 0;   // 0: the planner's; else percent of the tiles claimed dynamically
     int l2_promotion = 2;    // CUtensorMapL2promotion
     int timeout_ms = 1000;
     bool checked = false;
@@ -61,7 +63,14 @@ struct OpGeometry {
     int ctas_cap = 0;        // at most this many CTAs per SM (0: occupancy)
     int b_prefetch_ahead = 0;  // mixed variant: b's L2 prefetch, tiles beyond the producer's loads
     int l2_hint = 0;         // TMA copies marked evict-first in L2: bit 0 loads, bit 1 stores
+    int tile_order = 0;      // TMA: 1 static, 2 dynamic (tiles claimed from a counter)
+    int dynamic_share = 0;   // dynamic order: percent of the tiles claimed
 };
+
+// Dynamic order: the tiles each of `grid` CTAs takes in the static order
+// before it claims, so that about dynamic_share percent of the tiles are
+// claimed (at least max(1, S - 1)).
+int64_t static_tiles_per_cta(const Geometry& g, const OpGeometry& og, int64_t grid);
 
 struct TensorMapArgs {
     int rank = 0;

@@ -31,7 +31,16 @@ constexpr int kSmemPerCtaReserved = 1024;  // the system's share of each residen
 constexpr int kMaxStoreWarps = 2;      // TMA: store warps beside the producer warp
 // TMA CTAs: the producer warp and the store warps come ahead of the compute warps
 TSX_HD constexpr int tma_role_warps(int store_warps) { return 1 + store_warps; }
-constexpr int kTmaBarrierBytes = 24;   // full, computed and empty mbarriers of one stage
+// per stage: the full, computed and empty mbarriers and the index of the
+// tile the stage holds (the dynamic tile order hands it to the consumers)
+constexpr int kTmaBarrierBytes = 32;
+// Tile counters of the dynamic tile order: a plan keeps this many, one per
+// stream it launches on (two 64-bit words each: tiles claimed, CTAs done).
+constexpr int kTileCounterSlots = 64;
+// The planner takes the dynamic order only for launches with at least this
+// many tiles per CTA (GB300: copies of 2 to 4 tiles per CTA were 12-14 %
+// slower in it, of 36 or more 10-11 % faster).
+constexpr int kDynamicMinTilesPerCta = 16;
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
 TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }
@@ -83,6 +92,11 @@ struct TmaArgs {
     int b_prefetch_ahead;
     uint32_t box_bytes;        // rows_per_load * inner bytes: the data part of one load
     int swizzle_mask;          // 7, 3, 1 for the 128/64/32-byte swizzle, 0 for none
+    // dynamic tile order (nullptr: static, CTA c takes c, c + G, ...): {tiles
+    // claimed beyond the static ones, CTAs finished}, zero at launch; the
+    // launch's last CTA zeroes them again
+    unsigned long long* tile_counter;
+    int64_t static_tiles;   // dynamic order: tiles c, c + G, ... a CTA takes before it claims (>= 1)
     // test hook (traced kernels only): per CTA a ring of trace_cap events of
     // four 32-bit words each
     uint32_t* trace;
@@ -98,6 +112,7 @@ enum TraceKind {
     kTraceBody = 4,      // compute: tile k computed (thread 0's share)
     kTraceStore = 5,     // store: tile k's stores about to be issued from stage a
     kTraceRelease = 6,   // store: tile k's stage a handed back to the producer
+    kTraceTile = 7,      // producer: the CTA's k-th tile is tile a | b << 16 of the tensor
 };
 
 // Kernel arguments of the cp.async and synchronous ablation kernels.

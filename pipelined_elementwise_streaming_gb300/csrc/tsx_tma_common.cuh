@@ -65,6 +65,18 @@ struct TileCursor {
         }
     }
     __device__ __forceinline__ int64_t tile(const TmaArgs& p) const { return band * p.tiles_c + ct; }
+    // Move to tile t (the step stays).
+    __device__ __forceinline__ void seek(const TmaArgs& p, int64_t t)
+    {
+        if (p.tiles <= 0x7fffffff) {
+            const uint32_t q = static_cast<uint32_t>(t) / static_cast<uint32_t>(p.tiles_c);
+            band = q;
+            ct = t - static_cast<int64_t>(q) * p.tiles_c;
+        } else {
+            band = t / p.tiles_c;
+            ct = t - band * p.tiles_c;
+        }
+    }
 };
 
 // Stage s = k mod S and parity (k / S) mod 2 of a tile counter k.

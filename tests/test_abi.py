@@ -323,3 +323,26 @@ def test_query_l2_hint(tsx):
     with pytest.raises(tsx.TsxError, match="l2_hint"):
         tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"l2_hint": 4})
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "fma", tuning={"l2_hint": 3})["l2_hint"] == 0
+
+
+def test_query_tile_order(tsx):
+    """TMA copies take tiles in the dynamic order unless told otherwise
+    (the last `dynamic_share` percent claimed from a counter); every other
+    op, and the reduce-store, keep the static order; the ablations and row
+    sums have no tile order."""
+    q = tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "copy")
+    assert (q["tile_order"], q["dynamic_share"]) == (2, 100)
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma_rank3", "copy")["tile_order"] == 2
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma_mixed", "copy")["tile_order"] == 2
+    q = tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "copy", tuning={"dynamic_share": 25})
+    assert (q["tile_order"], q["dynamic_share"]) == (2, 25)
+    q = tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "copy", tuning={"tile_order": 1})
+    assert (q["tile_order"], q["dynamic_share"]) == (1, 0)
+    for op in ("sqrt", "exp", "add", "mul", "fma"):
+        q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", op, tuning={"tile_order": 2})
+        assert (q["tile_order"], q["dynamic_share"]) == (1, 0), op
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "copy")["tile_order"] == 0
+    with pytest.raises(tsx.TsxError, match="tile_order"):
+        tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"tile_order": 3})
+    with pytest.raises(tsx.TsxError, match="dynamic_share"):
+        tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"dynamic_share": 101})

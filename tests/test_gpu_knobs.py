@@ -5,14 +5,12 @@ through the traced kernel."""
 
 import zlib
 
-import numpy as np
 import pytest
 
 import oracle
-from oracle import structure as st
 from tests import _gpu
 from tests._gpu import bits_of, compare, random_bits, to_dev, torch
-from tests.test_gpu_schedule_trace import _check_cta
+from tests.test_gpu_schedule_trace import _check_all
 
 pytestmark = pytest.mark.gpu
 
@@ -76,7 +74,8 @@ def test_knobs_leave_results_unchanged(tsx, knob, values, case):
 def test_store_lag_follows_the_schedule_model(tsx, lag, stages):
     """With a forced store lag one store warp releases tile i - lag (lag
     capped at S - 1) after tile i's stores; the trace must still satisfy the
-    model (two store warps: test_gpu_schedule_trace.py)."""
+    model (two store warps and the copy's dynamic order:
+    test_gpu_schedule_trace.py)."""
     tiles = 1000
     rows, cols = 8 * tiles, 32
     a, b = random_bits("f32", (rows, cols), lag), random_bits("f32", (rows, cols), lag + 1)
@@ -88,7 +87,4 @@ def test_store_lag_follows_the_schedule_model(tsx, lag, stages):
         assert plan.status() == tsx.TSX_OK
         trace = plan.trace()
     compare("add", "f32", bits_of(out, "f32"), oracle.ewise("add", "f32", a, b), "traced add")
-    eff = min(lag, stages - 1)
-    G = trace.shape[0]
-    for c in range(G):
-        _check_cta(trace[c], len(st.cta_tiles(tiles, G, c)), stages, eff, "add")
+    _check_all(trace, tiles, stages, min(lag, stages - 1), "add", 1, 1, 0)
