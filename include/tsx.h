@@ -174,6 +174,10 @@ typedef struct tsx_plan_info {
     /* dynamic order: the share of the tiles, in percent, claimed from the
      * counter (the launch takes the CTAs' static tiles from it) */
     int32_t dynamic_share;
+    /* TMA variants: groups of a tile's boxes that the compute warps hand to
+     * the store warps one by one (2: the first half is stored while the
+     * second is computed) */
+    int32_t compute_groups;
 } tsx_plan_info;
 
 /* Launch knobs of a plan.  Every field has a "planner's choice" value; start
@@ -214,6 +218,12 @@ typedef struct tsx_plan_info {
  *                last ones) is claimed from the counter, 1..100 (a CTA
  *                takes at least max(1, S - 1) tiles in the static order
  *                first); <= 0: the planner's (100)
+ *  store_split   TMA variants, ops with a compute step and an even number
+ *                of boxes per tile (not the mixed variant's binary ops): 2
+ *                stores the first half of a tile's boxes while the compute
+ *                warps work on the second, 1 stores the tile at once; <= 0:
+ *                the planner's (2 for sqrt and exp with tiles of 16 KB or
+ *                more)
  *  l2_hint       TMA variants: 0..3, bit 0 marks the lines of the TMA loads
  *                evict-first in L2, bit 1 those of the TMA stores (the
  *                reduce-store of TSX_ACCUMULATE keeps the normal priority);
@@ -226,7 +236,7 @@ typedef struct tsx_plan_info {
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
     int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait;
-    int32_t b_prefetch, l2_hint, tile_order, dynamic_share;
+    int32_t b_prefetch, l2_hint, tile_order, dynamic_share, store_split;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

@@ -94,6 +94,38 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
     bulk_commit();
 }
 
+// The store warp's TMA stores of boxes [lo, hi) of one tile (box numbering
+// as in store_tile), lanes lo + lane, lo + lane + lanes, ..., committed as
+// one bulk group per lane.
+template <bool ACC>
+__device__ __forceinline__ void store_boxes(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc, int lo,
+                                            int hi, int lanes, uint32_t slot)
+{
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const TileBoxes b = boxes_at(p, tc.band, tc.ct);
+    for (int L = lo + lane; L < hi; L += lanes) {
+        const BoxRef x = box_ref(maps, p, L, 3);
+        if (!box_in(x, b))
+            continue;
+        const uint32_t src = slot + x.off;
+        const int y = b.row0 + x.dy;
+        if (p.rank3) {
+            const int z = static_cast<int>(tc.ct * p.atoms);
+            if constexpr (ACC)
+                tma_reduce_add_3d(x.map, src, 0, y, z);
+            else
+                tma_store_3d(x.map, src, 0, y, z);
+        } else {
+            const int xc = (b.col0 >> p.promote_shift) + x.dx;
+            if constexpr (ACC)
+                tma_reduce_add_2d(x.map, src, xc, y);
+            else
+                tma_store_2d(x.map, src, xc, y);
+        }
+    }
+    bulk_commit();
+}
+
 // Operand b of the mixed variant is not staged by TMA.  The compute threads
 // load it from global memory with plain 16-byte loads at the elements their
 // staged vectors hold: the "Set" circular buffering of the nvFuser page's
@@ -227,9 +259,12 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
     uint8_t* const smem = smem_raw + (base - raw);
     const int S = p.stages;
-    const uint32_t full = base + static_cast<uint32_t>(S) * p.stage_bytes;   // S barriers each
+    const uint32_t full = base + static_cast<uint32_t>(S) * p.stage_bytes;   // S barriers
+    // two per stage (computed + 16 s + 8 g): group g of the stage's boxes computed
     const uint32_t computed = full + 8u * S;
-    const uint32_t empty = computed + 8u * S;
+    const uint32_t empty = computed + 16u * S;
+    // groups of boxes the compute warps hand to the store warps one by one (1 or 2)
+    const int CG = MIXED ? 1 : p.compute_groups;
     // dynamic tile order: the tile each stage holds (-1: no more tiles)
     volatile int64_t* tile_of = reinterpret_cast<volatile int64_t*>(smem + (empty + 8u * S - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 16u * S - base));
@@ -265,7 +300,8 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
             prefetch_tensormap(&maps.m[j]);
         for (int s = 0; s < S; ++s) {
             mbar_init(full + 8u * s, 1);
-            mbar_init(computed + 8u * s, static_cast<uint32_t>(compute_warps));
+            for (int g = 0; g < CG; ++g)
+                mbar_init(computed + 16u * s + 8u * g, static_cast<uint32_t>(compute_warps));
             mbar_init(empty + 8u * s, 1);
         }
         *abort_flag = 0;
@@ -399,8 +435,8 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         int64_t i = sw;
         for (; sw < W && (dyn || i < N); i += W, ++stored) {
             // copy has no compute step: the loaded tile goes straight back
-            const uint32_t ready = OP == TSX_COPY ? full : computed;
-            if (!role_wait(ready + 8u * st.s, st.phase, p, abort_flag, p.lane0_wait != 0))
+            const uint32_t ready = OP == TSX_COPY ? full + 8u * st.s : computed + 16u * st.s;
+            if (!role_wait(ready, st.phase, p, abort_flag, p.lane0_wait != 0))
                 break;
             if (dyn) {
                 if (i < P) {
@@ -422,9 +458,24 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
                 trace_event<TRACE>(p, trace_counter, kTraceStore, i, st.s, st.phase);
             // release tile i - lag W once every lane's stores of it have read
             // shared memory (lanes without boxes keep out of the bulk groups)
-            if (lane < lanes) {
-                store_tile<ACC>(maps, p, tc, mine, n_boxes, lanes, base + st.s * p.stage_bytes);
-                bulk_wait_read(lag);
+            if (CG == 1) {
+                if (lane < lanes) {
+                    store_tile<ACC>(maps, p, tc, mine, n_boxes, lanes, base + st.s * p.stage_bytes);
+                    bulk_wait_read(lag);
+                }
+            } else {
+                // the first half of the boxes goes out while the compute warps
+                // finish the second
+                const int half = n_boxes / 2;
+                const int lanes_g = ACC ? 1 : half < 32 ? half : 32;
+                if (lane < lanes_g)
+                    store_boxes<ACC>(maps, p, tc, 0, half, lanes_g, base + st.s * p.stage_bytes);
+                if (!role_wait(computed + 16u * st.s + 8u, st.phase, p, abort_flag, p.lane0_wait != 0))
+                    break;
+                if (lane < lanes_g) {
+                    store_boxes<ACC>(maps, p, tc, half, n_boxes, lanes_g, base + st.s * p.stage_bytes);
+                    bulk_wait_read(2 * lag);
+                }
             }
             __syncwarp();
             if (stored >= lag) {
@@ -490,13 +541,25 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
             if constexpr (kSet) {
                 compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, tb, tid, threads, b_cur);
             } else {
+                // group by group: the units of the first half of the boxes,
+                // handed to the store warp, then those of the second
                 const uint4* B = A + p.slot_bytes / 16;
                 const uint4* C = A + 2 * (p.slot_bytes / 16);
-                for (uint32_t u = tid; u < p.vec16_per_slot; u += threads) {
-                    const uint4 va = A[u];
-                    const uint4 vb = NIN > 1 ? B[u] : va;
-                    const uint4 vc = NIN > 2 ? C[u] : va;
-                    A[u] = op_vec16<DT, OP>(va, vb, vc);
+                const uint32_t n = p.vec16_per_slot;
+                for (int g = 0; g < CG; ++g) {
+                    const uint32_t hi = g + 1 == CG ? n : n / 2;
+                    for (uint32_t u = (g == 0 ? 0u : n / 2) + tid; u < hi; u += threads) {
+                        const uint4 va = A[u];
+                        const uint4 vb = NIN > 1 ? B[u] : va;
+                        const uint4 vc = NIN > 2 ? C[u] : va;
+                        A[u] = op_vec16<DT, OP>(va, vb, vc);
+                    }
+                    if (g + 1 < CG) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if ((threadIdx.x & 31) == 0)
+                            mbar_arrive(computed + 16u * st.s + 8u * g);
+                    }
                 }
             }
             // this thread's generic-proxy writes become visible to the TMA store
@@ -505,7 +568,7 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
                 trace_event<TRACE>(p, trace_counter, kTraceBody, i, st.s, 0);
             __syncwarp();
             if ((threadIdx.x & 31) == 0)
-                mbar_arrive(computed + 8u * st.s);
+                mbar_arrive(computed + 16u * st.s + 8u * (CG - 1));
             st.next(S);
         }
     }
@@ -515,7 +578,8 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     if (warp == 0 && elected) {
         for (int s = 0; s < S; ++s) {
             mbar_inval(full + 8u * s);
-            mbar_inval(computed + 8u * s);
+            for (int g = 0; g < CG; ++g)
+                mbar_inval(computed + 16u * s + 8u * g);
             mbar_inval(empty + 8u * s);
         }
     }

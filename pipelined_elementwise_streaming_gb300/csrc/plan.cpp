@@ -199,6 +199,9 @@ int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
         return fail(why, "tuning.dynamic_share must be 1..100 percent (got %lld)", t->dynamic_share),
                TSX_ERR_INVALID;
     k->dynamic_share = t->dynamic_share > 0 ? t->dynamic_share : 0;
+    if (t->store_split > 2)
+        return fail(why, "tuning.store_split must be 1 or 2 (got %lld)", t->store_split), TSX_ERR_INVALID;
+    k->store_split = t->store_split > 0 ? t->store_split : 0;
     if (t->l2_promotion > 3)
         return fail(why, "tuning.l2_promotion must be 0..3 (got %lld)", t->l2_promotion), TSX_ERR_INVALID;
     k->l2_promotion = t->l2_promotion < 0 ? 2 : t->l2_promotion;
@@ -376,6 +379,16 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         // compute step measured slower with it on GB300)
         og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : 2) : 1;
         og->dynamic_share = og->tile_order == 2 ? (g.knobs.dynamic_share > 0 ? g.knobs.dynamic_share : 100) : 0;
+        // two groups of boxes need a compute step, an even box count and
+        // all operands staged
+        const int boxes = g.variant == TSX_TMA_RANK3 ? g.row_chunks : g.row_chunks * g.atoms;
+        const bool can_split = op != TSX_COPY && boxes % 2 == 0 && !(g.variant == TSX_TMA_MIXED && og->n_in >= 2);
+        // measured on GB300: the one-operand sqrt and exp gain 1-4 % with
+        // tiles of 16 KB or more; ops with two or three operands, and small
+        // tiles, lose
+        const bool split_pays = (op == TSX_SQRT || op == TSX_EXP) && g.slot_bytes >= 16384;
+        const bool split = g.knobs.store_split == 2 || (g.knobs.store_split == 0 && split_pays);
+        og->compute_groups = can_split && split ? 2 : 1;
     }
     og->ctas_cap = default_ctas_cap(g, op, og->stage_bytes);
     // the mixed variant's L2 prefetch of b, for the CTAs that shared memory
@@ -436,6 +449,7 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->l2_hint = og.l2_hint;
     info->tile_order = og.tile_order;
     info->dynamic_share = og.dynamic_share;
+    info->compute_groups = is_tma_variant(g.variant) ? og.compute_groups : 0;
     info->timeout_ms = g.knobs.timeout_ms;
     info->vec = og.vec;
     info->outer = og.outer;
@@ -491,6 +505,7 @@ void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t
     args->lane0_wait = og.lane0_wait ? 1 : 0;
     args->b_prefetch_ahead = og.b_prefetch_ahead;
     args->l2_hint = og.l2_hint;
+    args->compute_groups = og.compute_groups;
     args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
     args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
@@ -551,6 +566,7 @@ extern "C" void tsx_tuning_defaults(tsx_tuning* t)
     t->l2_hint = -1;
     t->tile_order = 0;
     t->dynamic_share = 0;
+    t->store_split = 0;
     t->l2_promotion = -1;
     t->timeout_ms = 0;
     t->checked = 0;

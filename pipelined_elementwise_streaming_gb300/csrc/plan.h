@@ -22,6 +22,7 @@ struct Knobs {
     int l2_hint = -1;        // < 0: the planner's; bit 0 loads, bit 1 stores evict-first
     int tile_order = 0;      // 0: the planner's; 1 static; 2 dynamic
     int dynamic_share = 0;   // 0: the planner's; else percent of the tiles claimed dynamically
+    int store_split = 0;     // 0: the planner's; 1 one group of boxes; 2 two
     int l2_promotion = 2;    // CUtensorMapL2promotion
     int timeout_ms = 1000;
     bool checked = false;
@@ -65,6 +66,7 @@ struct OpGeometry {
     int l2_hint = 0;         // TMA copies marked evict-first in L2: bit 0 loads, bit 1 stores
     int tile_order = 0;      // TMA: 1 static, 2 dynamic (tiles claimed from a counter)
     int dynamic_share = 0;   // dynamic order: percent of the tiles claimed
+    int compute_groups = 1;  // TMA: groups of boxes handed from the compute to the store warps (1, 2)
 };
 
 // Dynamic order: the tiles each of `grid` CTAs takes in the static order

@@ -229,6 +229,9 @@ __device__ __forceinline__ void bulk_wait_read(int n)
     case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
     case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
     case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group.read 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group.read 6;" ::: "memory"); break;
     default: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
     }
 }

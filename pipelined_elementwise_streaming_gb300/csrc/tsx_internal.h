@@ -31,9 +31,10 @@ constexpr int kSmemPerCtaReserved = 1024;  // the system's share of each residen
 constexpr int kMaxStoreWarps = 2;      // TMA: store warps beside the producer warp
 // TMA CTAs: the producer warp and the store warps come ahead of the compute warps
 TSX_HD constexpr int tma_role_warps(int store_warps) { return 1 + store_warps; }
-// per stage: the full, computed and empty mbarriers and the index of the
-// tile the stage holds (the dynamic tile order hands it to the consumers)
-constexpr int kTmaBarrierBytes = 32;
+// per stage: the full mbarrier, two computed ones (one per group of boxes),
+// the empty one and the index of the tile the stage holds (the dynamic tile
+// order hands it to the consumers)
+constexpr int kTmaBarrierBytes = 40;
 // Tile counters of the dynamic tile order: a plan keeps this many, one per
 // stream it launches on (two 64-bit words each: tiles claimed, CTAs done).
 constexpr int kTileCounterSlots = 64;
@@ -70,6 +71,7 @@ struct TmaArgs {
     int store_lag;          // a store warp's tiles between a store's issue and its stage's release
     int store_warps;        // store warp w of W takes the CTA's tiles w, w + W, ...
     int lane0_wait;         // 1: the producer and store warps wait on lane 0 alone
+    int compute_groups;     // 1, or 2: the first half of a tile's boxes is stored while the second is computed
     int l2_hint;            // bit 0: TMA loads, bit 1: TMA stores mark their L2 lines evict-first
     int promote_shift;      // log2(tensor-map element / element): box x coordinates are in map elements
     int rows, cols;         // tensor extent (< 2^31)

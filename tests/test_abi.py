@@ -346,3 +346,25 @@ def test_query_tile_order(tsx):
         tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"tile_order": 3})
     with pytest.raises(tsx.TsxError, match="dynamic_share"):
         tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"dynamic_share": 101})
+
+
+def test_query_store_split(tsx):
+    """Two groups of boxes for ops with a compute step, an even number of
+    boxes per tile and every operand staged; by default for sqrt and exp
+    with tiles of 16 KB or more."""
+    q = lambda *a, **k: tsx.query(*a, **k)["compute_groups"]
+    assert q("bf16", 16384, 16384, (128, 128), 2, "tma", "exp") == 2
+    assert q("bf16", 16384, 16384, (128, 128), 3, "tma", "sqrt") == 2
+    assert q("bf16", 16384, 16384, (64, 64), 3, "tma", "exp") == 1      # 8 KB tiles
+    assert q("bf16", 16384, 16384, (128, 128), 3, "tma", "mul") == 1
+    assert q("f32", 128, 1 << 20, (8, 128), 4, "tma", "exp") == 1       # 4 KB tiles
+    assert q("bf16", 16384, 16384, (128, 128), 2, "tma", "exp", tuning={"store_split": 1}) == 1
+    assert q("bf16", 16384, 16384, (128, 128), 2, "tma", "exp", tuning={"store_split": 2}) == 2
+    assert q("bf16", 16384, 16384, (128, 128), 2, "tma_rank3", "exp", tuning={"store_split": 2}) == 1  # 1 box
+    assert q("bf16", 16384, 16384, (128, 128), 2, "tma", "copy", tuning={"store_split": 2}) == 1
+    assert q("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"store_split": 2}) == 2
+    assert q("f32", 128, 1 << 20, (8, 128), 4, "tma_mixed", "fma", tuning={"store_split": 2}) == 1
+    assert q("f32", 128, 1 << 20, (8, 96), 4, "tma", "fma", tuning={"store_split": 2}) == 1   # 3 boxes
+    assert q("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "fma", tuning={"store_split": 2}) == 0
+    with pytest.raises(tsx.TsxError, match="store_split"):
+        q("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"store_split": 3})

@@ -45,6 +45,7 @@ def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", tuning=None):
     ("role_wait", [1, 2]),
     ("l2_promotion", [0, 1, 2, 3]),
     ("l2_hint", [1, 2, 3]),
+    ("store_split", [1, 2]),
     ("threads", [32, 96, 256, 960]),
     ("ctas_per_sm", [1, 2, 3]),
 ])
@@ -65,6 +66,8 @@ def test_knobs_leave_results_unchanged(tsx, knob, values, case):
                     assert info["ctas_per_sm"] <= v
                 if knob in ("store_lag", "store_warps", "role_wait", "l2_hint"):
                     assert info[knob] == q[knob] == v
+                if knob == "store_split":
+                    assert info["compute_groups"] == q["compute_groups"] <= v
                 if knob == "l2_promotion":
                     assert info["l2_promotion"] == q["l2_promotion"] == v
 

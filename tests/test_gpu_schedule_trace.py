@@ -46,14 +46,15 @@ def tsx():
     return m
 
 
-def _run(tsx, op, tiles, stages, variant="tma", tuning=None):
-    """fp32 [8 * tiles, 32] with 8x32 boxes: one tile per row band, at most
-    one CTA per SM.  Returns (trace [G, cap, 4], effective store lag, store
-    warps)."""
-    rows, cols = 8 * tiles, 32
+def _run(tsx, op, tiles, stages, variant="tma", tuning=None, cols=32):
+    """fp32 [8 * tiles, cols] with 8 x cols boxes (one box per 32 columns):
+    one tile per row band, at most one CTA per SM.  Returns (trace [G, cap,
+    4], effective store lag, store warps, the dynamic order's static tiles
+    per CTA, the tile order)."""
+    rows = 8 * tiles
     a = random_bits("f32", (rows, cols), tiles + stages)
     b = random_bits("f32", (rows, cols), tiles + stages + 1)
-    with tsx.Plan("f32", rows, cols, box=(8, 32), stages=stages, variant=variant,
+    with tsx.Plan("f32", rows, cols, box=(8, cols), stages=stages, variant=variant,
                   tuning=dict({"ctas_per_sm": 1}, **(tuning or {}))) as plan:
         plan.enable_trace(256)
         da, db = to_dev(a, "f32"), to_dev(b, "f32")
@@ -106,11 +107,13 @@ def _check_dynamic(trace, tiles, P):
     return counts
 
 
-def _check_cta(ev, N, S, lag, op, W=1, dynamic=False):
+def _check_cta(ev, N, S, lag, op, W=1, dynamic=False, split=False):
     """One CTA's events against the model; W store warps take the CTA's
     tiles in turn (warp w: tiles w, w + W, ...), each releasing its tile j
     after storing its tile j + lag (in the dynamic order also its last
-    `lag` tiles once the tiles have run out)."""
+    `lag` tiles once the tiles have run out).  With split stores the store of
+    a tile's first half starts before its compute ends: the tile must then be
+    computed before its stage is released."""
     ev = ev[ev[:, 1] != 0]
     assert np.array_equal(ev[:, 0], np.arange(len(ev))), "sequence numbers are not dense"
     kind, k, a, b = ev[:, 1], ev[:, 2].astype(np.int64), ev[:, 3] & 0xFFFF, ev[:, 3] >> 16
@@ -156,13 +159,17 @@ def _check_cta(ev, N, S, lag, op, W=1, dynamic=False):
 
     for i in range(N):
         assert seq[(LOAD, i)] < seq[(STORE, i)]
-        if op != "copy":
+        if op != "copy" and not split:
             assert seq[(LOAD, i)] < seq[(WAIT, i)] < seq[(BODY, i)] < seq[(STORE, i)]
+        if split:
+            assert seq[(LOAD, i)] < seq[(WAIT, i)] < seq[(STORE, i)]
+            if (RELEASE, i) in seq:
+                assert seq[(BODY, i)] < seq[(RELEASE, i)]
         if i >= S:
             assert seq[(RELEASE, i - S)] < seq[(REUSE, i)] < seq[(LOAD, i)], f"stage of tile {i} reused early"
 
 
-def _check_all(trace, tiles, stages, lag, op, W, order, P):
+def _check_all(trace, tiles, stages, lag, op, W, order, P, split=False):
     G = trace.shape[0]
     assert G <= tiles
     if order == 2:
@@ -170,7 +177,7 @@ def _check_all(trace, tiles, stages, lag, op, W, order, P):
     else:
         counts = [len(st.cta_tiles(tiles, G, c)) for c in range(G)]
     for c in range(G):
-        _check_cta(trace[c], counts[c], stages, lag, op, W, dynamic=order == 2)
+        _check_cta(trace[c], counts[c], stages, lag, op, W, dynamic=order == 2, split=split)
 
 
 ORDERS = [{"tile_order": 1}, {"tile_order": 2}, {"tile_order": 2, "dynamic_share": 100},
@@ -239,3 +246,14 @@ def test_trace_is_refused_where_no_traced_kernel_exists(tsx):
         with pytest.raises(tsx.TsxError) as ei:
             plan.trace()
         assert ei.value.code == tsx.TSX_ERR_INVALID
+
+
+@pytest.mark.parametrize("store_warps,store_lag", [(1, 0), (1, 1), (2, 0), (1, 2)])
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_split_stores_follow_the_model(tsx, stages, store_warps, store_lag):
+    """Two groups of boxes per tile (the first half stored while the second
+    is computed): the schedule is the model's, the results the oracle's."""
+    tiles = 900
+    trace, lag, W, P, got = _run(tsx, "add", tiles, stages, cols=64,
+                                 tuning={"store_split": 2, "store_warps": store_warps, "store_lag": store_lag})
+    _check_all(trace, tiles, stages, lag, "add", W, got, P, split=True)
