@@ -541,25 +541,29 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
             if constexpr (kSet) {
                 compute_tile_mixed<DT, OP>(p, A, A + p.slot_bytes / 16, tb, tid, threads, b_cur);
             } else {
-                // group by group: the units of the first half of the boxes,
-                // handed to the store warp, then those of the second
                 const uint4* B = A + p.slot_bytes / 16;
                 const uint4* C = A + 2 * (p.slot_bytes / 16);
                 const uint32_t n = p.vec16_per_slot;
-                for (int g = 0; g < CG; ++g) {
-                    const uint32_t hi = g + 1 == CG ? n : n / 2;
-                    for (uint32_t u = (g == 0 ? 0u : n / 2) + tid; u < hi; u += threads) {
+                uint32_t u = tid;
+                if (CG == 2) {
+                    // the units of the first half of the boxes, handed to the
+                    // store warp before those of the second
+                    for (; u < n / 2; u += threads) {
                         const uint4 va = A[u];
                         const uint4 vb = NIN > 1 ? B[u] : va;
                         const uint4 vc = NIN > 2 ? C[u] : va;
                         A[u] = op_vec16<DT, OP>(va, vb, vc);
                     }
-                    if (g + 1 < CG) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if ((threadIdx.x & 31) == 0)
-                            mbar_arrive(computed + 16u * st.s + 8u * g);
-                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if ((threadIdx.x & 31) == 0)
+                        mbar_arrive(computed + 16u * st.s);
+                }
+                for (; u < n; u += threads) {
+                    const uint4 va = A[u];
+                    const uint4 vb = NIN > 1 ? B[u] : va;
+                    const uint4 vc = NIN > 2 ? C[u] : va;
+                    A[u] = op_vec16<DT, OP>(va, vb, vc);
                 }
             }
             // this thread's generic-proxy writes become visible to the TMA store
