@@ -164,9 +164,6 @@ typedef struct tsx_plan_info {
      * producer prefetches b into L2 (from the CTAs per SM: tsx_plan_query
      * assumes the CTAs that shared memory alone fits) */
     int32_t b_prefetch;
-    /* TMA variants: L2 eviction priority of the TMA copies (bit 0 loads,
-     * bit 1 stores marked evict-first; 0 the normal priority) */
-    int32_t l2_hint;
     /* TMA variants: the order CTAs take tiles in, 1 static (CTA c of G takes
      * c, c + G, ...), 2 dynamic (TSX_COPY: each CTA's first tiles as in the
      * static order, every later one claimed from a per-launch counter) */
@@ -210,10 +207,10 @@ typedef struct tsx_plan_info {
  *                c, c + G, ...), 2 dynamic (a CTA's first tiles as in the
  *                static order, then tiles claimed in order from a counter,
  *                so that CTAs streaming faster take more tiles); <= 0: the
- *                planner's: dynamic for launches of at least 16 tiles per
- *                CTA (the host-only query, which knows no grid, reports
- *                that case).  The other ops, and TSX_ACCUMULATE, always
- *                take the static order
+ *                planner's: dynamic for tiles of 16 KB or more in launches
+ *                of at least 16 tiles per CTA (the host-only query, which
+ *                knows no grid, reports that case).  The other ops, and
+ *                TSX_ACCUMULATE, always take the static order
  *  dynamic_share dynamic order: about this percentage of the tiles (the
  *                last ones) is claimed from the counter, 1..100 (a CTA
  *                takes at least max(1, S - 1) tiles in the static order
@@ -224,10 +221,6 @@ typedef struct tsx_plan_info {
  *                warps work on the second, 1 stores the tile at once; <= 0:
  *                the planner's (2 for sqrt and exp with tiles of 16 KB or
  *                more)
- *  l2_hint       TMA variants: 0..3, bit 0 marks the lines of the TMA loads
- *                evict-first in L2, bit 1 those of the TMA stores (the
- *                reduce-store of TSX_ACCUMULATE keeps the normal priority);
- *                < 0: the planner's
  *  l2_promotion  CUtensorMapL2promotion of the tensor maps, 0..3 (none, 64,
  *                128, 256 B); < 0: 128 B, the value of TVM docs
  *                "copy_async -> tma" ("Generated TIRx IR")
@@ -236,7 +229,7 @@ typedef struct tsx_plan_info {
  *                stream and return the device status (debugging) */
 typedef struct tsx_tuning {
     int32_t threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait;
-    int32_t b_prefetch, l2_hint, tile_order, dynamic_share, store_split;
+    int32_t b_prefetch, tile_order, dynamic_share, store_split;
 } tsx_tuning;
 
 /* Fill *t with the planner's-choice value of every field.  No source on the

@@ -56,7 +56,7 @@ class tsx_plan_info(ctypes.Structure):
                                                "ctas_per_sm", "grid", "sm_count", "block_threads")] + \
                [("pitch", ctypes.c_int64), ("tma_elem_bytes", ctypes.c_int32), ("store_lag", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("store_warps", ctypes.c_int32), ("role_wait", ctypes.c_int32),
-                ("b_prefetch", ctypes.c_int32), ("l2_hint", ctypes.c_int32), ("tile_order", ctypes.c_int32),
+                ("b_prefetch", ctypes.c_int32), ("tile_order", ctypes.c_int32),
                 ("dynamic_share", ctypes.c_int32), ("compute_groups", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
@@ -70,7 +70,7 @@ class tsx_plan_info(ctypes.Structure):
 class tsx_tuning(ctypes.Structure):
     """Launch knobs of a plan (include/tsx.h); see ``tuning()``."""
     _fields_ = [(n, ctypes.c_int32) for n in ("threads", "ctas_per_sm", "store_lag", "l2_promotion", "timeout_ms",
-                                               "checked", "store_warps", "role_wait", "b_prefetch", "l2_hint",
+                                               "checked", "store_warps", "role_wait", "b_prefetch",
                                                "tile_order", "dynamic_share", "store_split")]
 
 
@@ -170,7 +170,7 @@ def _code(table: dict, key) -> int:
 def tuning(**knobs) -> tsx_tuning:
     """A tsx_tuning with the planner's choices, except the knobs given
     (threads, ctas_per_sm, store_lag, l2_promotion, timeout_ms, checked, store_warps, role_wait,
-    b_prefetch, l2_hint, tile_order, dynamic_share, store_split)."""
+    b_prefetch, tile_order, dynamic_share, store_split)."""
     t = tsx_tuning()
     tsx_tuning_defaults(ctypes.byref(t))
     for k, v in knobs.items():

@@ -142,25 +142,27 @@ namespace {
 // The mixed variant runs its own instantiation only for ops with a b operand.
 bool mixed_launch(int variant, int op) { return variant == TSX_TMA_MIXED && op_arity(op) >= 2; }
 
-int tma_kind(int variant, int op, bool accumulate, bool traced)
+int tma_kind(int variant, int op, bool accumulate, bool traced, bool split)
 {
     if (accumulate)
         return kTmaAccumulate;
     if (mixed_launch(variant, op))
         return kTmaMixed;
+    if (split)
+        return traced ? kTmaTracedSplit : kTmaSplit;
     return traced ? kTmaTraced : kTmaPlain;
 }
 
 // The reduce-store is offered by the two all-TMA variants.
 bool accumulate_offered(int variant) { return variant == TSX_TMA || variant == TSX_TMA_RANK3; }
 
-const void* kernel_of(int variant, int dtype, int op, bool accumulate, bool traced)
+const void* kernel_of(int variant, int dtype, int op, bool accumulate, bool traced, bool split)
 {
     if (variant == TSX_LDGSTS)
         return ldgsts_kernel(dtype, op);
     if (variant == TSX_SYNC)
         return sync_kernel(dtype, op);
-    return tma_kernel(dtype, op, tma_kind(variant, op, accumulate, traced));
+    return tma_kernel(dtype, op, tma_kind(variant, op, accumulate, traced, split));
 }
 
 // The trace ring of the traced kernel (test hook): large enough for `grid`
@@ -194,8 +196,10 @@ int prepare_op(tsx_plan* p, int op, bool accumulate, tsx_plan::OpLaunch** out)
         if (accumulate) {
             L.og.tile_order = 1;   // the reduce-store kernels take the static order
             L.og.dynamic_share = 0;
+            L.og.compute_groups = 1;   // and store a tile at once
         }
-        const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate, p->trace_cap > 0);
+        const void* fn = kernel_of(p->g.variant, p->g.dtype, op, accumulate, p->trace_cap > 0,
+                                   L.og.compute_groups == 2);
         if (!fn)
             return set_error(TSX_ERR_UNSUPPORTED, "traced launches: only fp32 copy and add have a traced kernel");
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.og.smem_bytes));
@@ -710,8 +714,8 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
             args.trace = p->trace_buf;
             args.trace_cap = p->trace_cap;
         }
-        e = launch_tma(g.dtype, op, tma_kind(g.variant, op, accumulate, p->trace_cap > 0), L->grid, L->og.block_threads,
-                       L->og.smem_bytes, st, maps, args);
+        e = launch_tma(g.dtype, op, tma_kind(g.variant, op, accumulate, p->trace_cap > 0, L->og.compute_groups == 2),
+                       L->grid, L->og.block_threads, L->og.smem_bytes, st, maps, args);
     } else {
         int vb = g.copy_vec_bytes < align ? g.copy_vec_bytes : align;
         if (vb < 4)

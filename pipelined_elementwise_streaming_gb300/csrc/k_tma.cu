@@ -59,8 +59,7 @@ using namespace dev;
 // `slot`: each of the first `lanes` lanes stores the boxes numbered lane,
 // lane + lanes, ... of the n_boxes of a full tile (`mine` is its first) and
 // commits them as one bulk group of its own; with ACC a reduce-store that
-// adds the tile into global memory.  With bit 1 of l2_hint a plain store
-// marks its lines evict-first in L2.
+// adds the tile into global memory.
 template <bool ACC>
 __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p, const TileCursor& tc,
                                            const BoxRef& mine, int n_boxes, int lanes, uint32_t slot)
@@ -77,16 +76,12 @@ __device__ __forceinline__ void store_tile(const TmaMaps& maps, const TmaArgs& p
             const int z = static_cast<int>(tc.ct * p.atoms);
             if constexpr (ACC)
                 tma_reduce_add_3d(x.map, src, 0, y, z);
-            else if (p.l2_hint & 2)
-                tma_store_3d_hint(x.map, src, 0, y, z, l2_evict_first_policy());
             else
                 tma_store_3d(x.map, src, 0, y, z);
         } else {
             const int xc = (b.col0 >> p.promote_shift) + x.dx;
             if constexpr (ACC)
                 tma_reduce_add_2d(x.map, src, xc, y);
-            else if (p.l2_hint & 2)
-                tma_store_2d_hint(x.map, src, xc, y, l2_evict_first_policy());
             else
                 tma_store_2d(x.map, src, xc, y);
         }
@@ -247,8 +242,12 @@ __device__ __forceinline__ void trace_event(const TmaArgs& p, uint32_t* counter,
     }
 }
 
-template <int DT, int OP, bool MIXED, bool ACC, bool TRACE = false>
-__global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
+// Registers: at most 56 a thread (96 in the mixed variant, whose compute
+// threads hold b a tile ahead).  A warp's registers are allocated in blocks
+// of 256, so at 58 a warp takes 2048 instead of 1792 and one CTA of 128
+// threads per SM fewer fits: on GB300 such a build ran fp32 sqrt 7 % slower.
+template <int DT, int OP, bool MIXED, bool ACC, bool TRACE = false, bool SPLIT = false>
+__global__ void __maxnreg__(MIXED ? kMixedMaxRegs : kMaxRegs)
     tma_ewise(const __grid_constant__ TmaMaps maps, const TmaArgs p)
 {
     constexpr int NIN = op_arity(OP);
@@ -263,8 +262,9 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     // two per stage (computed + 16 s + 8 g): group g of the stage's boxes computed
     const uint32_t computed = full + 8u * S;
     const uint32_t empty = computed + 16u * S;
-    // groups of boxes the compute warps hand to the store warps one by one (1 or 2)
-    const int CG = MIXED ? 1 : p.compute_groups;
+    // groups of boxes the compute warps hand to the store warps one by one:
+    // two in the split instantiations (ops with a compute step)
+    constexpr int CG = SPLIT && !MIXED && OP != TSX_COPY ? 2 : 1;
     // dynamic tile order: the tile each stage holds (-1: no more tiles)
     volatile int64_t* tile_of = reinterpret_cast<volatile int64_t*>(smem + (empty + 8u * S - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (empty + 16u * S - base));
@@ -291,8 +291,6 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     constexpr bool kDynamic = OP == TSX_COPY && !MIXED && !ACC;
     const bool dyn = kDynamic && p.tile_counter != nullptr;
     const int64_t P = p.static_tiles > 0 ? p.static_tiles : 1;
-    // store warps that take tiles (copy: only if they divide S, see below)
-    const int W = OP == TSX_COPY && S % p.store_warps != 0 ? 1 : p.store_warps;
 
     // Pre-prologue: the barriers of every stage; descriptor prefetch.
     if (warp == 0 && elected) {
@@ -363,6 +361,8 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
             // Lane 0 claims the tile of k + 1 as soon as it knows the tile
             // of k, so the atomic's round trip overlaps the wait for a free
             // stage, and publishes each claimed tile in the stage's slot.
+            // one "no more tiles" stage per store warp that takes tiles
+            const int W = OP == TSX_COPY && S % p.store_warps != 0 ? 1 : p.store_warps;
             const int64_t static_end = P * G;
             int64_t claim = p.tiles;   // lane 0: the claimed tile of the next k (>= tiles: none)
             int ended = 0;             // "no more tiles" stages issued
@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
         // loads complete in any order, so there the stage's previous tile
         // must be this warp's own: W must divide S (the planner ensures it;
         // a second store warp that would break it stays idle).
+        const int W = OP == TSX_COPY && S % p.store_warps != 0 ? 1 : p.store_warps;
         const int sw = warp - 1;   // this warp takes the CTA's tiles sw, sw + W, ...
         const int n_boxes = p.rank3 ? p.row_chunks : p.row_chunks * p.atoms;
         // lanes issuing stores: one per box, except that reduce-stores go out
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
                 trace_event<TRACE>(p, trace_counter, kTraceStore, i, st.s, st.phase);
             // release tile i - lag W once every lane's stores of it have read
             // shared memory (lanes without boxes keep out of the bulk groups)
-            if (CG == 1) {
+            if constexpr (CG == 1) {
                 if (lane < lanes) {
                     store_tile<ACC>(maps, p, tc, mine, n_boxes, lanes, base + st.s * p.stage_bytes);
                     bulk_wait_read(lag);
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
                 const uint4* C = A + 2 * (p.slot_bytes / 16);
                 const uint32_t n = p.vec16_per_slot;
                 uint32_t u = tid;
-                if (CG == 2) {
+                if constexpr (CG == 2) {
                     // the units of the first half of the boxes, handed to the
                     // store warp before those of the second
                     for (; u < n / 2; u += threads) {
@@ -602,28 +603,38 @@ __global__ void __launch_bounds__(MIXED ? kMixedMaxThreads : kMaxThreads)
     {(const void*)tma_ewise<DT, 0, M, A>, (const void*)tma_ewise<DT, 1, M, A>, (const void*)tma_ewise<DT, 2, M, A>, \
      (const void*)tma_ewise<DT, 3, M, A>, (const void*)tma_ewise<DT, 4, M, A>, (const void*)tma_ewise<DT, 5, M, A>}
 #define TSX_KIND(M, A) {TSX_ROW(TSX_F16, M, A), TSX_ROW(TSX_BF16, M, A), TSX_ROW(TSX_F32, M, A)}
-// indexed by TmaKind: plain, mixed, accumulate
-const void* const kKernels[3][3][6] = {TSX_KIND(false, false), TSX_KIND(true, false), TSX_KIND(false, true)};
+// the split instantiations (copy has no compute step to split: its plain one)
+#define TSX_SPLIT_ROW(DT) \
+    {(const void*)tma_ewise<DT, 0, false, false>, (const void*)tma_ewise<DT, 1, false, false, false, true>, \
+     (const void*)tma_ewise<DT, 2, false, false, false, true>, (const void*)tma_ewise<DT, 3, false, false, false, true>, \
+     (const void*)tma_ewise<DT, 4, false, false, false, true>, (const void*)tma_ewise<DT, 5, false, false, false, true>}
+// indexed by TmaKind: plain, mixed, accumulate, split
+const void* const kKernels[4][3][6] = {TSX_KIND(false, false), TSX_KIND(true, false), TSX_KIND(false, true),
+                                       {TSX_SPLIT_ROW(TSX_F16), TSX_SPLIT_ROW(TSX_BF16), TSX_SPLIT_ROW(TSX_F32)}};
+#undef TSX_SPLIT_ROW
 #undef TSX_KIND
 #undef TSX_ROW
 
 }  // namespace
 
 // the traced instantiations (test hook)
-const void* traced_kernel(int dtype, int op)
+const void* traced_kernel(int dtype, int op, bool split)
 {
     if (dtype != TSX_F32)
         return nullptr;
-    if (op == TSX_COPY)
+    if (op == TSX_COPY && !split)
         return (const void*)tma_ewise<TSX_F32, TSX_COPY, false, false, true>;
     if (op == TSX_ADD)
-        return (const void*)tma_ewise<TSX_F32, TSX_ADD, false, false, true>;
+        return split ? (const void*)tma_ewise<TSX_F32, TSX_ADD, false, false, true, true>
+                     : (const void*)tma_ewise<TSX_F32, TSX_ADD, false, false, true>;
     return nullptr;
 }
 
 const void* tma_kernel(int dtype, int op, int kind)
 {
-    return kind == kTmaTraced ? traced_kernel(dtype, op) : kKernels[kind][dtype][op];
+    if (kind == kTmaTraced || kind == kTmaTracedSplit)
+        return traced_kernel(dtype, op, kind == kTmaTracedSplit);
+    return kKernels[kind][dtype][op];
 }
 
 cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_t smem, cudaStream_t stream,

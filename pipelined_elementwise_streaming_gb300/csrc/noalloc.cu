@@ -152,7 +152,8 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
     rc = make_op_geometry(g, op, max_smem, &og, &why);
     if (rc != TSX_OK)
         return fail(rc, "no launch for these arguments", why);
-    const void* fn = tma_kernel(dtype, op);
+    const int kind = og.compute_groups == 2 ? kTmaSplit : kTmaPlain;
+    const void* fn = tma_kernel(dtype, op, kind);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(og.smem_bytes));
     if (e != cudaSuccess)
         return fail_cuda(e, "cudaFuncSetAttribute");
@@ -184,7 +185,7 @@ extern "C" int tsx_ewise_noalloc(tsx_dtype dtype, int64_t rows, int64_t cols, in
     e = cudaMemsetAsync(scratch, 0, kStatusWordBytes, st);
     if (e != cudaSuccess)
         return fail_cuda(e, "clearing the status word");
-    e = launch_tma(dtype, op, kTmaPlain, grid, og.block_threads, og.smem_bytes, st, maps, args);
+    e = launch_tma(dtype, op, kind, grid, og.block_threads, og.smem_bytes, st, maps, args);
     if (e != cudaSuccess)
         return fail_cuda(e, "kernel launch");
     if (status_out) {

@@ -188,9 +188,6 @@ int resolve_knobs(const tsx_tuning* t, Knobs* k, std::string* why)
     if (t->b_prefetch > 8)
         return fail(why, "tuning.b_prefetch must be at most 8 (got %lld)", t->b_prefetch), TSX_ERR_INVALID;
     k->b_prefetch = t->b_prefetch;
-    if (t->l2_hint > 3)
-        return fail(why, "tuning.l2_hint must be 0..3 (got %lld)", t->l2_hint), TSX_ERR_INVALID;
-    k->l2_hint = t->l2_hint;
     if (t->tile_order > 2)
         return fail(why, "tuning.tile_order must be 1 (static) or 2 (dynamic) (got %lld)", t->tile_order),
                TSX_ERR_INVALID;
@@ -374,10 +371,12 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         og->store_warps = ss.store_warps;
         og->store_lag = ss.store_lag;
         og->lane0_wait = ss.lane0_wait;
-        og->l2_hint = g.knobs.l2_hint >= 0 ? g.knobs.l2_hint : 0;
         // the dynamic order is built into the copy kernels only (ops with a
-        // compute step measured slower with it on GB300)
-        og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : 2) : 1;
+        // compute step measured slower with it on GB300); by default for
+        // tiles of 16 KB or more: with smaller tiles the claims on the one
+        // counter came too fast (fp32 copy in 4 KB tiles: half the speed)
+        const int order = g.slot_bytes >= kDynamicMinTileBytes ? 2 : 1;
+        og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : order) : 1;
         og->dynamic_share = og->tile_order == 2 ? (g.knobs.dynamic_share > 0 ? g.knobs.dynamic_share : 100) : 0;
         // two groups of boxes need a compute step, an even box count and
         // all operands staged
@@ -446,7 +445,6 @@ void fill_info(const Geometry& g, const OpGeometry& og, tsx_plan_info* info)
     info->store_warps = is_tma_variant(g.variant) ? og.store_warps : 0;
     info->role_wait = is_tma_variant(g.variant) ? (og.lane0_wait ? 2 : 1) : 0;
     info->b_prefetch = og.b_prefetch_ahead;
-    info->l2_hint = og.l2_hint;
     info->tile_order = og.tile_order;
     info->dynamic_share = og.dynamic_share;
     info->compute_groups = is_tma_variant(g.variant) ? og.compute_groups : 0;
@@ -504,8 +502,6 @@ void fill_tma_args(const Geometry& g, const OpGeometry& og, int* status, int64_t
     args->store_warps = og.store_warps;
     args->lane0_wait = og.lane0_wait ? 1 : 0;
     args->b_prefetch_ahead = og.b_prefetch_ahead;
-    args->l2_hint = og.l2_hint;
-    args->compute_groups = og.compute_groups;
     args->promote_shift = g.tma_es == 8 * g.es ? 3 : g.tma_es == 4 * g.es ? 2 : g.tma_es == 2 * g.es ? 1 : 0;
     args->box_bytes = uint32_t(g.rows_per_load) * uint32_t(g.inner_bytes);
     args->swizzle_mask = g.swizzle_bytes == 128 ? 7 : g.swizzle_bytes == 64 ? 3 : g.swizzle_bytes == 32 ? 1 : 0;
@@ -563,7 +559,6 @@ extern "C" void tsx_tuning_defaults(tsx_tuning* t)
     t->store_warps = 0;
     t->role_wait = 0;
     t->b_prefetch = -1;
-    t->l2_hint = -1;
     t->tile_order = 0;
     t->dynamic_share = 0;
     t->store_split = 0;

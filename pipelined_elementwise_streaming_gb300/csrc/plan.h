@@ -19,7 +19,6 @@ struct Knobs {
     int store_warps = 0;     // 0: the planner's
     int role_wait = 0;       // 0: the planner's; 1: every lane waits; 2: lane 0 waits
     int b_prefetch = -1;     // < 0: the planner's
-    int l2_hint = -1;        // < 0: the planner's; bit 0 loads, bit 1 stores evict-first
     int tile_order = 0;      // 0: the planner's; 1 static; 2 dynamic
     int dynamic_share = 0;   // 0: the planner's; else percent of the tiles claimed dynamically
     int store_split = 0;     // 0: the planner's; 1 one group of boxes; 2 two
@@ -63,7 +62,6 @@ struct OpGeometry {
     bool lane0_wait = false; // the producer and store warps wait on lane 0 alone
     int ctas_cap = 0;        // at most this many CTAs per SM (0: occupancy)
     int b_prefetch_ahead = 0;  // mixed variant: b's L2 prefetch, tiles beyond the producer's loads
-    int l2_hint = 0;         // TMA copies marked evict-first in L2: bit 0 loads, bit 1 stores
     int tile_order = 0;      // TMA: 1 static, 2 dynamic (tiles claimed from a counter)
     int dynamic_share = 0;   // dynamic order: percent of the tiles claimed
     int compute_groups = 1;  // TMA: groups of boxes handed from the compute to the store warps (1, 2)

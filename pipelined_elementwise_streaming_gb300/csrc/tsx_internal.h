@@ -20,8 +20,13 @@ namespace tsx {
 constexpr int kMaxStages = 16;
 constexpr int kMaxThreads = 1024;
 // CTA threads of the mixed variant's kernel (its compute threads hold b in
-// registers one tile ahead: the lower bound leaves them 102 registers)
+// registers one tile ahead)
 constexpr int kMixedMaxThreads = 640;
+// Register caps of the TMA elementwise kernels: every thread count up to
+// kMaxThreads (kMixedMaxThreads) still fits the SM's 64 K registers.
+constexpr int kMaxRegs = 56;
+constexpr int kMixedMaxRegs = 96;
+static_assert(kMaxRegs * kMaxThreads <= 65536 && kMixedMaxRegs * kMixedMaxThreads <= 65536, "register caps");
 constexpr int kSmemAlign = 1024;       // 128-B swizzle pattern period
 constexpr int kBoxMax = 256;           // per TMA box dimension
 constexpr int kSwizzleAtom = 128;      // bytes
@@ -42,6 +47,9 @@ constexpr int kTileCounterSlots = 64;
 // many tiles per CTA (GB300: copies of 2 to 4 tiles per CTA were 12-14 %
 // slower in it, of 36 or more 10-11 % faster).
 constexpr int kDynamicMinTilesPerCta = 16;
+// ... and tiles of at least this many bytes (an fp32 copy in 4 KB tiles ran
+// at half the speed in it: one counter, 700 claims per microsecond).
+constexpr uint32_t kDynamicMinTileBytes = 16384;
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
 TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }
@@ -71,8 +79,6 @@ struct TmaArgs {
     int store_lag;          // a store warp's tiles between a store's issue and its stage's release
     int store_warps;        // store warp w of W takes the CTA's tiles w, w + W, ...
     int lane0_wait;         // 1: the producer and store warps wait on lane 0 alone
-    int compute_groups;     // 1, or 2: the first half of a tile's boxes is stored while the second is computed
-    int l2_hint;            // bit 0: TMA loads, bit 1: TMA stores mark their L2 lines evict-first
     int promote_shift;      // log2(tensor-map element / element): box x coordinates are in map elements
     int rows, cols;         // tensor extent (< 2^31)
     int box_rows, box_cols;
@@ -138,7 +144,7 @@ struct CopyArgs {
 // accumulate (the result reduce-added into out), and traced (a plain kernel
 // that also records its schedule; fp32 copy and add only, else NULL).
 // maps[0..2] are the TMA-loaded operands in slot order, maps[3] the output.
-enum TmaKind { kTmaPlain = 0, kTmaMixed = 1, kTmaAccumulate = 2, kTmaTraced = 3 };
+enum TmaKind { kTmaPlain = 0, kTmaMixed = 1, kTmaAccumulate = 2, kTmaSplit = 3, kTmaTraced = 4, kTmaTracedSplit = 5 };
 const void* tma_kernel(int dtype, int op, int kind = kTmaPlain);
 cudaError_t launch_tma(int dtype, int op, int kind, int grid, int threads, size_t smem, cudaStream_t stream,
                        const CUtensorMap* maps, const TmaArgs& args);

@@ -137,23 +137,15 @@ __device__ __forceinline__ BoxRef box_ref(const TmaMaps& maps, const TmaArgs& p,
 __device__ __forceinline__ bool box_in(const BoxRef& x, const TileBoxes& b) { return x.r < b.chunks && x.a < b.atoms; }
 
 // Load box x of the tile at origin b (column tile ct) into the stage at
-// shared address `stage`, completing on `bar`; with bit 0 of l2_hint the
-// lines are marked evict-first in L2.
+// shared address `stage`, completing on `bar`.
 __device__ __forceinline__ void load_box(const TmaArgs& p, const BoxRef& x, const TileBoxes& b, int64_t ct,
                                          uint32_t stage, uint32_t bar)
 {
     const int y = b.row0 + x.dy;
-    if (p.l2_hint & 1) {
-        const uint64_t pol = l2_evict_first_policy();
-        if (p.rank3)
-            tma_load_3d_hint(stage + x.off, x.map, 0, y, static_cast<int>(ct * p.atoms), bar, pol);
-        else
-            tma_load_2d_hint(stage + x.off, x.map, (b.col0 >> p.promote_shift) + x.dx, y, bar, pol);
-    } else if (p.rank3) {
+    if (p.rank3)
         tma_load_3d(stage + x.off, x.map, 0, y, static_cast<int>(ct * p.atoms), bar);
-    } else {
+    else
         tma_load_2d(stage + x.off, x.map, (b.col0 >> p.promote_shift) + x.dx, y, bar);
-    }
 }
 
 // The producer warp's issue of one tile: lane 0 arrives on `bar` with

@@ -312,24 +312,11 @@ def test_query_mixed_prefetch_lead(tsx):
     assert tsx.query("f32", 1024, 1 << 16, (8, 128), 4, "tma", "mul")["b_prefetch"] == 0
 
 
-def test_query_l2_hint(tsx):
-    """The L2 eviction hint of the TMA copies: 0..3 (bit 0 loads, bit 1
-    stores evict-first), the planner's default, and out-of-range values
-    declined with the reason."""
-    base = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma")
-    assert base["l2_hint"] in (0, 1, 2, 3)
-    for h in range(4):
-        assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"l2_hint": h})["l2_hint"] == h
-    with pytest.raises(tsx.TsxError, match="l2_hint"):
-        tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "fma", tuning={"l2_hint": 4})
-    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "fma", tuning={"l2_hint": 3})["l2_hint"] == 0
-
-
 def test_query_tile_order(tsx):
-    """TMA copies take tiles in the dynamic order unless told otherwise
-    (the last `dynamic_share` percent claimed from a counter); every other
-    op, and the reduce-store, keep the static order; the ablations and row
-    sums have no tile order."""
+    """TMA copies of tiles of 16 KB or more take tiles in the dynamic order
+    unless told otherwise (the last `dynamic_share` percent claimed from a
+    counter); every other op, and the reduce-store, keep the static order;
+    the ablations and row sums have no tile order."""
     q = tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "copy")
     assert (q["tile_order"], q["dynamic_share"]) == (2, 100)
     assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma_rank3", "copy")["tile_order"] == 2
@@ -341,6 +328,8 @@ def test_query_tile_order(tsx):
     for op in ("sqrt", "exp", "add", "mul", "fma"):
         q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", op, tuning={"tile_order": 2})
         assert (q["tile_order"], q["dynamic_share"]) == (1, 0), op
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy")["tile_order"] == 1      # 4 KB tiles
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"tile_order": 2})["tile_order"] == 2
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "copy")["tile_order"] == 0
     with pytest.raises(tsx.TsxError, match="tile_order"):
         tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"tile_order": 3})

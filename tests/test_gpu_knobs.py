@@ -44,7 +44,6 @@ def _run(tsx, dtype, op, rows, cols, box, stages, variant="tma", tuning=None):
     ("store_warps", [1, 2]),
     ("role_wait", [1, 2]),
     ("l2_promotion", [0, 1, 2, 3]),
-    ("l2_hint", [1, 2, 3]),
     ("store_split", [1, 2]),
     ("threads", [32, 96, 256, 960]),
     ("ctas_per_sm", [1, 2, 3]),
@@ -64,7 +63,7 @@ def test_knobs_leave_results_unchanged(tsx, knob, values, case):
                     assert info["threads"] == q["threads"] == v
                 if knob == "ctas_per_sm":
                     assert info["ctas_per_sm"] <= v
-                if knob in ("store_lag", "store_warps", "role_wait", "l2_hint"):
+                if knob in ("store_lag", "store_warps", "role_wait"):
                     assert info[knob] == q[knob] == v
                 if knob == "store_split":
                     assert info["compute_groups"] == q["compute_groups"] <= v
