@@ -1,8 +1,9 @@
 // The TMA circular-buffer elementwise kernel.
 //
 // A persistent CTA c of G takes tiles c, c + G, c + 2G, ... (row-major tile
-// order) and streams them through S stage buffers in shared memory.  The
-// warps of a CTA have three roles:
+// order) and streams them through S stage buffers in shared memory; a long
+// copy takes its first tiles that way and claims the rest from a counter
+// (the dynamic tile order, below).  The warps of a CTA have three roles:
 //
 //   warp 0      the producer: lane 0 arrives once on the stage's `full`
 //               mbarrier with expect_tx = the bytes of the stage's loads,
@@ -41,6 +42,11 @@
 // the next tile's stores; with two store warps the other warp stores the
 // next tile meanwhile, so each can release its stage as soon as its own
 // stores have read it.
+//
+// In the split instantiations (sqrt and exp with large tiles) the compute
+// warps hand a tile over in two halves of its boxes, each with its own
+// `computed` barrier, and the store warp stores the first half while the
+// second is computed.
 //
 // Every mbarrier wait is bounded in time and also gives up when another
 // thread has raised the CTA's abort flag.  A wait that runs out records
