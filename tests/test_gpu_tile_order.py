@@ -166,3 +166,35 @@ def test_planner_takes_the_dynamic_order_for_long_copies(tsx):
         assert info["tiles"] < 16 * info["grid"] and info["tile_order"] == 1
     with tsx.Plan("f16", 1024, 8192, box=(64, 64), stages=3, tuning={"tile_order": 2}) as plan:
         assert plan.info("copy")["tile_order"] == 2
+
+
+def test_dynamic_order_copy_in_a_cuda_graph(tsx):
+    """A launch captured into a graph takes the static order (a graph may be
+    replayed on any stream, so no per-stream counter applies); replays copy
+    every element, and direct launches on the capturing stream still use
+    their counter."""
+    rows, cols = 300, 4096
+    ins = _inputs("f32", "copy", rows, cols, "graph")
+    want = oracle.ewise("copy", "f32", *ins)
+    d = to_dev(ins[0], "f32")
+    out = torch.empty_like(d)
+    with tsx.Plan("f32", rows, cols, box=(16, 128), stages=3, tuning={"tile_order": 2}) as plan:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            plan.ewise("copy", d, out=out, stream=s)   # first call: sets up the launch
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.ewise("copy", d, out=out)
+        for _ in range(3):
+            _poison(out)
+            g.replay()
+            torch.cuda.synchronize()
+            compare("copy", "f32", bits_of(out, "f32"), want, "replayed copy")
+        _poison(out)
+        with torch.cuda.stream(s):
+            plan.ewise("copy", d, out=out, stream=s)
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+    compare("copy", "f32", bits_of(out, "f32"), want, "direct copy after the graph")
