@@ -368,6 +368,9 @@ int read_status(tsx_plan* p, bool clear)
 // abort flag and one fp32
 // partial per 16-byte unit of a staged slot; compute warps plus the
 // producer warp.
+// fp32 row sums: stage bytes per SM the CTA count aims at.
+constexpr int64_t kRowsumRingPerSm = 96 * 1024;
+
 int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
 {
     tsx_plan::OpLaunch& L = p->rowsum_ops[op];
@@ -384,20 +387,30 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         if (smem > size_t(p->max_smem))
             return set_error(TSX_ERR_UNSUPPORTED, "the row reduction's stages do not fit in shared memory");
         L.og.smem_bytes = smem;
-        // Compute threads per SM: a 16-bit element is half an fp32 one's
-        // bytes, so 16-bit row sums need about twice the threads per byte.
-        // 16-bit: about 768 per SM, shared by every CTA that fits.  fp32: at
-        // most three CTAs of 192 threads.  Measured on GB300: fp32 fma
-        // [128, 2^20] row sums at 4 stages (12 KB) 6236 GB/s with the four
-        // CTAs that fit, 6884 with three of 192 threads (6 stages: 6757);
-        // bf16 exp [16384, 16384] with 32x256 tiles at 2 stages 5942 with
+        // CTAs and compute threads per SM.  16-bit: about 768 threads per
+        // SM, shared by every CTA that fits (a 16-bit element is half an fp32
+        // one's bytes, so it needs about twice the threads per byte).  fp32:
+        // enough CTAs for about 96 KB of stages per SM, at least three (as
+        // many as fit), of 384 threads in all.  Measured on GB300, [128, 2^20] in 8x128 tiles
+        // at 4 stages: fp32 fma (12 KB stages) 6884 GB/s with three CTAs of
+        // 192 threads against 6236 with every CTA that fits; fp32 copy, exp
+        // and sqrt (4 KB stages) 5775, 4290 and 3647 with six to eight CTAs
+        // of 64 threads against 3451, 3156 and 2471 with three of 192.
+        // bf16 exp [16384, 16384] in 32x256 tiles at 2 stages: 5942 with
         // five CTAs of 128 threads, 5247 with three of 160.
         const int fit0 = int(kSmemPerSm / (smem + kSmemPerCtaReserved));
         const int fit = fit0 < 1 ? 1 : fit0;
         const bool wide = p->g.es == 4;
-        const int ctas = wide && fit > 3 ? 3 : fit;
+        int ctas = fit;
+        if (wide) {
+            const int64_t ring = int64_t(p->g.stages) * int64_t(L.og.stage_bytes);
+            int64_t want = (kRowsumRingPerSm + ring / 2) / ring;
+            want = want < 3 ? 3 : want;
+            ctas = want < fit ? int(want) : fit;
+        }
         L.ctas_per_sm = ctas;   // the cap, before occupancy below
-        int threads = (wide ? 576 : 768) / ctas / 32 * 32;
+        // (fp32 CTAs that do not reach three keep 192 threads each)
+        int threads = (wide ? (ctas >= 3 ? 384 : 192 * ctas) : 768) / ctas / 32 * 32;
         threads = threads < 64 ? 64 : threads > 512 ? 512 : threads;
         const int forced = p->g.knobs.threads;
         if (forced > 0) {

@@ -233,3 +233,20 @@ def test_rowsum_exp_meets_every_16bit_input(tsx, dtype):
         d = oracle.ulp_distance(bits, want, dtype)
         bad = np.flatnonzero(d > oracle.EXP_ULP_BOUND[dtype])
         assert bad.size == 0, f"box {box}: {bad.size} inputs off, first {int(a[bad[0], 0]):#06x}"
+
+
+def test_rowsum_launch_shape(tsx):
+    """fp32 row sums take enough CTAs for about 96 KB of stages per SM (at
+    least three) of 384 threads in all; 16-bit ones about 768 threads per SM
+    over every CTA that fits."""
+    with tsx.Plan("f32", 128, 1 << 20, box=(8, 128), stages=4) as plan:
+        fma = plan.info("fma", row_sums=True)      # 12 KB stages: three CTAs
+        copy = plan.info("copy", row_sums=True)    # 4 KB stages: six
+    assert (fma["ctas_per_sm"], fma["threads"]) == (3, 128)
+    assert (copy["ctas_per_sm"], copy["threads"]) == (6, 64)
+    with tsx.Plan("f32", 128, 1 << 20, box=(8, 256), stages=6) as plan:
+        big = plan.info("fma", row_sums=True)      # 144 KB of stages: the one CTA that fits
+    assert (big["ctas_per_sm"], big["threads"]) == (1, 192)
+    with tsx.Plan("bf16", 16384, 16384, box=(32, 256), stages=2) as plan:
+        h = plan.info("exp", row_sums=True)
+    assert h["ctas_per_sm"] * h["threads"] <= 768 and h["ctas_per_sm"] >= 3
