@@ -19,13 +19,15 @@ SIGN = {"f16": 0x8000, "bf16": 0x8000, "f32": 0x80000000}
 
 
 def decode(bits, dtype: str) -> np.ndarray:
-    """Library decode of element bits to float64 (numpy casts)."""
+    """Library decode of element bits to float64 (numpy casts; signalling
+    NaNs widen quietly)."""
     b = np.asarray(bits)
-    if dtype == "f16":
-        return b.astype(np.uint16).view(np.float16).astype(np.float64)
-    if dtype == "bf16":
-        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
-    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        if dtype == "f16":
+            return b.astype(np.uint16).view(np.float16).astype(np.float64)
+        if dtype == "bf16":
+            return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        return b.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
 def frac_of_bits(bits: int, dtype: str) -> Fraction:
