@@ -118,3 +118,32 @@ def test_pitched_row_sums(tsx, variant, dtype):
         torch.cuda.synchronize()
         assert plan.status() == tsx.TSX_OK
     assert np.array_equal(got, vals.astype(np.float64).sum(axis=1))
+
+
+@pytest.mark.parametrize("variant", ["tma", "tma_rank3"])
+@pytest.mark.parametrize("op,tuning", [("copy", {"tile_order": 2}), ("copy", {"tile_order": 2, "dynamic_share": 30}),
+                                       ("exp", {"store_split": 2}), ("fma", {"store_split": 2})])
+def test_pitched_with_the_tile_order_and_split_knobs(tsx, variant, op, tuning):
+    """The copy's dynamic tile order and the split stores on pitched rows:
+    tile coordinates and box groups address the rows by the pitch."""
+    dtype, rows, cols, pitch, box = "bf16", 70, 128, 192, (32, 128)
+    try:
+        q = tsx.query(dtype, rows, cols, box, 3, variant, op, pitch=pitch, tuning=tuning)
+    except tsx.TsxError:
+        pytest.skip("declined on the host")
+    seed = zlib.crc32(f"pitch-knob/{variant}/{op}/{sorted(tuning.items())}".encode())
+    ins = [random_bits(dtype, (rows, cols), seed + k) for k in range(ARITY[op])]
+    want = oracle.ewise(op, dtype, *ins)
+    views = [_pitched(x, dtype, pitch) for x in ins]
+    obuf, out = _pitched(np.zeros((rows, cols), dtype=ins[0].dtype), dtype, pitch)
+    with tsx.Plan(dtype, rows, cols, box=box, stages=3, variant=variant, pitch=pitch, tuning=tuning) as plan:
+        info = plan.info(op)
+        if "tile_order" in tuning:
+            assert info["tile_order"] == 2
+        if "store_split" in tuning:
+            assert info["compute_groups"] == q["compute_groups"]
+        plan.ewise(op, *[v for _, v in views], out=out)
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+    compare(op, dtype, bits_of(out, dtype), want, f"{variant} {op} {tuning}")
+    assert _padding_intact(obuf, dtype, cols)
