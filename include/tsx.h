@@ -207,14 +207,15 @@ typedef struct tsx_plan_info {
  *                c, c + G, ...), 2 dynamic (a CTA's first tiles as in the
  *                static order, then tiles claimed in order from a counter,
  *                so that CTAs streaming faster take more tiles); <= 0: the
- *                planner's: dynamic for tiles of 16 KB or more in launches
- *                of at least 16 tiles per CTA (the host-only query, which
- *                knows no grid, reports that case).  The other ops, and
- *                TSX_ACCUMULATE, always take the static order
+ *                planner's: dynamic for launches of at least 16 tiles per
+ *                CTA (the host-only query, which knows no grid, reports
+ *                that case).  The other ops, and TSX_ACCUMULATE, always
+ *                take the static order
  *  dynamic_share dynamic order: about this percentage of the tiles (the
  *                last ones) is claimed from the counter, 1..100 (a CTA
  *                takes at least max(1, S - 1) tiles in the static order
- *                first); <= 0: the planner's (100)
+ *                first); <= 0: the planner's (100 for tiles of 16 KB or
+ *                more, 25 for smaller ones)
  *  store_split   TMA variants, ops with a compute step and an even number
  *                of boxes per tile (not the mixed variant's binary ops): 2
  *                stores the first half of a tile's boxes while the compute

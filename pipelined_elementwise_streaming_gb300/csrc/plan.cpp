@@ -372,12 +372,13 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         og->store_lag = ss.store_lag;
         og->lane0_wait = ss.lane0_wait;
         // the dynamic order is built into the copy kernels only (ops with a
-        // compute step measured slower with it on GB300); by default for
-        // tiles of 16 KB or more: with smaller tiles the claims on the one
-        // counter came too fast (fp32 copy in 4 KB tiles: half the speed)
-        const int order = g.slot_bytes >= kDynamicMinTileBytes ? 2 : 1;
-        og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : order) : 1;
-        og->dynamic_share = og->tile_order == 2 ? (g.knobs.dynamic_share > 0 ? g.knobs.dynamic_share : 100) : 0;
+        // compute step measured slower with it on GB300).  Tiles of 16 KB or
+        // more have every tile past the static prefix claimed; smaller ones
+        // the last quarter only (claiming all of them, an fp32 copy in 4 KB
+        // tiles ran at half the speed; the last quarter gained up to 33 %)
+        og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : 2) : 1;
+        const int share = g.slot_bytes >= kDynamicAllTileBytes ? 100 : 25;
+        og->dynamic_share = og->tile_order == 2 ? (g.knobs.dynamic_share > 0 ? g.knobs.dynamic_share : share) : 0;
         // two groups of boxes need a compute step, an even box count and
         // all operands staged
         const int boxes = g.variant == TSX_TMA_RANK3 ? g.row_chunks : g.row_chunks * g.atoms;

@@ -71,6 +71,9 @@ struct OpGeometry {
 // before it claims, so that about dynamic_share percent of the tiles are
 // claimed (at least max(1, S - 1)).
 int64_t static_tiles_per_cta(const Geometry& g, const OpGeometry& og, int64_t grid);
+// Dynamic order: tiles of at least this many bytes have every tile past the
+// static prefix claimed; smaller ones only the last quarter.
+constexpr uint32_t kDynamicAllTileBytes = 16384;
 
 struct TensorMapArgs {
     int rank = 0;

@@ -47,9 +47,6 @@ constexpr int kTileCounterSlots = 64;
 // many tiles per CTA (GB300: copies of 2 to 4 tiles per CTA were 12-14 %
 // slower in it, of 36 or more 10-11 % faster).
 constexpr int kDynamicMinTilesPerCta = 16;
-// ... and tiles of at least this many bytes (an fp32 copy in 4 KB tiles ran
-// at half the speed in it: one counter, 700 claims per microsecond).
-constexpr uint32_t kDynamicMinTileBytes = 16384;
 
 TSX_HD constexpr int elem_size(int dtype) { return dtype == TSX_F32 ? 4 : 2; }
 TSX_HD constexpr int op_arity(int op) { return op == TSX_FMA ? 3 : (op == TSX_ADD || op == TSX_MUL) ? 2 : 1; }

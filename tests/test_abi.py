@@ -313,10 +313,11 @@ def test_query_mixed_prefetch_lead(tsx):
 
 
 def test_query_tile_order(tsx):
-    """TMA copies of tiles of 16 KB or more take tiles in the dynamic order
-    unless told otherwise (the last `dynamic_share` percent claimed from a
-    counter); every other op, and the reduce-store, keep the static order;
-    the ablations and row sums have no tile order."""
+    """TMA copies take tiles in the dynamic order unless told otherwise (the
+    last `dynamic_share` percent claimed from a counter: all past the static
+    prefix for tiles of 16 KB or more, the last quarter for smaller ones);
+    every other op, and the reduce-store, keep the static order; the
+    ablations and row sums have no tile order."""
     q = tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma", "copy")
     assert (q["tile_order"], q["dynamic_share"]) == (2, 100)
     assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma_rank3", "copy")["tile_order"] == 2
@@ -328,8 +329,10 @@ def test_query_tile_order(tsx):
     for op in ("sqrt", "exp", "add", "mul", "fma"):
         q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", op, tuning={"tile_order": 2})
         assert (q["tile_order"], q["dynamic_share"]) == (1, 0), op
-    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy")["tile_order"] == 1      # 4 KB tiles
-    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"tile_order": 2})["tile_order"] == 2
+    q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy")      # 4 KB tiles: the last quarter claimed
+    assert (q["tile_order"], q["dynamic_share"]) == (2, 25)
+    q = tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"dynamic_share": 60})
+    assert (q["tile_order"], q["dynamic_share"]) == (2, 60)
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "ldgsts", "copy")["tile_order"] == 0
     with pytest.raises(tsx.TsxError, match="tile_order"):
         tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "copy", tuning={"tile_order": 3})
