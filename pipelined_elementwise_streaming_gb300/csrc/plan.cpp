@@ -27,6 +27,9 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+// Stage bytes per SM that rings of small exp stages aim at (make_op_geometry).
+constexpr int64_t kSmallRingPerSm = 144 * 1024;
+
 int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {
     (void)op;
@@ -405,6 +408,22 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
                TSX_ERR_UNSUPPORTED;
     if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && two_large_ctas(g, op, og->stage_bytes))
         og->threads = 256;   // the two large CTAs of a two-stage sqrt / exp ring (default_ctas_cap)
+    // Rings of four or more small stages of exp (and of 16-bit sqrt): enough
+    // CTAs for about 144 KB of stages per SM, sharing about 256 compute
+    // threads, one warp at least.  Measured on GB300 over fp32 8x128, 8x256
+    // and 16x128 tiles and bf16 32x128, 64x64 and 16x256 tiles at 4 and 6
+    // stages: +1 to +22 % against every CTA that fits with the usual thread
+    // share.  fp32 sqrt, which needs more threads per byte, lost with it,
+    // and two or three stages were mixed.
+    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && g.variant != TSX_TMA_MIXED &&
+        (op == TSX_EXP || (op == TSX_SQRT && g.es == 2)) && og->stage_bytes < 16384 && g.stages >= 4) {
+        const int64_t ring = int64_t(g.stages) * og->stage_bytes;
+        int64_t want = (kSmallRingPerSm + ring / 2 - 1) / ring;   // halves round down
+        want = want < 1 ? 1 : want;
+        og->ctas_cap = int(want);
+        int threads = int(256 / want) / 32 * 32;
+        og->threads = threads < 32 ? 32 : threads > 256 ? 256 : threads;
+    }
     og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors
     og->vec = 16 / g.es;
