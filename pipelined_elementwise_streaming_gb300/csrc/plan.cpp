@@ -408,21 +408,24 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
                TSX_ERR_UNSUPPORTED;
     if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && two_large_ctas(g, op, og->stage_bytes))
         og->threads = 256;   // the two large CTAs of a two-stage sqrt / exp ring (default_ctas_cap)
-    // Rings of four or more small stages of exp (and of 16-bit sqrt): enough
-    // CTAs for about 144 KB of stages per SM, sharing about 256 compute
-    // threads, one warp at least.  Measured on GB300 over fp32 8x128, 8x256
-    // and 16x128 tiles and bf16 32x128, 64x64 and 16x256 tiles at 4 and 6
-    // stages: +1 to +22 % against every CTA that fits with the usual thread
-    // share.  fp32 sqrt, which needs more threads per byte, lost with it,
-    // and two or three stages were mixed.
+    // Rings of four or more small stages (under 16 KB) of sqrt and exp:
+    // enough CTAs for about 144 KB of stages per SM, sharing about 256
+    // compute threads (one warp at least), or 576 (two warps at least) for
+    // fp32 sqrt, which needs more threads per byte.  Measured on GB300 over
+    // fp32 8x128, 8x256 and 16x128 tiles and bf16 32x128, 64x64 and 16x256
+    // tiles at 4, 6 and 8 stages, against every CTA that fits with the usual
+    // thread share: exp and 16-bit sqrt +1 to +22 %, fp32 sqrt -2 to +31 %;
+    // two or three stages were mixed.
+    const bool sqrt32 = op == TSX_SQRT && g.es == 4;
     if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && g.variant != TSX_TMA_MIXED &&
-        (op == TSX_EXP || (op == TSX_SQRT && g.es == 2)) && og->stage_bytes < 16384 && g.stages >= 4) {
+        (op == TSX_EXP || op == TSX_SQRT) && og->stage_bytes < 16384 && g.stages >= 4) {
         const int64_t ring = int64_t(g.stages) * og->stage_bytes;
         int64_t want = (kSmallRingPerSm + ring / 2 - 1) / ring;   // halves round down
         want = want < 1 ? 1 : want;
         og->ctas_cap = int(want);
-        int threads = int(256 / want) / 32 * 32;
-        og->threads = threads < 32 ? 32 : threads > 256 ? 256 : threads;
+        const int least = sqrt32 ? 64 : 32;
+        int threads = int((sqrt32 ? 576 : 256) / want) / 32 * 32;
+        og->threads = threads < least ? least : threads > 512 ? 512 : threads;
     }
     og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors

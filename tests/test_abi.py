@@ -363,12 +363,13 @@ def test_query_store_split(tsx):
 
 
 def test_query_small_exp_rings(tsx):
-    """Rings of four or more small exp stages (and 16-bit sqrt) take about
-    256 compute threads per SM over enough CTAs for about 144 KB of stages;
-    fp32 sqrt and shorter rings keep the usual share."""
+    """Rings of four or more small sqrt / exp stages take about 256 compute
+    threads per SM (576 for fp32 sqrt) over enough CTAs for about 144 KB of
+    stages; shorter rings keep the usual share."""
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "exp")["threads"] == 32    # 9 CTAs of 16 KB
     assert tsx.query("f32", 128, 1 << 20, (8, 256), 4, "tma", "exp")["threads"] == 64    # 4 CTAs of 32 KB
     assert tsx.query("bf16", 16384, 16384, (64, 64), 6, "tma", "sqrt")["threads"] == 64  # 3 CTAs of 48 KB
-    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "sqrt")["threads"] == 64   # the usual share
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "sqrt")["threads"] == 64   # 9 CTAs, 576 threads
+    assert tsx.query("f32", 128, 1 << 20, (16, 128), 8, "tma", "sqrt")["threads"] == 288  # 2 CTAs of 64 KB
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 3, "tma", "exp")["threads"] == 64    # three stages
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "exp", tuning={"threads": 128})["threads"] == 128
