@@ -27,8 +27,10 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-// Stage bytes per SM that rings of small exp stages aim at (make_op_geometry).
+// Stage bytes per SM that rings of small sqrt / exp stages, and of add / mul
+// stages on long streams, aim at (make_op_geometry).
 constexpr int64_t kSmallRingPerSm = 144 * 1024;
+constexpr int64_t kLongStreamTiles = 32768;
 
 int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {
@@ -426,6 +428,20 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         const int least = sqrt32 ? 64 : 32;
         int threads = int((sqrt32 ? 576 : 256) / want) / 32 * 32;
         og->threads = threads < least ? least : threads > 512 ? 512 : threads;
+    }
+    // The same target for add and mul on long streams (at least 32768 tiles)
+    // from three stages on, where it leaves two CTAs per SM or more:
+    // measured on GB300 over fp32 8x128 and 8x64 tiles and bf16 64x64 and
+    // 32x128 tiles, +0 to +12 % (two stages, and a single CTA, lost 1-9 %).
+    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && g.variant != TSX_TMA_MIXED &&
+        (op == TSX_ADD || op == TSX_MUL) && g.stages >= 3 && g.tiles >= kLongStreamTiles) {
+        const int64_t ring = int64_t(g.stages) * og->stage_bytes;
+        const int64_t want = (kSmallRingPerSm + ring / 2 - 1) / ring;
+        if (want >= 2) {
+            og->ctas_cap = int(want);
+            const int threads = int(256 / want) / 32 * 32;
+            og->threads = threads < 32 ? 32 : threads;
+        }
     }
     og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);
     // [outer, threads, vec] of the elementwise stage: 16-byte vectors

@@ -373,3 +373,16 @@ def test_query_small_exp_rings(tsx):
     assert tsx.query("f32", 128, 1 << 20, (16, 128), 8, "tma", "sqrt")["threads"] == 288  # 2 CTAs of 64 KB
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 3, "tma", "exp")["threads"] == 64    # three stages
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "exp", tuning={"threads": 128})["threads"] == 128
+
+
+def test_query_add_mul_rings(tsx):
+    """add and mul on long streams from three stages on take enough CTAs for
+    about 144 KB of stages per SM when that leaves two or more; short
+    streams (the stated fp16 add workload), two stages and single-CTA rings
+    keep the usual share."""
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "add")["threads"] == 64     # 4 CTAs of 32 KB
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 3, "tma", "mul")["threads"] == 32     # 6 CTAs of 24 KB
+    assert tsx.query("bf16", 16384, 16384, (64, 64), 4, "tma", "add")["threads"] == 128   # 2 CTAs of 64 KB
+    assert tsx.query("bf16", 16384, 16384, (64, 64), 6, "tma", "add")["threads"] == 128   # the usual share: 1 CTA would be the target
+    assert tsx.query("f16", 1024, 8192, (64, 64), 3, "tma", "add")["threads"] == 64        # 2048 tiles
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 2, "tma", "add")["threads"] == 64     # two stages
