@@ -31,6 +31,8 @@ uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // stages on long streams, aim at (make_op_geometry).
 constexpr int64_t kSmallRingPerSm = 144 * 1024;
 constexpr int64_t kLongStreamTiles = 32768;
+// Staged bytes per SM that the mixed variant's add and mul aim at.
+constexpr int64_t kMixedRingPerSm = 96 * 1024;
 
 int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {
@@ -441,6 +443,27 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
             og->ctas_cap = int(want);
             const int threads = int(256 / want) / 32 * 32;
             og->threads = threads < 32 ? 32 : threads;
+        }
+    }
+    // The mixed variant: as few compute threads as hold b a tile ahead
+    // (kSetUnits 16-byte units each), so that registers leave room for more
+    // CTAs; fma (two operands staged) keeps every CTA that fits, add and mul
+    // (a alone staged) aim at about 96 KB of stages per SM.  Measured on
+    // GB300 against the thread share above over fp32 8x64, 8x128, 8x256 and
+    // 16x128 tiles and bf16 32x64, 32x128, 64x64, 64x128 and 128x128 tiles at
+    // 2 to 8 stages: +0 to +49 % (fp32 fma 8x128 at 6 stages 5959 -> 6943
+    // GB/s, at 8 stages 4433 -> 6624; bf16 add 64x64 at 6 stages 6005 ->
+    // 6679), never below the share by more than the noise.
+    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && g.variant == TSX_TMA_MIXED && og->n_in >= 2) {
+        const int cover = int((g.slot_bytes / 16 + kSetUnits - 1) / kSetUnits + 31) / 32 * 32;
+        const int most = kMixedMaxThreads - 32 * tma_role_warps(og->store_warps);
+        og->threads = cover < most ? cover : most;
+        if (og->n_in == 2) {
+            const int64_t ring = int64_t(g.stages) * og->stage_bytes;
+            const int64_t want = (kMixedRingPerSm + ring / 2 - 1) / ring;   // halves round down
+            og->ctas_cap = int(want < 1 ? 1 : want);
+        } else {
+            og->ctas_cap = 0;
         }
     }
     og->block_threads = og->threads + (tma ? 32 * tma_role_warps(og->store_warps) : 0);

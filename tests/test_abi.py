@@ -375,6 +375,18 @@ def test_query_small_exp_rings(tsx):
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "exp", tuning={"threads": 128})["threads"] == 128
 
 
+def test_query_mixed_threads(tsx):
+    """The mixed variant's add, mul and fma take as few compute threads as
+    hold b a tile ahead (four 16-byte units each); given knobs win."""
+    for S in (2, 4, 6, 8):
+        assert tsx.query("f32", 128, 1 << 20, (8, 128), S, "tma_mixed", "fma")["threads"] == 64   # 256 units
+    assert tsx.query("f32", 128, 1 << 20, (8, 64), 4, "tma_mixed", "fma")["threads"] == 32
+    assert tsx.query("f32", 128, 1 << 20, (16, 128), 4, "tma_mixed", "add")["threads"] == 128
+    assert tsx.query("bf16", 16384, 16384, (64, 128), 4, "tma_mixed", "mul")["threads"] == 256
+    assert tsx.query("bf16", 16384, 16384, (128, 128), 3, "tma_mixed", "mul")["threads"] == 512
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 6, "tma_mixed", "fma", tuning={"threads": 128})["threads"] == 128
+
+
 def test_query_add_mul_rings(tsx):
     """add and mul on long streams from three stages on take enough CTAs for
     about 144 KB of stages per SM when that leaves two or more; short

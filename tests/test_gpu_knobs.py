@@ -90,3 +90,22 @@ def test_store_lag_follows_the_schedule_model(tsx, lag, stages):
         trace = plan.trace()
     compare("add", "f32", bits_of(out, "f32"), oracle.ewise("add", "f32", a, b), "traced add")
     _check_all(trace, tiles, stages, min(lag, stages - 1), "add", 1, 1, 0)
+
+
+@pytest.mark.parametrize("dtype,rows,cols,box,stages,op,shape", [
+    ("f32", 128, 1 << 20, (8, 128), 4, "fma", (5, 64)),     # every CTA the registers leave
+    ("f32", 128, 1 << 20, (8, 128), 6, "fma", (4, 64)),     # every CTA shared memory leaves
+    ("f32", 128, 1 << 20, (8, 128), 8, "fma", (3, 64)),
+    ("f32", 128, 1 << 20, (8, 128), 6, "add", (4, 64)),     # 96 KB of 24 KB rings
+    ("bf16", 16384, 16384, (64, 64), 6, "add", (2, 128)),   # 96 KB of 48 KB rings
+    ("bf16", 16384, 16384, (64, 128), 4, "mul", (1, 256)),  # 1.5 rounds down
+])
+def test_mixed_variant_launch_shape(tsx, dtype, rows, cols, box, stages, op, shape):
+    """The mixed variant's default launch: compute threads that just hold b a
+    tile ahead; fma keeps every CTA that fits, add and mul enough for about
+    96 KB of stages per SM.  The same defaults on a ragged shape match the
+    oracle."""
+    with tsx.Plan(dtype, rows, cols, box=box, stages=stages, variant="tma_mixed") as plan:
+        info = plan.info(op)
+    assert (info["ctas_per_sm"], info["threads"]) == shape
+    _run(tsx, dtype, op, 3 * box[0] + 5, 7 * box[1] + 8, box, stages, "tma_mixed")
