@@ -33,6 +33,9 @@ constexpr int64_t kSmallRingPerSm = 144 * 1024;
 constexpr int64_t kLongStreamTiles = 32768;
 // Staged bytes per SM that the mixed variant's add and mul aim at.
 constexpr int64_t kMixedRingPerSm = 96 * 1024;
+// Two-stage rings on streams of at least this many tiles take the targets
+// of two_stage_ring_per_sm.
+constexpr int64_t kTwoStageStreamTiles = 16384;
 
 int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {
@@ -43,7 +46,8 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
     // and store warps); the mixed variant, whose compute threads also load
     // b one tile ahead for at most kSetUnits of the slot's `units` 16-byte
     // vectors each, aims at about 512 per SM, rounded to the nearest warp,
-    // and at least enough threads to cover the slot that way.
+    // and at least enough threads to cover the slot that way.  Rules of
+    // make_op_geometry replace these shares where no knob is given.
     // The cp.async / synchronous ablations give each thread about four
     // 16-byte units of the slot, between 128 threads (the TVM ldgsts
     // demonstration program's count, which its 128x32 fp16 tile gets) and
@@ -75,9 +79,13 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
 // and reach a stage from one operand only).
 static bool one_operand_compute(int op) { return op == TSX_SQRT || op == TSX_EXP; }
 
-static bool two_large_ctas(const Geometry& g, int op, uint32_t stage_bytes)
+// Stage bytes per SM that a two-stage ring aims at: copy, add and mul 96 KB,
+// the one-operand sqrt and exp 128 KB, fma 144 KB (make_op_geometry).
+static int64_t two_stage_ring_per_sm(int op)
 {
-    return is_tma_variant(g.variant) && g.stages == 2 && one_operand_compute(op) && stage_bytes >= 16384;
+    if (op == TSX_FMA)
+        return 144 * 1024;
+    return one_operand_compute(op) ? 128 * 1024 : 96 * 1024;
 }
 
 int mixed_prefetch_ahead(const Geometry& g, int ctas_per_sm)
@@ -98,19 +106,6 @@ int mixed_prefetch_ahead(const Geometry& g, int ctas_per_sm)
     lead = lead < 1 ? 1 : lead;
     const int64_t ahead = lead - (g.stages - 2);
     return ahead < 0 ? 0 : ahead > 8 ? 8 : int(ahead);
-}
-
-int default_ctas_cap(const Geometry& g, int op, uint32_t stage_bytes)
-{
-    // A two-stage ring of large one-operand tiles streams best from two CTAs
-    // per SM of 256 compute threads: bf16 exp [16384, 16384] with 128x128
-    // tiles (32 KB stages) 6467 GB/s against 5760 with the three CTAs that
-    // fit, and bf16 sqrt 6282 against 5683 (GB300; at one CTA 4352 / 4222).
-    // Smaller stages and other ops keep every CTA that fits (fp32 fma with
-    // 12 KB stages: 7177 GB/s at six CTAs, 4520 at two).
-    if (g.knobs.ctas_per_sm > 0)
-        return g.knobs.ctas_per_sm;
-    return two_large_ctas(g, op, stage_bytes) ? 2 : 0;
 }
 
 StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes)
@@ -397,7 +392,8 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         const bool split = g.knobs.store_split == 2 || (g.knobs.store_split == 0 && split_pays);
         og->compute_groups = can_split && split ? 2 : 1;
     }
-    og->ctas_cap = default_ctas_cap(g, op, og->stage_bytes);
+    // every CTA that fits, unless forced or capped by a rule below
+    og->ctas_cap = g.knobs.ctas_per_sm > 0 ? g.knobs.ctas_per_sm : 0;
     // the mixed variant's L2 prefetch of b, for the CTAs that shared memory
     // alone would fit (the launch recomputes it for the resident CTAs)
     if (g.variant == TSX_TMA_MIXED && og->n_in >= 2) {
@@ -410,8 +406,26 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         return fail(why, "the mixed variant runs at most %lld threads per CTA (%lld asked)", kMixedMaxThreads,
                     og->threads + 32 * tma_role_warps(og->store_warps)),
                TSX_ERR_UNSUPPORTED;
-    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && two_large_ctas(g, op, og->stage_bytes))
-        og->threads = 256;   // the two large CTAs of a two-stage sqrt / exp ring (default_ctas_cap)
+    const bool tma_rules = tma && g.variant != TSX_TMA_MIXED && g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0;
+    // Two-stage rings on long streams: enough CTAs for the op's target of
+    // stage bytes per SM (halves round up), sharing 512 compute threads per
+    // SM (256 for copy).  One stage loads while the other is computed and
+    // stored, so the CTAs that fit hold too much or too little in flight.
+    // Measured on GB300 over fp32 8x128, 8x256 and 16x128 tiles and bf16
+    // 128x128, 64x128, 32x128 and 64x64 tiles of every op, against every
+    // CTA that fits with the usual thread share: +0 to +41 % (bf16 exp in
+    // 64x128 tiles 4483 -> 6343 GB/s, fp32 add in 16x128 tiles 5248 -> 6730,
+    // fp32 add in 8x128 tiles 6303 -> 6870), nowhere lower by more than the
+    // noise.  bf16 exp [16384, 16384] in 128x128 tiles keeps its two CTAs of
+    // 256 threads (6467 GB/s against 5760 with the three that fit).
+    if (tma_rules && g.stages == 2 && g.tiles >= kTwoStageStreamTiles) {
+        const int64_t ring = 2 * int64_t(og->stage_bytes);
+        int64_t want = (two_stage_ring_per_sm(op) + ring / 2) / ring;   // halves round up
+        want = want < 1 ? 1 : want;
+        og->ctas_cap = int(want);
+        const int threads = int((op == TSX_COPY ? 256 : 512) / want) / 32 * 32;
+        og->threads = threads < 32 ? 32 : threads;
+    }
     // Rings of four or more small stages (under 16 KB) of sqrt and exp:
     // enough CTAs for about 144 KB of stages per SM, sharing about 256
     // compute threads (one warp at least), or 576 (two warps at least) for
@@ -421,8 +435,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     // thread share: exp and 16-bit sqrt +1 to +22 %, fp32 sqrt -2 to +31 %;
     // two or three stages were mixed.
     const bool sqrt32 = op == TSX_SQRT && g.es == 4;
-    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && g.variant != TSX_TMA_MIXED &&
-        (op == TSX_EXP || op == TSX_SQRT) && og->stage_bytes < 16384 && g.stages >= 4) {
+    if (tma_rules && (op == TSX_EXP || op == TSX_SQRT) && og->stage_bytes < 16384 && g.stages >= 4) {
         const int64_t ring = int64_t(g.stages) * og->stage_bytes;
         int64_t want = (kSmallRingPerSm + ring / 2 - 1) / ring;   // halves round down
         want = want < 1 ? 1 : want;
@@ -435,8 +448,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     // from three stages on, where it leaves two CTAs per SM or more:
     // measured on GB300 over fp32 8x128 and 8x64 tiles and bf16 64x64 and
     // 32x128 tiles, +0 to +12 % (two stages, and a single CTA, lost 1-9 %).
-    if (g.knobs.threads <= 0 && g.knobs.ctas_per_sm <= 0 && g.variant != TSX_TMA_MIXED &&
-        (op == TSX_ADD || op == TSX_MUL) && g.stages >= 3 && g.tiles >= kLongStreamTiles) {
+    if (tma_rules && (op == TSX_ADD || op == TSX_MUL) && g.stages >= 3 && g.tiles >= kLongStreamTiles) {
         const int64_t ring = int64_t(g.stages) * og->stage_bytes;
         const int64_t want = (kSmallRingPerSm + ring / 2 - 1) / ring;
         if (want >= 2) {

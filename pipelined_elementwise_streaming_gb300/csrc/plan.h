@@ -92,9 +92,6 @@ struct StoreSchedule {
     bool lane0_wait;
 };
 StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes);
-// At most this many CTAs per SM for `op` (0: as occupancy allows), unless
-// the knobs say otherwise.
-int default_ctas_cap(const Geometry& g, int op, uint32_t stage_bytes);
 // Mixed variant: how many of a CTA's tiles beyond the tile it loads the
 // producer prefetches b into L2, for ctas_per_sm resident CTAs.
 int mixed_prefetch_ahead(const Geometry& g, int ctas_per_sm);

@@ -272,15 +272,28 @@ def test_query_store_schedule(tsx, op, stages, box, want):
     assert (f["store_warps"], f["store_lag"], f["role_wait"]) == (1, 1, 1)
 
 
-def test_query_two_stage_large_tiles_take_256_threads(tsx):
-    """A two-stage ring of 32 KB sqrt / exp tiles runs as at most two CTAs
-    per SM of 256 compute threads (the CTA cap shows in a plan's launch on a
-    GPU); other ops, smaller stages and forced knobs keep the usual share."""
-    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "exp")["threads"] == 256
-    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "sqrt")["threads"] == 256
-    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "copy")["threads"] == 64
-    assert tsx.query("bf16", 16384, 16384, (64, 64), 2, "tma", "exp")["threads"] == 64
-    assert tsx.query("bf16", 16384, 16384, (128, 128), 2, "tma", "exp", tuning={"ctas_per_sm": 3})["threads"] == 64
+def test_query_two_stage_rings(tsx):
+    """Two-stage rings on streams of 16384 tiles or more share 512 compute
+    threads per SM (256 for copy) among enough CTAs for about 96 KB of
+    stages per SM (copy, add, mul), 128 KB (sqrt, exp) or 144 KB (fma),
+    halves rounding up; the CTA cap shows in a plan's launch on a GPU.
+    Short streams, other variants and forced knobs keep the usual share."""
+    big = ("bf16", 16384, 16384)
+    assert tsx.query(*big, (128, 128), 2, "tma", "exp")["threads"] == 256    # 2 CTAs of 64 KB
+    assert tsx.query(*big, (128, 128), 2, "tma", "sqrt")["threads"] == 256
+    assert tsx.query(*big, (64, 128), 2, "tma", "exp")["threads"] == 128     # 4 CTAs of 32 KB
+    assert tsx.query(*big, (128, 128), 2, "tma", "copy")["threads"] == 128   # 1.5 rounds up to 2
+    assert tsx.query(*big, (128, 128), 2, "tma", "mul")["threads"] == 512    # one CTA of 128 KB
+    assert tsx.query(*big, (32, 128), 2, "tma", "add")["threads"] == 160     # 3 CTAs of 32 KB
+    assert tsx.query(*big, (32, 128), 2, "tma", "fma")["threads"] == 160     # 3 CTAs of 48 KB
+    assert tsx.query(*big, (64, 64), 2, "tma_rank3", "add")["threads"] == 160
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 2, "tma", "copy")["threads"] == 32   # 12 CTAs wanted
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 2, "tma", "fma")["threads"] == 64    # 6 CTAs of 24 KB
+    assert tsx.query("f16", 1024, 8192, (64, 64), 2, "tma", "add")["threads"] == 64       # 2048 tiles
+    assert tsx.query("f32", 500, 4096, (32, 32), 2, "tma", "sqrt")["threads"] == 64       # 2048 tiles
+    assert tsx.query(*big, (128, 128), 2, "ldgsts", "exp")["threads"] == 512
+    assert tsx.query(*big, (128, 128), 2, "tma", "exp", tuning={"ctas_per_sm": 3})["threads"] == 64
+    assert tsx.query(*big, (128, 128), 3, "tma", "exp")["threads"] == 128    # three stages
 
 
 @pytest.mark.parametrize("op,stages,want", [
@@ -390,11 +403,11 @@ def test_query_mixed_threads(tsx):
 def test_query_add_mul_rings(tsx):
     """add and mul on long streams from three stages on take enough CTAs for
     about 144 KB of stages per SM when that leaves two or more; short
-    streams (the stated fp16 add workload), two stages and single-CTA rings
-    keep the usual share."""
+    streams (the stated fp16 add workload) and single-CTA rings keep the
+    usual share, and two-stage rings have a rule of their own."""
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 4, "tma", "add")["threads"] == 64     # 4 CTAs of 32 KB
     assert tsx.query("f32", 128, 1 << 20, (8, 128), 3, "tma", "mul")["threads"] == 32     # 6 CTAs of 24 KB
     assert tsx.query("bf16", 16384, 16384, (64, 64), 4, "tma", "add")["threads"] == 128   # 2 CTAs of 64 KB
     assert tsx.query("bf16", 16384, 16384, (64, 64), 6, "tma", "add")["threads"] == 128   # the usual share: 1 CTA would be the target
     assert tsx.query("f16", 1024, 8192, (64, 64), 3, "tma", "add")["threads"] == 64        # 2048 tiles
-    assert tsx.query("f32", 128, 1 << 20, (8, 128), 2, "tma", "add")["threads"] == 64     # two stages
+    assert tsx.query("f32", 128, 1 << 20, (8, 128), 2, "tma", "add")["threads"] == 64     # two stages: their own rule

@@ -109,3 +109,23 @@ def test_mixed_variant_launch_shape(tsx, dtype, rows, cols, box, stages, op, sha
         info = plan.info(op)
     assert (info["ctas_per_sm"], info["threads"]) == shape
     _run(tsx, dtype, op, 3 * box[0] + 5, 7 * box[1] + 8, box, stages, "tma_mixed")
+
+
+@pytest.mark.parametrize("dtype,rows,cols,box,op,shape", [
+    ("bf16", 16384, 16384, (128, 128), "exp", (2, 256)),   # 128 KB of 64 KB rings
+    ("bf16", 16384, 16384, (64, 128), "exp", (4, 128)),    # 128 KB of 32 KB rings
+    ("bf16", 16384, 16384, (128, 128), "copy", (2, 128)),  # 96 KB of 64 KB rings: 1.5 rounds up
+    ("bf16", 16384, 16384, (32, 128), "add", (3, 160)),    # 96 KB of 32 KB rings
+    ("f32", 128, 1 << 20, (8, 128), "fma", (6, 64)),       # 144 KB of 24 KB rings
+    ("f32", 128, 1 << 20, (8, 128), "add", (6, 64)),       # 96 KB of 16 KB rings
+])
+def test_two_stage_ring_launch_shape(tsx, dtype, rows, cols, box, op, shape):
+    """Two-stage rings on long streams: CTAs for the op's target of stage
+    bytes per SM, sharing 512 compute threads (256 for copy).  The same
+    launch shape on a ragged shape (too few tiles for the rule, so given as
+    knobs) matches the oracle."""
+    with tsx.Plan(dtype, rows, cols, box=box, stages=2) as plan:
+        info = plan.info(op)
+    assert (info["ctas_per_sm"], info["threads"]) == shape
+    _run(tsx, dtype, op, 3 * box[0] + 5, 7 * box[1] + 8, box, 2,
+         tuning={"ctas_per_sm": shape[0], "threads": shape[1]})
