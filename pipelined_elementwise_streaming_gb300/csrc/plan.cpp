@@ -35,7 +35,7 @@ constexpr int64_t kLongStreamTiles = 32768;
 constexpr int64_t kMixedRingPerSm = 96 * 1024;
 // Two-stage rings on streams of at least this many tiles take the targets
 // of two_stage_ring_per_sm.
-constexpr int64_t kTwoStageStreamTiles = 16384;
+constexpr int64_t kTwoStageStreamTiles = 8192;
 
 int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units, int store_warps)
 {

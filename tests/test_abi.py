@@ -273,7 +273,7 @@ def test_query_store_schedule(tsx, op, stages, box, want):
 
 
 def test_query_two_stage_rings(tsx):
-    """Two-stage rings on streams of 16384 tiles or more share 512 compute
+    """Two-stage rings on streams of 8192 tiles or more share 512 compute
     threads per SM (256 for copy) among enough CTAs for about 96 KB of
     stages per SM (copy, add, mul), 128 KB (sqrt, exp) or 144 KB (fma),
     halves rounding up; the CTA cap shows in a plan's launch on a GPU.
@@ -294,6 +294,7 @@ def test_query_two_stage_rings(tsx):
     assert tsx.query(*big, (128, 128), 2, "ldgsts", "exp")["threads"] == 512
     assert tsx.query(*big, (128, 128), 2, "tma", "exp", tuning={"ctas_per_sm": 3})["threads"] == 64
     assert tsx.query(*big, (128, 128), 3, "tma", "exp")["threads"] == 128    # three stages
+    assert tsx.query(*big, (64, 512), 2, "tma_promoted", "exp")["threads"] == 512   # 8192 tiles, one CTA
 
 
 @pytest.mark.parametrize("op,stages,want", [
