@@ -417,7 +417,8 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     // 64x128 tiles 4483 -> 6343 GB/s, fp32 add in 16x128 tiles 5248 -> 6730,
     // fp32 add in 8x128 tiles 6303 -> 6870), nowhere lower by more than the
     // noise.  bf16 exp [16384, 16384] in 128x128 tiles keeps its two CTAs of
-    // 256 threads (6467 GB/s against 5760 with the three that fit).
+    // 256 threads (6467 GB/s against 5760 with the three that fit).  Short
+    // streams (a few tiles per CTA, bound by latency) keep the usual share.
     if (tma_rules && g.stages == 2 && g.tiles >= kTwoStageStreamTiles) {
         const int64_t ring = 2 * int64_t(og->stage_bytes);
         int64_t want = (two_stage_ring_per_sm(op) + ring / 2) / ring;   // halves round up
@@ -433,7 +434,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     // fp32 8x128, 8x256 and 16x128 tiles and bf16 32x128, 64x64 and 16x256
     // tiles at 4, 6 and 8 stages, against every CTA that fits with the usual
     // thread share: exp and 16-bit sqrt +1 to +22 %, fp32 sqrt -2 to +31 %;
-    // two or three stages were mixed.
+    // three stages were mixed (two have the rule above).
     const bool sqrt32 = op == TSX_SQRT && g.es == 4;
     if (tma_rules && (op == TSX_EXP || op == TSX_SQRT) && og->stage_bytes < 16384 && g.stages >= 4) {
         const int64_t ring = int64_t(g.stages) * og->stage_bytes;
@@ -447,7 +448,8 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
     // The same target for add and mul on long streams (at least 32768 tiles)
     // from three stages on, where it leaves two CTAs per SM or more:
     // measured on GB300 over fp32 8x128 and 8x64 tiles and bf16 64x64 and
-    // 32x128 tiles, +0 to +12 % (two stages, and a single CTA, lost 1-9 %).
+    // 32x128 tiles, +0 to +12 % (a single CTA lost 1-9 %; two stages have
+    // the rule above).
     if (tma_rules && (op == TSX_ADD || op == TSX_MUL) && g.stages >= 3 && g.tiles >= kLongStreamTiles) {
         const int64_t ring = int64_t(g.stages) * og->stage_bytes;
         const int64_t want = (kSmallRingPerSm + ring / 2 - 1) / ring;
