@@ -368,8 +368,13 @@ int read_status(tsx_plan* p, bool clear)
 // abort flag and one fp32
 // partial per 16-byte unit of a staged slot; compute warps plus the
 // producer warp.
-// fp32 row sums: stage bytes per SM the CTA count aims at.
-constexpr int64_t kRowsumRingPerSm = 96 * 1024;
+// fp32 row sums: stage bytes per SM the CTA count aims at (the
+// compute-heavy sqrt and exp, the other ops).
+constexpr int64_t kRowsumRingPerSmHeavy = 96 * 1024;
+constexpr int64_t kRowsumRingPerSm = 128 * 1024;
+// and at most this many CTAs per SM (eight CTAs of 64 threads ran fp32 copy
+// row sums in 4 KB tiles at 4298 GB/s against 5666 with six)
+constexpr int64_t kRowsumMaxCtas = 6;
 
 int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
 {
@@ -390,22 +395,27 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
         // CTAs and compute threads per SM.  16-bit: about 768 threads per
         // SM, shared by every CTA that fits (a 16-bit element is half an fp32
         // one's bytes, so it needs about twice the threads per byte).  fp32:
-        // enough CTAs for about 96 KB of stages per SM, at least three (as
-        // many as fit), of 384 threads in all.  Measured on GB300, [128, 2^20] in 8x128 tiles
-        // at 4 stages: fp32 fma (12 KB stages) 6884 GB/s with three CTAs of
-        // 192 threads against 6236 with every CTA that fits; fp32 copy, exp
-        // and sqrt (4 KB stages) 5775, 4290 and 3647 with six to eight CTAs
-        // of 64 threads against 3451, 3156 and 2471 with three of 192.
-        // bf16 exp [16384, 16384] in 32x256 tiles at 2 stages: 5942 with
-        // five CTAs of 128 threads, 5247 with three of 160.
+        // enough CTAs for about 128 KB of stages per SM (96 KB for sqrt and
+        // exp, which are bound by their arithmetic), at least three (as many
+        // as fit) and at most six, of 384 threads in all.  Measured on GB300, [128, 2^20] in
+        // 8x128 tiles at 4 stages: fp32 fma (12 KB stages) 6884 GB/s with
+        // three CTAs of 192 threads against 6236 with every CTA that fits;
+        // fp32 copy, exp and sqrt (4 KB stages) 5775, 4290 and 3647 with six
+        // to eight CTAs of 64 threads against 3451, 3156 and 2471 with three
+        // of 192.  The 128 KB target against 96 KB: fp32 add in 8x128 tiles
+        // at 4 stages 5765 -> 6488, copy in 8x256 tiles 5350 -> 5981, fma at
+        // 2 and 3 stages +2.6 %.  bf16 exp [16384, 16384] in 32x256 tiles at
+        // 2 stages: 5942 with five CTAs of 128 threads, 5247 with three of
+        // 160.
         const int fit0 = int(kSmemPerSm / (smem + kSmemPerCtaReserved));
         const int fit = fit0 < 1 ? 1 : fit0;
         const bool wide = p->g.es == 4;
         int ctas = fit;
         if (wide) {
             const int64_t ring = int64_t(p->g.stages) * int64_t(L.og.stage_bytes);
-            int64_t want = (kRowsumRingPerSm + ring / 2) / ring;
-            want = want < 3 ? 3 : want;
+            const int64_t target = op == TSX_SQRT || op == TSX_EXP ? kRowsumRingPerSmHeavy : kRowsumRingPerSm;
+            int64_t want = (target + ring / 2) / ring;
+            want = want < 3 ? 3 : want > kRowsumMaxCtas ? kRowsumMaxCtas : want;
             ctas = want < fit ? int(want) : fit;
         }
         L.ctas_per_sm = ctas;   // the cap, before occupancy below

@@ -236,14 +236,18 @@ def test_rowsum_exp_meets_every_16bit_input(tsx, dtype):
 
 
 def test_rowsum_launch_shape(tsx):
-    """fp32 row sums take enough CTAs for about 96 KB of stages per SM (at
-    least three) of 384 threads in all; 16-bit ones about 768 threads per SM
-    over every CTA that fits."""
+    """fp32 row sums take enough CTAs for about 128 KB of stages per SM (96
+    KB for sqrt and exp; three to six) of 384 threads in all; 16-bit ones
+    about 768 threads per SM over every CTA that fits."""
     with tsx.Plan("f32", 128, 1 << 20, box=(8, 128), stages=4) as plan:
         fma = plan.info("fma", row_sums=True)      # 12 KB stages: three CTAs
-        copy = plan.info("copy", row_sums=True)    # 4 KB stages: six
+        add = plan.info("add", row_sums=True)      # 8 KB stages: four
+        copy = plan.info("copy", row_sums=True)    # 4 KB stages: eight wanted, six at most
+        exp = plan.info("exp", row_sums=True)      # 4 KB stages, 96 KB: six
     assert (fma["ctas_per_sm"], fma["threads"]) == (3, 128)
+    assert (add["ctas_per_sm"], add["threads"]) == (4, 96)
     assert (copy["ctas_per_sm"], copy["threads"]) == (6, 64)
+    assert (exp["ctas_per_sm"], exp["threads"]) == (6, 64)
     with tsx.Plan("f32", 128, 1 << 20, box=(8, 256), stages=6) as plan:
         big = plan.info("fma", row_sums=True)      # 144 KB of stages: the one CTA that fits
     assert (big["ctas_per_sm"], big["threads"]) == (1, 192)
