@@ -186,8 +186,13 @@ typedef struct tsx_plan_info {
  *                multiple of 32; <= 0: the planner's choice
  *  ctas_per_sm   at most this many resident CTAs per SM in the persistent
  *                grid; <= 0: the planner's (as many as occupancy allows,
- *                but two, of 256 compute threads, for a two-stage ring of
- *                sqrt or exp stages of 16 KB or more)
+ *                unless a rule measured on GB300 aims at a number of
+ *                stage bytes per SM: two-stage rings on long streams,
+ *                rings of four or more small sqrt / exp stages, add and
+ *                mul on long streams, the mixed variant's add and mul,
+ *                fp32 row sums; tsx_plan_get_info reports the launch's
+ *                count).  Setting threads or ctas_per_sm turns those rules
+ *                off
  *  store_lag     TMA variants: 0..3 of a store warp's tiles between a
  *                store's issue and the release of its stage; < 0: the
  *                planner's
