@@ -191,8 +191,9 @@ typedef struct tsx_plan_info {
  *                rings of four or more small sqrt / exp stages, add and
  *                mul on long streams, the mixed variant's add and mul,
  *                fp32 row sums; tsx_plan_get_info reports the launch's
- *                count).  Setting threads or ctas_per_sm turns those rules
- *                off
+ *                count).  For tsx_ewise, setting threads or ctas_per_sm
+ *                turns those rules off; for row sums each knob replaces its
+ *                own half of the rule
  *  store_lag     TMA variants: 0..3 of a store warp's tiles between a
  *                store's issue and the release of its stage; < 0: the
  *                planner's
