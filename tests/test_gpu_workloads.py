@@ -64,3 +64,45 @@ def test_workload_full_compare_at_full_size(tsx, name):
         bad, first = oracle.count_mismatches(w.op, w.dtype, bits_of(out, w.dtype), want)
         assert bad == 0, f"{name} S={stages}: {bad} of {w.elems} elements differ, first at {first}"
         del out
+
+
+_INPUTS = {}
+
+
+def _full_inputs(w):
+    """The workload's input tensors (seeded per tensor index, so an op of
+    arity n takes the first n), generated once per module."""
+    have = _INPUTS.get(w.name, [])
+    if len(have) < w.n_in:
+        have = w.inputs()
+        _INPUTS[w.name] = have
+    return have[: w.n_in]
+
+
+@pytest.mark.parametrize("name,op,box,stages,variant", [
+    ("exp_16384x16384_bf16", "exp", (64, 128), 2, "tma"),        # two-stage ring: 4 CTAs of 128 threads
+    ("exp_16384x16384_bf16", "add", (32, 128), 2, "tma"),        # two-stage ring: 3 CTAs of 160
+    ("exp_16384x16384_bf16", "exp", (64, 64), 4, "tma"),         # small sqrt / exp stages
+    ("exp_16384x16384_bf16", "mul", (64, 128), 4, "tma_mixed"),  # mixed add / mul: 1 CTA of 256
+    ("fma_128x1048576_f32", "fma", (8, 128), 2, "tma"),          # two-stage ring: 6 CTAs of 64
+    ("fma_128x1048576_f32", "add", (8, 128), 4, "tma"),          # add / mul on a long stream
+    ("fma_128x1048576_f32", "fma", (8, 128), 6, "tma_mixed"),    # mixed fma: every CTA that fits
+])
+def test_planner_launch_shapes_at_full_size(tsx, name, op, box, stages, variant):
+    """The launch shapes the planner's rules choose on long streams, on the
+    full-size inputs, every element against the oracle."""
+    from dataclasses import replace
+
+    w = replace(ti.WORKLOADS[name], op=op, box_rows=box[0], box_cols=box[1])
+    ins = _full_inputs(w)
+    want = oracle.ewise_parallel(op, w.dtype, *ins)
+    dev = [to_dev(x, w.dtype) for x in ins]
+    with tsx.Plan(w.dtype, w.rows, w.cols, box=box, stages=stages, variant=variant) as plan:
+        out = torch.zeros_like(dev[0])
+        plan.ewise(op, *dev, out=out)
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+        info = plan.info(op)
+    bad, first = oracle.count_mismatches(op, w.dtype, bits_of(out, w.dtype), want)
+    assert bad == 0, f"{name} {op} {box} S={stages} {variant} ({info['ctas_per_sm']} CTAs of " \
+                     f"{info['threads']}): {bad} of {w.elems} elements differ, first at {first}"
