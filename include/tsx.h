@@ -329,6 +329,28 @@ int tsx_ewise(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const vo
 int tsx_reduce_rows(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, float *row_sums,
                     tsx_stream_t stream);
 
+/* Measure the op's launch on the caller's own operands under a set of
+ * candidate shapes, and keep the fastest for the plan's later tsx_ewise
+ * calls of that op.  The candidates are the planner's own launch and
+ * 1..8 CTAs per SM, each set sharing 256 or 512 compute threads per SM.
+ * Source: the measurement side of the library's specification, which
+ * chooses a launch from measured throughput; the pages fix none.  Each
+ * candidate is launched once, then timed over `launches` launches (<= 0:
+ * 10; at most 1000) with CUDA events on `stream`, in two rounds; the
+ * shortest round wins.  Results never depend on the shape, so `out` ends
+ * holding op(a, b, c).  Because the op runs repeatedly, `out` must not alias
+ * an input (TSX_ERR_INVALID), and TSX_ACCUMULATE is rejected
+ * (TSX_ERR_INVALID).  Row sums are not tuned.  A plan created with
+ * tsx_tuning.threads or ctas_per_sm keeps that shape and launches once.  A
+ * traced plan is not tuned (TSX_ERR_UNSUPPORTED).  Synchronizes `stream`, so
+ * it cannot be captured into a graph; the calls after it can.  Returns what
+ * tsx_ewise would for the arguments, TSX_ERR_TIMEOUT if a launch's
+ * device-side wait gave up (the status word is then cleared), or
+ * TSX_ERR_CUDA for a CUDA error.  `chosen` may be NULL; otherwise it
+ * receives the launch kept, as tsx_plan_get_info gives it. */
+int tsx_plan_tune(tsx_plan_t plan, tsx_op op, const void *a, const void *b, const void *c, void *out,
+                  tsx_stream_t stream, int32_t launches, tsx_plan_info *chosen);
+
 /* Release the plan, its tensor-map cache and its device status word.
  * Source: the library's specified call list (no counterpart on the pages;
  * the post-epilogue's mbarrier.inval of nvFuser PR #2833 "Loop Structure"

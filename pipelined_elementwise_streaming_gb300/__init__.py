@@ -113,6 +113,9 @@ def _load():
     L.tsx_plan_get_info.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(tsx_plan_info)]
     L.tsx_reduce_rows.restype = ctypes.c_int
     L.tsx_reduce_rows.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5
+    L.tsx_plan_tune.restype = ctypes.c_int
+    L.tsx_plan_tune.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5 + \
+                               [ctypes.c_int32, ctypes.POINTER(tsx_plan_info)]
     L.tsx_ewise_noalloc.restype = ctypes.c_int
     L.tsx_ewise_noalloc.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5 + \
@@ -147,6 +150,7 @@ tsx_plan_status = lib.tsx_plan_status
 tsx_plan_query = lib.tsx_plan_query
 tsx_plan_get_info = lib.tsx_plan_get_info
 tsx_reduce_rows = lib.tsx_reduce_rows
+tsx_plan_tune = lib.tsx_plan_tune
 # The plan-free, allocation-free form of tsx_ewise (device status word in a
 # static device array; see include/tsx.h for who needs it and its limits).
 tsx_ewise_noalloc = lib.tsx_ewise_noalloc
@@ -269,6 +273,25 @@ class Plan:
         if rc != TSX_OK:
             raise TsxError(rc, tsx_last_error())
         return out
+
+    def tune(self, op: str, a, b=None, c=None, out=None, launches: int = 10, stream=None) -> dict:
+        """Time the op's candidate launch shapes on these operands and keep
+        the fastest for the plan's later calls of `op` (tsx_plan_tune; out
+        must not alias an input and ends holding op(a, b, c)).  Returns the
+        launch kept, as info() gives it."""
+        import torch
+
+        if out is None:
+            out = torch.empty_like(a) if self.pitch == self.cols else \
+                torch.empty(self.rows, self.pitch, dtype=a.dtype, device=a.device)[:, : self.cols]
+        pa, pb, pc, po = (self._check(a, "a"), self._check(b, "b"), self._check(c, "c"), self._check(out, "out"))
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        info = tsx_plan_info()
+        rc = tsx_plan_tune(self.handle, _code(OPS, op), pa, pb, pc, po, s.cuda_stream, int(launches),
+                           ctypes.byref(info))
+        if rc != TSX_OK:
+            raise TsxError(rc, tsx_last_error())
+        return info.as_dict()
 
     def status(self) -> int:
         """Device-side status since the last call (reads and clears it)."""

@@ -474,6 +474,121 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
 
 }  // namespace
 
+namespace {
+
+// Candidate launch shapes of tsx_plan_tune: the planner's (0, 0), then
+// 1..8 CTAs per SM sharing 256 or 512 compute threads per SM.
+int tune_candidates(int (*out)[2])
+{
+    int n = 0;
+    out[n][0] = 0;
+    out[n][1] = 0;
+    ++n;
+    for (int ctas = 1; ctas <= 8; ++ctas)
+        for (int total : {256, 512}) {
+            int threads = total / ctas / 32 * 32;
+            threads = threads < 32 ? 32 : threads;
+            bool seen = false;
+            for (int k = 1; k < n; ++k)
+                seen = seen || (out[k][0] == ctas && out[k][1] == threads);
+            if (!seen) {
+                out[n][0] = ctas;
+                out[n][1] = threads;
+                ++n;
+            }
+        }
+    return n;
+}
+
+// Time every candidate shape of `op` (two rounds of `reps` launches each,
+// the shortest round counts) and leave the fastest in the plan's slot.  The
+// plan's knobs select a candidate while it is set up; the caller restores
+// them.  Shapes that cannot be resident are skipped.
+int tune_launch(tsx_plan* p, tsx_op op_arg, const void* a, const void* b, const void* c, void* out,
+                tsx_stream_t stream, int reps)
+{
+    const int op = int(op_arg);
+    tsx_plan::OpLaunch& slot = p->ops[op];
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int cand[24][2];
+    const int n = tune_candidates(cand);
+    tsx_plan::OpLaunch launch[24];
+    bool usable[24] = {};
+    float best_ms[24];
+    for (float& x : best_ms)
+        x = -1.f;
+    const tsx_plan::OpLaunch planner = slot;
+    const Knobs saved = p->g.knobs;
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    cudaError_t e = cudaEventCreate(&ev[0]);
+    if (e == cudaSuccess)
+        e = cudaEventCreate(&ev[1]);
+    int rc = e == cudaSuccess ? TSX_OK : cuda_error(e, "cudaEventCreate");
+    // set up each candidate once (a launch); keep the distinct shapes
+    for (int k = 0; k < n && rc == TSX_OK; ++k) {
+        if (k == 0) {
+            slot = planner;
+        } else {
+            p->g.knobs = saved;
+            p->g.knobs.ctas_per_sm = cand[k][0];
+            p->g.knobs.threads = cand[k][1];
+            slot.ready = false;
+        }
+        const int r = tsx_ewise(p, op_arg, a, b, c, out, stream);
+        if (r == TSX_ERR_UNSUPPORTED)
+            continue;   // this shape does not fit
+        if (r != TSX_OK) {
+            rc = r;
+            break;
+        }
+        bool dup = false;
+        for (int j = 0; j < k; ++j)
+            dup = dup || (usable[j] && launch[j].ctas_per_sm == slot.ctas_per_sm &&
+                          launch[j].og.threads == slot.og.threads);
+        launch[k] = slot;
+        usable[k] = !dup;
+    }
+    // two rounds over the distinct shapes, each timed over `reps` launches
+    for (int round = 0; round < 2 && rc == TSX_OK; ++round)
+        for (int k = 0; k < n && rc == TSX_OK; ++k) {
+            if (!usable[k])
+                continue;
+            slot = launch[k];
+            e = cudaEventRecord(ev[0], st);
+            for (int i = 0; i < reps && e == cudaSuccess && rc == TSX_OK; ++i)
+                rc = tsx_ewise(p, op_arg, a, b, c, out, stream);
+            if (e == cudaSuccess && rc == TSX_OK)
+                e = cudaEventRecord(ev[1], st);
+            if (e == cudaSuccess && rc == TSX_OK)
+                e = cudaEventSynchronize(ev[1]);
+            float ms = 0.f;
+            if (e == cudaSuccess && rc == TSX_OK)
+                e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
+            if (e != cudaSuccess && rc == TSX_OK)
+                rc = cuda_error(e, "timing a candidate launch");
+            if (rc == TSX_OK && (best_ms[k] < 0.f || ms < best_ms[k]))
+                best_ms[k] = ms;
+        }
+    for (cudaEvent_t x : ev)
+        if (x)
+            cudaEventDestroy(x);
+    p->g.knobs = saved;
+    int pick = 0;
+    for (int k = 1; k < n; ++k)
+        if (usable[k] && best_ms[k] >= 0.f && (best_ms[pick] < 0.f || best_ms[k] < best_ms[pick]))
+            pick = k;
+    slot = usable[pick] ? launch[pick] : planner;
+    slot.ready = true;
+    if (rc != TSX_OK)
+        return rc;
+    const int s = read_status(p, true);
+    if (s != TSX_OK)
+        return set_error(s, "a device-side wait gave up while tuning");
+    return TSX_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 tsx_plan_t tsx_plan_create(tsx_dtype dtype, int64_t rows, int64_t cols, int box_rows, int box_cols, int stages,
@@ -771,6 +886,44 @@ int tsx_ewise(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const v
         const int s = read_status(p, true);
         if (s != TSX_OK)
             return set_error(s, "a device-side wait gave up");
+    }
+    set_last_error("");
+    return TSX_OK;
+}
+
+int tsx_plan_tune(tsx_plan_t p, tsx_op op_arg, const void* a, const void* b, const void* c, void* out,
+                  tsx_stream_t stream, int32_t launches, tsx_plan_info* chosen)
+{
+    if (!p)
+        return set_error(TSX_ERR_INVALID, "NULL plan");
+    int op;
+    bool accumulate;
+    if (!split_op(op_arg, &op, &accumulate))
+        return set_error(TSX_ERR_INVALID, "unknown op");
+    if (accumulate)
+        return set_error(TSX_ERR_INVALID, "tuning runs the op repeatedly: TSX_ACCUMULATE is not tuned");
+    if (out && (out == a || out == b || out == c))
+        return set_error(TSX_ERR_INVALID, "tuning runs the op repeatedly: out must not alias an input");
+    if (p->trace_cap > 0)
+        return set_error(TSX_ERR_UNSUPPORTED, "a traced plan is not tuned");
+    const int reps = launches <= 0 ? 10 : launches > 1000 ? 1000 : launches;
+    // the planner's launch first: it checks the arguments and sets up the op
+    int rc = tsx_ewise(p, op_arg, a, b, c, out, stream);
+    if (rc != TSX_OK)
+        return rc;
+    tsx_plan::OpLaunch& slot = p->ops[op];
+    const Knobs saved = p->g.knobs;
+    if (p->g.tiles > 0 && saved.threads <= 0 && saved.ctas_per_sm <= 0) {
+        rc = tune_launch(p, op_arg, a, b, c, out, stream, reps);
+        p->g.knobs = saved;
+        if (rc != TSX_OK)
+            return rc;
+    }
+    if (chosen) {
+        fill_info(p->g, slot.og, chosen);
+        chosen->ctas_per_sm = slot.ctas_per_sm;
+        chosen->grid = slot.grid;
+        chosen->sm_count = p->sm_count;
     }
     set_last_error("");
     return TSX_OK;

@@ -37,7 +37,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("tsx_plan_create", "tsx_ewise", "tsx_plan_destroy", "tsx_plan_status", "tsx_last_error",
-                     "tsx_reduce_rows", "tsx_ewise_noalloc", "tsx_debug_trace"):
+                     "tsx_reduce_rows", "tsx_ewise_noalloc", "tsx_plan_tune", "tsx_debug_trace"):
         assert required in names
 
 
@@ -50,6 +50,14 @@ def test_library_exports_every_declared_symbol(tsx):
 def test_binding_uses_the_c_names(tsx):
     for n in _declared_functions():
         assert hasattr(tsx, n), n
+
+
+def test_calls_on_a_null_plan_are_invalid(tsx):
+    """Host-side argument checks that need no GPU."""
+    info = tsx.tsx_plan_info()
+    assert tsx.tsx_plan_tune(None, 0, None, None, None, None, None, 10, ctypes.byref(info)) == tsx.TSX_ERR_INVALID
+    assert tsx.tsx_ewise(None, 0, None, None, None, None, None) == tsx.TSX_ERR_INVALID
+    assert tsx.tsx_plan_get_info(None, 0, ctypes.byref(info)) == tsx.TSX_ERR_INVALID
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
