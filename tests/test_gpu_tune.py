@@ -44,6 +44,7 @@ def _candidates():
     ("f32", 257, 8200, (8, 128), 6, "tma_mixed", "mul"),
     ("bf16", 513, 8192, (64, 64), 3, "tma", "copy"),
     ("f32", 300, 4096, (16, 64), 2, "ldgsts", "sqrt"),
+    ("f32", 70, 8192, (8, 512), 2, "tma_promoted", "exp"),
 ])
 def test_tune_keeps_a_candidate_and_exact_results(tsx, dtype, rows, cols, box, stages, variant, op):
     ins = _inputs(dtype, op, rows, cols, "main")
