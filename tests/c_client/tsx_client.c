@@ -7,7 +7,8 @@
  *   3. on a GPU, an fp32 fma over a ragged [rows, cols] tensor equals the C
  *      library's fmaf element by element (fmaf rounds a * b + c once, as
  *      the operation is defined), and the plan's status stays TSX_OK;
- *   4. tsx_ewise_noalloc gives the same bits;
+ *   4. tsx_ewise_noalloc gives the same bits, and so does the launch shape
+ *      tsx_plan_tune keeps;
  *   5. row sums of small integers are exact.
  *
  * Usage: tsx_client [--no-gpu].  Prints one line per check and exits 0 when
@@ -102,6 +103,19 @@ static void gpu_checks(void)
           "tsx_ewise_noalloc");
     cudaMemcpy(h_na, d[3], bytes, cudaMemcpyDeviceToHost);
     check(memcmp(h_na, h[3], bytes) == 0, "noalloc equals tsx_ewise bit for bit");
+
+    /* the launch shape tsx_plan_tune keeps gives the same bits */
+    tsx_plan_info chosen;
+    memset(&chosen, 0, sizeof chosen);
+    cudaMemset(d[3], 0xA5, bytes);
+    check(tsx_plan_tune(plan, TSX_FMA, d[0], d[1], d[2], d[3], NULL, 2, &chosen) == TSX_OK && chosen.ctas_per_sm >= 1,
+          "tsx_plan_tune");
+    cudaMemset(d[3], 0x5A, bytes);
+    check(tsx_ewise(plan, TSX_FMA, d[0], d[1], d[2], d[3], NULL) == TSX_OK, "tsx_ewise after tuning");
+    cudaMemcpy(h_na, d[3], bytes, cudaMemcpyDeviceToHost);
+    check(memcmp(h_na, h[3], bytes) == 0, "tuned launch equals the planner's bit for bit");
+    check(tsx_plan_tune(plan, TSX_FMA, d[3], d[1], d[2], d[3], NULL, 2, NULL) == TSX_ERR_INVALID,
+          "tuning with out aliasing an input is an error");
     free(h_na);
 
     /* row sums of small integers are exact in fp32 whatever the order */
