@@ -79,6 +79,20 @@ int default_threads(const Geometry& g, int op, size_t smem_bytes, uint32_t units
 // and reach a stage from one operand only).
 static bool one_operand_compute(int op) { return op == TSX_SQRT || op == TSX_EXP; }
 
+// Groups of a tile's boxes that the compute warps hand to the store warps
+// one by one (TMA variants).  Two need a compute step, an even box count and
+// every operand staged; measured on GB300, the one-operand sqrt and exp gain
+// 1-4 % with tiles of 16 KB or more, while ops with two or three operands,
+// and small tiles, lose.
+static int compute_groups_of(const Geometry& g, int op)
+{
+    const int boxes = g.variant == TSX_TMA_RANK3 ? g.row_chunks : g.row_chunks * g.atoms;
+    const bool can_split = op != TSX_COPY && boxes % 2 == 0 && !(g.variant == TSX_TMA_MIXED && op_arity(op) >= 2);
+    const bool split_pays = one_operand_compute(op) && g.slot_bytes >= 16384;
+    const bool split = g.knobs.store_split == 2 || (g.knobs.store_split == 0 && split_pays);
+    return can_split && split ? 2 : 1;
+}
+
 // Stage bytes per SM that a two-stage ring aims at: copy, add and mul 96 KB,
 // the one-operand sqrt and exp 128 KB, fma 144 KB (make_op_geometry).
 static int64_t two_stage_ring_per_sm(int op)
@@ -115,9 +129,14 @@ StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes)
     // have read shared memory; with two store warps taking tiles in turn, a
     // warp can wait for its own store (lag 0) while the other stores the
     // next tile.  Measured on GB300 (all settings give identical results):
-    //  - 2 stages: two store warps, lag 0, for every op: with one warp the
-    //    ring holds a stage back for a whole tile (bf16 exp [16384, 16384]
-    //    4298 -> 5893 GB/s, fp32 fma [128, 2^20] 6690 -> 7135);
+    //  - 2 stages: two store warps, lag 0: with one warp the ring holds a
+    //    stage back for a whole tile (bf16 exp [16384, 16384] 4298 -> 5893
+    //    GB/s, fp32 fma [128, 2^20] 6690 -> 7135).  Except where sqrt or
+    //    exp stores tiles of 32 KB or more in two groups: there one warp at
+    //    lag 0 streams faster (bf16 exp [16384, 16384] in 128x128 tiles 6261
+    //    -> 6459, bf16 sqrt 6396 -> 6462; with 16 KB tiles it was mixed,
+    //    bf16 exp in 64x128 tiles -5.6 %, fp32 exp and sqrt in 16x256 tiles
+    //    +3.4 and +4.6 %);
     //  - 3 to 5 stages: one store warp, lag 1 (bf16 exp 6457 against 5763
     //    at lag 0; fp32 fma 7160 at 4 stages against 6827), except that the
     //    one-operand ops sqrt and exp with stages of 16 KB or more take two
@@ -133,7 +152,8 @@ StoreSchedule store_schedule(const Geometry& g, int op, uint32_t stage_bytes)
     const bool one_operand = one_operand_compute(op);
     StoreSchedule r;
     if (S <= 2) {
-        r.store_warps = 2;
+        const bool large_split = one_operand && S == 2 && g.slot_bytes >= 32768 && compute_groups_of(g, op) == 2;
+        r.store_warps = large_split ? 1 : 2;
         r.store_lag = 0;
     } else if (S < 6) {
         r.store_warps = one_operand && S >= 4 && stage_bytes >= 16384 ? 2 : 1;
@@ -381,16 +401,7 @@ int make_op_geometry(const Geometry& g, int op, int max_smem, OpGeometry* og, st
         og->tile_order = op == TSX_COPY ? (g.knobs.tile_order > 0 ? g.knobs.tile_order : 2) : 1;
         const int share = g.slot_bytes >= kDynamicAllTileBytes ? 100 : 25;
         og->dynamic_share = og->tile_order == 2 ? (g.knobs.dynamic_share > 0 ? g.knobs.dynamic_share : share) : 0;
-        // two groups of boxes need a compute step, an even box count and
-        // all operands staged
-        const int boxes = g.variant == TSX_TMA_RANK3 ? g.row_chunks : g.row_chunks * g.atoms;
-        const bool can_split = op != TSX_COPY && boxes % 2 == 0 && !(g.variant == TSX_TMA_MIXED && og->n_in >= 2);
-        // measured on GB300: the one-operand sqrt and exp gain 1-4 % with
-        // tiles of 16 KB or more; ops with two or three operands, and small
-        // tiles, lose
-        const bool split_pays = (op == TSX_SQRT || op == TSX_EXP) && g.slot_bytes >= 16384;
-        const bool split = g.knobs.store_split == 2 || (g.knobs.store_split == 0 && split_pays);
-        og->compute_groups = can_split && split ? 2 : 1;
+        og->compute_groups = compute_groups_of(g, op);
     }
     // every CTA that fits, unless forced or capped by a rule below
     og->ctas_cap = g.knobs.ctas_per_sm > 0 ? g.knobs.ctas_per_sm : 0;

@@ -263,7 +263,8 @@ def test_query_store_warps_never_exceed_the_stages(tsx):
     # (store warps, lag, wait style: 1 every lane, 2 lane 0)
     ("fma", 2, (32, 128), (2, 0, 1)), ("fma", 3, (32, 128), (1, 1, 1)), ("fma", 4, (32, 128), (1, 1, 1)),
     ("fma", 6, (32, 128), (1, 2, 1)),
-    ("exp", 2, (128, 128), (2, 0, 2)), ("exp", 3, (128, 128), (1, 1, 2)), ("exp", 4, (128, 128), (2, 0, 2)),
+    ("exp", 2, (128, 128), (1, 0, 2)),         # 32 KB tiles stored in two groups: one warp
+    ("exp", 2, (64, 128), (2, 0, 2)), ("exp", 3, (128, 128), (1, 1, 2)), ("exp", 4, (128, 128), (2, 0, 2)),
     ("exp", 4, (32, 128), (1, 1, 2)),         # stages under 16 KB keep lag 1
     ("exp", 8, (32, 128), (1, 2, 2)), ("sqrt", 4, (128, 128), (2, 0, 2)),
     ("copy", 2, (32, 128), (2, 0, 1)), ("copy", 4, (128, 128), (1, 1, 1)), ("mul", 3, (32, 128), (1, 1, 1)),
