@@ -332,7 +332,9 @@ int tsx_reduce_rows(tsx_plan_t plan, tsx_op op, const void *a, const void *b, co
 /* Measure the op's launch on the caller's own operands under a set of
  * candidate shapes, and keep the fastest for the plan's later tsx_ewise
  * calls of that op.  The candidates are the planner's own launch and
- * 1..8 CTAs per SM, each set sharing 256 or 512 compute threads per SM.
+ * 1..8 CTAs per SM, each set sharing 256 or 512 compute threads per SM;
+ * then, on the TMA variants, the fastest of those with one or two store
+ * warps at lag 0 or 1 (unless the plan's knobs fix the store side).
  * Source: the measurement side of the library's specification, which
  * chooses a launch from measured throughput; the pages fix none.  Each
  * candidate is launched once, then timed over `launches` launches (<= 0:

@@ -476,64 +476,58 @@ int prepare_rowsum(tsx_plan* p, int op, tsx_plan::OpLaunch** out)
 
 namespace {
 
-// Candidate launch shapes of tsx_plan_tune: the planner's (0, 0), then
-// 1..8 CTAs per SM sharing 256 or 512 compute threads per SM.
-int tune_candidates(int (*out)[2])
+// A launch candidate of tsx_plan_tune: knob values (0 / -1: the planner's).
+struct TuneKnobs {
+    int ctas_per_sm, threads, store_warps, store_lag;
+};
+
+// The first pass: the planner's launch, then 1..8 CTAs per SM sharing 256
+// or 512 compute threads per SM (the store side as the plan's knobs say).
+int shape_candidates(const Knobs& base, TuneKnobs* out)
 {
     int n = 0;
-    out[n][0] = 0;
-    out[n][1] = 0;
-    ++n;
+    out[n++] = {0, 0, base.store_warps, base.store_lag};
     for (int ctas = 1; ctas <= 8; ++ctas)
         for (int total : {256, 512}) {
             int threads = total / ctas / 32 * 32;
             threads = threads < 32 ? 32 : threads;
             bool seen = false;
             for (int k = 1; k < n; ++k)
-                seen = seen || (out[k][0] == ctas && out[k][1] == threads);
-            if (!seen) {
-                out[n][0] = ctas;
-                out[n][1] = threads;
-                ++n;
-            }
+                seen = seen || (out[k].ctas_per_sm == ctas && out[k].threads == threads);
+            if (!seen)
+                out[n++] = {ctas, threads, base.store_warps, base.store_lag};
         }
     return n;
 }
 
-// Time every candidate shape of `op` (two rounds of `reps` launches each,
-// the shortest round counts) and leave the fastest in the plan's slot.  The
-// plan's knobs select a candidate while it is set up; the caller restores
-// them.  Shapes that cannot be resident are skipped.
-int tune_launch(tsx_plan* p, tsx_op op_arg, const void* a, const void* b, const void* c, void* out,
-                tsx_stream_t stream, int reps)
+// Set up every candidate (one launch each, distinct launches only), time
+// the distinct ones over two rounds of `reps` launches (the shortest round
+// counts), and return the fastest's index in `launch` (-1 if none ran).
+// The plan's knobs select a candidate while it is set up; the caller
+// restores them.  Shapes that cannot be resident are skipped.
+int time_candidates(tsx_plan* p, tsx_op op_arg, const void* a, const void* b, const void* c, void* out,
+                    tsx_stream_t stream, int reps, const TuneKnobs* cand, int n, tsx_plan::OpLaunch* launch,
+                    const Knobs& base, int* pick)
 {
-    const int op = int(op_arg);
-    tsx_plan::OpLaunch& slot = p->ops[op];
+    tsx_plan::OpLaunch& slot = p->ops[int(op_arg)];
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    int cand[24][2];
-    const int n = tune_candidates(cand);
-    tsx_plan::OpLaunch launch[24];
     bool usable[24] = {};
     float best_ms[24];
     for (float& x : best_ms)
         x = -1.f;
-    const tsx_plan::OpLaunch planner = slot;
-    const Knobs saved = p->g.knobs;
+    *pick = -1;
     cudaEvent_t ev[2] = {nullptr, nullptr};
     cudaError_t e = cudaEventCreate(&ev[0]);
     if (e == cudaSuccess)
         e = cudaEventCreate(&ev[1]);
     int rc = e == cudaSuccess ? TSX_OK : cuda_error(e, "cudaEventCreate");
-    // set up each candidate once (a launch); keep the distinct shapes
     for (int k = 0; k < n && rc == TSX_OK; ++k) {
-        if (k == 0) {
-            slot = planner;
-        } else {
-            p->g.knobs = saved;
-            p->g.knobs.ctas_per_sm = cand[k][0];
-            p->g.knobs.threads = cand[k][1];
-            slot.ready = false;
-        }
+        p->g.knobs = base;
+        p->g.knobs.ctas_per_sm = cand[k].ctas_per_sm;
+        p->g.knobs.threads = cand[k].threads;
+        p->g.knobs.store_warps = cand[k].store_warps;
+        p->g.knobs.store_lag = cand[k].store_lag;
+        slot.ready = false;
         const int r = tsx_ewise(p, op_arg, a, b, c, out, stream);
         if (r == TSX_ERR_UNSUPPORTED)
             continue;   // this shape does not fit
@@ -544,11 +538,11 @@ int tune_launch(tsx_plan* p, tsx_op op_arg, const void* a, const void* b, const 
         bool dup = false;
         for (int j = 0; j < k; ++j)
             dup = dup || (usable[j] && launch[j].ctas_per_sm == slot.ctas_per_sm &&
-                          launch[j].og.threads == slot.og.threads);
+                          launch[j].og.threads == slot.og.threads && launch[j].og.store_warps == slot.og.store_warps &&
+                          launch[j].og.store_lag == slot.og.store_lag);
         launch[k] = slot;
         usable[k] = !dup;
     }
-    // two rounds over the distinct shapes, each timed over `reps` launches
     for (int round = 0; round < 2 && rc == TSX_OK; ++round)
         for (int k = 0; k < n && rc == TSX_OK; ++k) {
             if (!usable[k])
@@ -572,12 +566,42 @@ int tune_launch(tsx_plan* p, tsx_op op_arg, const void* a, const void* b, const 
     for (cudaEvent_t x : ev)
         if (x)
             cudaEventDestroy(x);
-    p->g.knobs = saved;
-    int pick = 0;
-    for (int k = 1; k < n; ++k)
-        if (usable[k] && best_ms[k] >= 0.f && (best_ms[pick] < 0.f || best_ms[k] < best_ms[pick]))
-            pick = k;
-    slot = usable[pick] ? launch[pick] : planner;
+    for (int k = 0; k < n; ++k)
+        if (usable[k] && best_ms[k] >= 0.f && (*pick < 0 || best_ms[k] < best_ms[*pick]))
+            *pick = k;
+    return rc;
+}
+
+// tsx_plan_tune's search: the CTA and thread shapes first, then, unless the
+// plan's knobs fix it, the store side (one or two store warps, lag 0 or 1)
+// on the fastest shape.  The fastest launch stays in the plan's slot.
+int tune_launch(tsx_plan* p, tsx_op op_arg, const void* a, const void* b, const void* c, void* out,
+                tsx_stream_t stream, int reps)
+{
+    tsx_plan::OpLaunch& slot = p->ops[int(op_arg)];
+    const tsx_plan::OpLaunch planner = slot;
+    const Knobs base = p->g.knobs;
+    TuneKnobs cand[24];
+    tsx_plan::OpLaunch launch[24];
+    int n = shape_candidates(base, cand);
+    int pick = -1;
+    int rc = time_candidates(p, op_arg, a, b, c, out, stream, reps, cand, n, launch, base, &pick);
+    tsx_plan::OpLaunch best = pick >= 0 ? launch[pick] : planner;
+    if (rc == TSX_OK && pick >= 0 && is_tma_variant(p->g.variant) && base.store_warps <= 0 && base.store_lag < 0) {
+        // the store side on the fastest shape (the shape itself first)
+        const TuneKnobs shape = {best.ctas_per_sm, best.og.threads, best.og.store_warps, best.og.store_lag};
+        n = 0;
+        cand[n++] = shape;
+        for (int w = 1; w <= 2; ++w)
+            for (int lag = 0; lag <= 1; ++lag)
+                if (w != shape.store_warps || lag != shape.store_lag)
+                    cand[n++] = {shape.ctas_per_sm, shape.threads, w, lag};
+        rc = time_candidates(p, op_arg, a, b, c, out, stream, reps, cand, n, launch, base, &pick);
+        if (pick >= 0)
+            best = launch[pick];
+    }
+    p->g.knobs = base;
+    slot = best;
     slot.ready = true;
     if (rc != TSX_OK)
         return rc;

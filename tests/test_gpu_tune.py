@@ -94,6 +94,12 @@ def test_tune_keeps_a_forced_shape(tsx):
         torch.cuda.synchronize()
         assert plan.status() == tsx.TSX_OK
     assert (chosen["threads"], chosen["ctas_per_sm"]) == (before["threads"], before["ctas_per_sm"]) == (96, 2)
+    # a forced store side is kept while the shape is tuned
+    with tsx.Plan("bf16", rows, cols, box=(32, 128), stages=3, tuning={"store_warps": 2, "store_lag": 0}) as plan:
+        chosen = plan.tune("exp", to_dev(ins[0], "bf16"), launches=2)
+        torch.cuda.synchronize()
+        assert plan.status() == tsx.TSX_OK
+    assert (chosen["store_warps"], chosen["store_lag"]) == (2, 0)
 
 
 def test_tuned_launch_in_a_cuda_graph(tsx):
